@@ -1,0 +1,297 @@
+"""fp64 CPU oracle for the single-GPU MoE-layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only the test suite, `__graft_entry__.smoke()` and the
+CPU-baseline / reference arm of `bench.py` use it.  It shares no code with the
+CUDA library (no headers, helpers, tables or generators); both sides are fed by
+the seeded generators in `mixture_experts_layer_93_b300/inputs.py`, which hold
+none of the method's arithmetic.
+
+What it computes is the plain definition of an MoE layer forward, written out
+step by step in fp64 with numpy (matmul, lexsort and exp are the only library
+primitives used):
+
+  1. gate network: router logits L = x Wr (+ b)
+        ("MoE架构的物理瓶颈与扩展限制解析", section 工作原理, moe_forward
+        pseudocode, step 1; "硬件加速的考量", section 自定义核与核融合, step 1)
+  2. top-k expert selection per token
+        (same pseudocode, `top_k(router_logits)`; 自定义核与核融合 step 2)
+  3. gather/permutation: rows grouped per expert so each expert's tokens are
+     contiguous ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化", section
+     技术细节 / Gather 与加载融合, the "contiguous packed input" mode)
+  4. expert SwiGLU FFN (section 关键 Kernel 对比, row "SwiGLU 融合";
+     自定义核与核融合 step 4)
+  5. gate-score-weighted combine (自定义核与核融合 step 5)
+  6. optional token rounding of each expert's token count to a tile multiple
+     (SonicMoE page, section "3. Token Rounding 路由算法")
+
+Readings of the pages (where they are silent or at odds):
+  * Selection precision: a top-k choice is taken on fp32 logits (the kernel's
+    precision); the fp64 logits are rounded to fp32 before ranking.  Gate
+    weights are the fp64 softmax over the selected logits.
+  * Ties in top-k go to the lower expert id; -0.0 equals +0.0.
+  * Gate weights: softmax over the k selected logits (renormalised), which
+    is the same function as softmax-over-all-then-top-k-then-renormalise.
+  * SwiGLU: h = silu(x W1) * (x W3), silu(z) = z / (1 + exp(-z)); W1 is the
+    gated branch, W3 the linear one; o = h W2.
+  * Token rounding: the SonicMoE page asks for rounding "up" to a tile
+    multiple, for at most one tile of deviation from top-k, and for an
+    unchanged expected total.  Always rounding up raises the total, so the
+    default mode rounds to the NEAREST multiple (half up); "up" is kept as the
+    literal variant.  Counts are capped at tile*floor(T/tile).  When the
+    rounded count c' exceeds c, the c'-c not-yet-routed tokens with the
+    highest L[t,e] join (ties: lower t first); when c' < c, the c-c' routed
+    tokens with the lowest L[t,e] leave (ties: higher t leaves first).  Each
+    expert is rounded from the original top-k sets.  A token's final set is
+    ordered by (L desc, id asc) and weighted by softmax over that set; an empty
+    set gives y_t = 0.
+
+Pins (tests/test_oracle.py): brute-force k-subset top-k; the closed form
+w0 = sigmoid(L0 - L1) at k=2; numpy's stable argsort for the permutation;
+index-arithmetic SwiGLU on one-nonzero-per-column weights (catches a
+transposed operand); E=1,k=1 == dense FFN; identical experts == dense FFN;
+relabelling invariance; W2=0 -> 0; token-rounding invariants checked by
+brute force on tiny inputs.  No function here is unpinned.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+ROUND_OFF = "off"
+ROUND_NEAREST = "nearest"
+ROUND_UP = "up"
+
+
+def _f64(a) -> np.ndarray:
+    """bf16/fp32 torch tensor or numpy array -> fp64 numpy (exact widening)."""
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            return a.detach().to("cpu", dtype=torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(a, dtype=F64)
+
+
+# --------------------------------------------------------------------------
+# 1. gate network
+# --------------------------------------------------------------------------
+def router_logits(x, Wr, bias=None) -> np.ndarray:
+    """L[t, e] = sum_i x[t, i] * Wr[i, e] + bias[e], in fp64.
+
+    Gate network of the moe_forward pseudocode ("MoE架构的物理瓶颈与扩展限制解析",
+    section 工作原理, step 1)."""
+    L = _f64(x) @ _f64(Wr)
+    if bias is not None:
+        L = L + _f64(bias)[None, :]
+    return L
+
+
+def decision_logits(L) -> np.ndarray:
+    """The logits the selection ranks: fp32, the kernel's precision."""
+    return np.asarray(L, dtype=F64).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# 2. top-k and gate weights
+# --------------------------------------------------------------------------
+def topk(L, k: int) -> np.ndarray:
+    """idx[t, :k]: the k experts with the largest L[t, e], in descending order
+    of L; equal values are ordered by ascending expert id.  int32 [T, k].
+
+    `top_k(router_logits)` of the moe_forward pseudocode (page above, 工作原理)."""
+    L = np.asarray(L)
+    T, E = L.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    # lexsort: last key is primary -> sort by -L ascending, then by id ascending
+    order = np.lexsort((ids, -L.astype(F64)), axis=-1)
+    return order[:, :k].astype(np.int32)
+
+
+def softmax(v) -> np.ndarray:
+    v = np.asarray(v, dtype=F64)
+    if v.size == 0:
+        return v.copy()
+    z = np.exp(v - v.max())
+    return z / z.sum()
+
+
+def gate_weights(L, idx) -> np.ndarray:
+    """w[t, j] = softmax over the selected logits L[t, idx[t, :]] (renormalised
+    gating), fp64 [T, k]."""
+    L = np.asarray(L, dtype=F64)
+    Ls = np.take_along_axis(L, np.asarray(idx, dtype=np.int64), axis=1)
+    z = np.exp(Ls - Ls.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+# --------------------------------------------------------------------------
+# 3. permutation (stable grouping of assignments by expert)
+# --------------------------------------------------------------------------
+def permute(idx, E: int):
+    """Group the A = T*k assignments a = t*k + j by expert, stably.
+
+    Returns (counts[E], offsets[E+1], src[A], dst[A]) as int64 arrays, with
+    src[row] = a (rows of expert e are offsets[e]..offsets[e+1]-1, in ascending
+    a) and dst[a] = row."""
+    flat = np.asarray(idx).reshape(-1)
+    groups = [np.flatnonzero(flat == e) for e in range(E)]
+    counts = np.array([g.size for g in groups], dtype=np.int64)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    src = np.concatenate(groups).astype(np.int64) if groups else np.zeros(0, np.int64)
+    dst = np.empty_like(src)
+    dst[src] = np.arange(src.size)
+    return counts, offsets, src, dst
+
+
+# --------------------------------------------------------------------------
+# 6. token rounding
+# --------------------------------------------------------------------------
+def rounded_count(c: int, tile: int, mode: str, T: int) -> int:
+    """Per-expert token count after rounding to a multiple of `tile`."""
+    if mode == ROUND_OFF:
+        return int(c)
+    if mode == ROUND_NEAREST:
+        c2 = tile * ((c + tile // 2) // tile)
+    elif mode == ROUND_UP:
+        c2 = tile * (-(-c // tile))
+    else:
+        raise ValueError(mode)
+    return int(min(c2, tile * (T // tile)))
+
+
+def token_round(L, idx, tile: int, mode: str):
+    """Token rounding (SonicMoE page, "3. Token Rounding 路由算法").
+
+    Returns a dict with
+      member  [T, E] bool   final membership
+      counts  [E]           rounded counts (multiples of tile)
+      sets    list of T int arrays: each token's experts, (L desc, id asc)
+      added / dropped: per-expert arrays of token ids
+    L is the fp32 decision matrix (ranked in fp64, which is exact for fp32)."""
+    L = np.asarray(L, dtype=F64)
+    T, E = L.shape
+    idx = np.asarray(idx)
+    member = np.zeros((T, E), dtype=bool)
+    member[np.repeat(np.arange(T), idx.shape[1]), idx.reshape(-1)] = True
+    final = member.copy()
+    counts0 = member.sum(axis=0)
+    added, dropped = [], []
+    for e in range(E):
+        c = int(counts0[e])
+        c2 = rounded_count(c, tile, mode, T)
+        add = np.zeros(0, np.int64)
+        drop = np.zeros(0, np.int64)
+        if c2 > c:
+            cand = np.flatnonzero(~member[:, e])
+            order = np.lexsort((cand, -L[cand, e]))      # L desc, then t asc
+            add = cand[order[: c2 - c]]
+            final[add, e] = True
+        elif c2 < c:
+            routed = np.flatnonzero(member[:, e])
+            order = np.lexsort((routed, -L[routed, e]))  # best first
+            drop = routed[order[c2:]]                    # worst c-c2 leave
+            final[drop, e] = False
+        added.append(add)
+        dropped.append(drop)
+    sets = []
+    for t in range(T):
+        es = np.flatnonzero(final[t])
+        es = es[np.lexsort((es, -L[t, es]))] if es.size else es
+        sets.append(es.astype(np.int64))
+    return {"member": final, "counts": final.sum(axis=0).astype(np.int64),
+            "sets": sets, "added": added, "dropped": dropped}
+
+
+# --------------------------------------------------------------------------
+# 4. expert SwiGLU FFN
+# --------------------------------------------------------------------------
+def silu(z) -> np.ndarray:
+    z = np.asarray(z, dtype=F64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def expert_hidden(xr, W1e, W3e) -> np.ndarray:
+    """h = silu(xr W1e) * (xr W3e), fp64 [m, n]."""
+    xr = _f64(xr)
+    return silu(xr @ _f64(W1e)) * (xr @ _f64(W3e))
+
+
+def expert_out(h, W2e) -> np.ndarray:
+    """o = h W2e, fp64 [m, d]."""
+    return _f64(h) @ _f64(W2e)
+
+
+# --------------------------------------------------------------------------
+# 5. full layer forward
+# --------------------------------------------------------------------------
+def route(x, Wr, bias, k: int, tile: int = 128, mode: str = ROUND_OFF, tokens=None,
+          logits=None):
+    """Per-token expert sets and gate weights.
+
+    Without rounding only the tokens in `tokens` (all when None) are routed.
+    With rounding every token is routed (rounding couples tokens through the
+    per-expert counts) and the requested subset is returned.  `logits`, when
+    given, replaces the gate network (fp32 decision logits, e.g. synthetic).
+    Returns (tokens, sets, weights): lists of int64 / fp64 arrays."""
+    x64 = None
+    if logits is None:
+        x64 = _f64(x)
+    T = (x64.shape[0] if logits is None else np.asarray(logits).shape[0])
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    if mode == ROUND_OFF:
+        if logits is None:
+            L64 = router_logits(x64[tokens], Wr, bias)
+        else:
+            L64 = np.asarray(logits, dtype=F64)[tokens]
+        Ld = decision_logits(L64)
+        idx = topk(Ld, k)
+        w = gate_weights(L64, idx)
+        return tokens, [idx[i].astype(np.int64) for i in range(len(tokens))], [w[i] for i in range(len(tokens))]
+    L64 = router_logits(x64, Wr, bias) if logits is None else np.asarray(logits, dtype=F64)
+    Ld = decision_logits(L64)
+    idx = topk(Ld, k)
+    r = token_round(Ld, idx, tile, mode)
+    sets = [r["sets"][t] for t in tokens]
+    weights = [softmax(L64[t, s]) for t, s in zip(tokens, sets)]
+    return tokens, sets, weights
+
+
+def moe_forward(x, Wr, bias, W1, W3, W2, k: int, tile: int = 128, mode: str = ROUND_OFF,
+                tokens=None, return_routing: bool = False):
+    """y[t] = sum_{e in S_t} w_te * FFN_e(x[t]) for the requested tokens, fp64.
+
+    Dataflow of the moe_forward pseudocode ("MoE架构的物理瓶颈与扩展限制解析",
+    section 工作原理) with both all-to-all steps removed (one GPU), and the
+    five steps of the fused kernel ("硬件加速的考量", section 自定义核与核融合)."""
+    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, tokens)
+    x64 = _f64(x)
+    d = x64.shape[1]
+    y = np.zeros((len(tokens), d), dtype=F64)
+    E = W1.shape[0]
+    pos_of = {e: [] for e in range(E)}
+    w_of = {e: [] for e in range(E)}
+    for p, (s, w) in enumerate(zip(sets, weights)):
+        for e, we in zip(s, w):
+            pos_of[int(e)].append(p)
+            w_of[int(e)].append(we)
+    for e in range(E):
+        if not pos_of[e]:
+            continue
+        pos = np.array(pos_of[e], dtype=np.int64)
+        h = expert_hidden(x64[tokens[pos]], W1[e], W3[e])
+        o = expert_out(h, W2[e])
+        np.add.at(y, pos, np.array(w_of[e])[:, None] * o)
+    if return_routing:
+        return y, (tokens, sets, weights)
+    return y
+
+
+def dense_swiglu_ffn(x, W1e, W3e, W2e) -> np.ndarray:
+    """A dense (one-expert) SwiGLU FFN, the E=1/k=1 special case."""
+    return expert_out(expert_hidden(x, W1e, W3e), W2e)
