@@ -1,0 +1,426 @@
+"""Benchmark of the MoE-layer forward on B300: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixtral]
+                    [--round off|nearest|up] [--impl ours|reference]
+
+A step is one pass of the whole layer (route, permute or round, up-projection
++ SwiGLU, down-projection + gate weight, combine) over one batch of synthetic
+tokens, launched through the C ABI stage by stage with CUDA events between the
+stages (the same launches moe_forward makes), so the per-kernel durations come
+from the timed region itself.  `value` is the active-expert TFLOP/s
+(6*T*k*d*n useful FLOPs per step) summed over ranks; `tokens_per_s` and the
+fraction of the measured bf16 peak ride along.  `e2e` is the same metric
+through moe_forward with x copied from pinned host memory and y copied back
+inside the timed region.
+
+Multi-GPU: every rank runs its own replica on its own tokens (weak scaling, no
+collective on the data path); timing is the max over ranks.
+
+--impl reference times the fp64 CPU oracle (the checker the parity tests use)
+on a bounded token sample on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_layer_93_b300 import inputs as I  # noqa: E402
+
+METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- helpers
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "ours") else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        blas = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        return max(blas) if blas else 1
+    except Exception:  # pragma: no cover
+        return 1
+
+
+# ------------------------------------------------------------ oracle arm
+def oracle_sample_time(cfg, inp_host, round_mode, budget_s: float, seed: int = 0):
+    """Times the oracle (as it stands) on sampled tokens until ~budget_s of CPU
+    work; returns (tokens, seconds, description)."""
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    # size the sample from a short probe: per-token cost is dominated by
+    # widening the touched experts' weights, so grow the sample geometrically
+    n = 8 if round_mode == "off" else min(cfg.T, 64)
+    total_tok, total_s = 0, 0.0
+    while True:
+        toks = np.sort(rng.choice(cfg.T, size=min(n, cfg.T), replace=False))
+        t0 = time.perf_counter()
+        O.moe_forward(inp_host["x"], inp_host["Wr"], inp_host["bias"], inp_host["W1"], inp_host["W3"],
+                      inp_host["W2"], k=cfg.k, tile=cfg.tile, mode=round_mode, tokens=toks)
+        dt = time.perf_counter() - t0
+        total_tok += len(toks)
+        total_s += dt
+        if total_s >= budget_s:
+            break
+        if dt < budget_s / 4:
+            n = min(cfg.T, n * 2)
+    desc = (f"{total_tok} sampled tokens of the {cfg.name} workload (routing and expert FFN in fp64; "
+            f"expert weights widened per call), {total_s:.1f} s")
+    return total_tok, total_s, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    cfg = I.get_config(args.config)
+    inp = I.make_inputs(cfg, device="cpu", seed=0)
+    active_per_token = 6.0 * cfg.k * cfg.d * cfg.n
+    for _ in range(args.warmup):
+        oracle_sample_time(cfg, inp, args.round, budget_s=0.0)   # one small call each
+    times, toks = [], 0
+    budget = max(1.0, args.reference_seconds / max(args.steps, 1))
+    for i in range(args.steps):
+        nt, dt, desc = oracle_sample_time(cfg, inp, args.round, budget_s=budget, seed=100 + i)
+        times.append(dt)
+        toks += nt
+    total = sum(times)
+    tps = toks / total
+    value = tps * active_per_token / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.description, "round": args.round, "tokens_per_step": toks // args.steps},
+        "tokens_per_s": tps,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": desc, "host_cpus": os.cpu_count()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    from mixture_experts_layer_93_b300 import binding as B
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    cfg = I.get_config(args.config)
+    if args.tokens:
+        cfg = cfg.with_tokens(args.tokens)
+    mode = args.round
+    shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode)
+    inp = I.make_inputs(cfg, device=dev, seed=rank)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    inp_host = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    del inp["W1"], inp["W3"], inp["W2"]
+    torch.cuda.empty_cache()
+    x, Wr, bias = inp["x"], inp["Wr"], inp["bias"]
+    ws = B.Workspace(shape, dev)
+    lay = B.moe_workspace_layout(shape)
+    cap = B.moe_row_capacity(shape)
+    T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
+    A = T * k
+
+    def view(slot, dtype, numel):
+        off = lay[slot]
+        esz = torch.tensor([], dtype=dtype).element_size()
+        return ws.buf[off:off + numel * esz].view(dtype)
+
+    logits = view("logits", torch.float32, T * E)
+    idx = view("topk_idx", torch.int32, A)
+    w = view("topk_w", torch.float32, A)
+    counts = view("counts", torch.int32, E)
+    offsets = view("offsets", torch.int32, E + 1)
+    src = view("src", torch.int32, cap)
+    dst = view("dst", torch.int32, A)
+    row_token = view("row_token", torch.int32, cap)
+    row_w = view("row_w", torch.float32, cap)
+    tok_offsets = view("tok_offsets", torch.int32, T + 1)
+    tok_rows = view("tok_rows", torch.int32, cap)
+    h = view("h", torch.bfloat16, cap * n)
+    ys = view("ys", torch.bfloat16, cap * d)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    L = B.lib()
+    import ctypes
+    sp = ctypes.byref(shape)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    stream = torch.cuda.current_stream(dev)
+    st = ctypes.c_void_p(stream.cuda_stream)
+    stages = ["route", "permute", "up", "down", "combine"]
+    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + 1 + 1
+
+    def check(rc, what):
+        if rc != 0:
+            raise B.MoEError(rc, what)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        check(L.moe_route(sp, P(x), P(Wr), P(bias), P(logits), P(idx), P(w), ws.ptr, st), "route")
+        if ev:
+            ev[1].record(stream)
+        if mode == "off":
+            check(L.moe_permute(sp, P(idx), P(w), P(counts), P(offsets), P(src), P(dst), P(row_token), P(row_w),
+                                ws.ptr, ws.nbytes, st), "permute")
+            c_off, c_rows = None, dst
+        else:
+            check(L.moe_token_round(sp, P(logits), P(idx), P(counts), P(offsets), P(row_token), P(row_w),
+                                    P(tok_offsets), P(tok_rows), ws.ptr, ws.nbytes, st), "round")
+            c_off, c_rows = tok_offsets, tok_rows
+        if ev:
+            ev[2].record(stream)
+        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(h), 1, ws.ptr,
+                              ws.nbytes, st), "up")
+        if ev:
+            ev[3].record(stream)
+        check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,
+                                st), "down")
+        if ev:
+            ev[4].record(stream)
+        check(L.moe_combine(sp, P(ys), P(c_off), P(c_rows), P(y), st), "combine")
+        if ev:
+            ev[5].record(stream)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    B.moe_check_device_status(ws)
+
+    clocks = ClockSampler(local)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))          # L2 flush between steps (not timed)
+        step(events[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    B.moe_check_device_status(ws)
+    step_ms = [events[i][0].elapsed_time(events[i][5]) for i in range(args.steps)]
+    stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
+                for j, s in enumerate(stages)}
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    R = int(offsets[E].item())
+    active = cfg.active_flops()
+    value = world * active * args.steps / (total_ms * 1e-3) / 1e12
+    tokens_per_s = world * T * args.steps / (total_ms * 1e-3)
+
+    # ------------------------------------------------ e2e: through moe_forward, host buffers
+    x_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x.cpu())
+    y_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty_like(y)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        check(L.moe_forward(sp, P(x_dev), P(Wr), P(bias), P(W13p), P(W2p), P(y_dev), ws.ptr, ws.nbytes, st),
+              "forward")
+        y_host.copy_(y_dev, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        e2e_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    B.moe_check_device_status(ws)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
+    e2e_value = world * active * args.steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        return
+    # ------------------------------------------------ roofline of the dominant kernel (up-projection)
+    up_ms = statistics.mean(stage_ms["up"])
+    up_flops = 4.0 * R * d * n
+    up_tflops = up_flops / (up_ms * 1e-3) / 1e12
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up, SwiGLU>", "achieved": up_tflops,
+                "peak": peak_t, "unit": "TFLOP/s", "frac": up_tflops / peak_t, "traffic": None,
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "algorithmic_flops_per_launch": up_flops}
+    # HBM-bound stages: algorithmic bytes / time
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    comb_bytes = R * d * 2 + T * d * 2 + A * 4
+    comb_gbs = comb_bytes / (statistics.mean(stage_ms["combine"]) * 1e-3) / 1e9
+    down_flops = 2.0 * R * n * d
+    stage_summary = {s: round(statistics.mean(v), 4) for s, v in stage_ms.items()}
+    extra = {
+        "stage_ms": stage_summary,
+        "down_tflops": down_flops / (statistics.mean(stage_ms["down"]) * 1e-3) / 1e12,
+        "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / hbm_peak,
+        "rows": R,
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
+                   "tile": cfg.tile if mode != "off" else None,
+                   "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": tokens_per_s,
+        "frac_of_bf16_peak": value / world / peak_t,
+        "roofline": roofline,
+        "stages": extra,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "tokens_per_s": world * T * args.steps / (e2e_ms * 1e-3),
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if inp_host is not None:
+        ntok, secs, desc = oracle_sample_time(cfg, inp_host, mode, budget_s=args.cpu_seconds)
+        tps = ntok / secs
+        line["cpu_baseline"] = {"value": tps * 6.0 * k * d * n / 1e12, "unit": "TFLOP/s", "tokens_per_s": tps,
+                                "cores": cpu_threads(), "host_cpus": os.cpu_count(), "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="mixtral", choices=sorted(I.CONFIGS))
+    ap.add_argument("--round", default="off", choices=["off", "nearest", "up"])
+    ap.add_argument("--tokens", type=int, default=0, help="override T (parity/debug only)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        # the oracle runs on rank 0 only; the other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), 0)
+        return
+    world, rank, local = dist_init(args)
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moe.h — C ABI of libmoe.so: the forward pass of one Mixture-of-Experts
+ * layer on one B300 GPU (sm_103a).
+ *
+ * The layer (dataflow of the moe_forward pseudocode in "MoE架构的物理瓶颈与扩展限制解析",
+ * section 工作原理, with both all-to-all steps removed because every expert
+ * lives on this GPU; step list of the fused kernel in "硬件加速的考量",
+ * section 自定义核与核融合):
+ *
+ *   L      = x Wr + b                                  router logits      (moe_router_logits)
+ *   S_t, w = top-k of L[t], softmax over the selected   gating             (moe_topk_gating)
+ *   rows   = assignments grouped by expert (stable)     permutation        (moe_permute)
+ *   h[r]   = silu(x[t_r] W1_e) * (x[t_r] W3_e)          up-projection      (moe_expert_up)
+ *   ys[r]  = w_r * (h[r] W2_e)                          down-projection    (moe_expert_down)
+ *   y[t]   = sum over t's rows of ys[r], fixed order    combine            (moe_combine)
+ *
+ * The gather of token rows into the up-projection and the SwiGLU activation
+ * are fused into the grouped GEMM ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化",
+ * sections "Gather 与加载融合" and the "关键 Kernel 对比" table).  The optional
+ * token rounding (same page, "3. Token Rounding 路由算法") rounds each expert's
+ * row count to a multiple of a tile (moe_token_round).
+ *
+ * Conventions (every entry point):
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, row-major and
+ *     contiguous.  bf16 tensors are passed as `void*` (IEEE bfloat16 bits).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every launch
+ *     goes onto it, in order; no entry point synchronises the stream except
+ *     moe_check_device_status.
+ *   - The caller allocates and owns every buffer, including the workspace.
+ *     The library allocates nothing and frees nothing.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns MOE_ERR_INVALID (or MOE_ERR_UNSUPPORTED / _WORKSPACE)
+ *     and enqueues nothing.
+ *   - A launch failure returns MOE_ERR_CUDA.  Problems the kernels detect
+ *     (a bounded wait that ran out, an expert id out of range, a NaN logit) are
+ *     recorded in a status word at the start of the workspace and read by
+ *     moe_check_device_status.
+ *   - Results are deterministic: identical inputs give bitwise identical
+ *     outputs.  No atomic operation decides an order or a floating-point sum.
+ *
+ * Shape rules: T >= 1, 1 <= E <= 1024, 1 <= k <= min(E, 32), d % 64 == 0,
+ * n % 64 == 0, 64 <= d, n <= 65536; tile in {64, 128, 256} when rounding.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,      /* bad argument: nothing was launched */
+  MOE_ERR_CUDA = 2,         /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than moe_workspace_bytes() */
+  MOE_ERR_UNSUPPORTED = 4,  /* shape outside what the kernels support */
+  MOE_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+  MOE_ERR_DEVICE_CHECK = 6  /* a device-side input check failed */
+} moe_status;
+
+typedef enum {
+  MOE_ROUND_OFF = 0,        /* plain top-k routing */
+  MOE_ROUND_NEAREST = 1,    /* each count to the nearest tile multiple, half up */
+  MOE_ROUND_UP = 2          /* each count up to a tile multiple */
+} moe_round_mode;
+
+typedef struct {
+  int32_t T;      /* tokens */
+  int32_t d;      /* model dim */
+  int32_t n;      /* expert intermediate dim */
+  int32_t E;      /* experts */
+  int32_t k;      /* experts per token */
+  int32_t tile;   /* token-rounding tile; ignored when round == MOE_ROUND_OFF */
+  int32_t round;  /* moe_round_mode */
+} moe_shape;
+
+/* Number of rows the expert GEMMs can see: T*k without rounding, T*k + E*tile
+ * with it.  Every per-row buffer (row_token, row_w, h, ys, tok_rows) holds
+ * this many rows.  Returns 0 for an invalid shape. */
+int64_t moe_row_capacity(const moe_shape* s);
+
+/* Bytes of workspace moe_forward needs (the stage entry points need at most
+ * this much).  Returns 0 for an invalid shape. */
+size_t moe_workspace_bytes(const moe_shape* s);
+
+/* Static text for a status code. */
+const char* moe_status_string(int status);
+
+/* Synchronises `stream`, then reads and clears the device status word at the
+ * start of `ws`.  Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_CHECK or
+ * MOE_ERR_CUDA.  If `detail` is non-NULL it receives the kernel-specific
+ * detail word (which wait, or which bad index). */
+int moe_check_device_status(void* ws, int32_t* detail, void* stream);
+
+/* Clears the status word at the start of `ws` (stream-ordered). */
+int moe_clear_device_status(void* ws, void* stream);
+
+/* One-time weight repack into the layouts the grouped GEMMs read K-major.
+ *   W1, W3   [E, d, n] bf16   (W1 = gated branch, W3 = linear branch)
+ *   W2       [E, n, d] bf16
+ *   W13p     [E, 2n, d] bf16 out: per block b of H = (n % 128 ? 64 : 128)
+ *            columns, rows [2Hb, 2Hb+H) hold W1[e][:, Hb + i]^T and rows
+ *            [2Hb+H, 2Hb+2H) hold W3[e][:, Hb + i]^T, so one GEMM tile
+ *            carries matching gate and linear columns.
+ *   W2p      [E, d, n] bf16 out: W2p[e][i][j] = W2[e][j][i]. */
+int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, const void* W2,
+                        void* W13p, void* W2p, void* stream);
+
+/* Router logits (gate network; "MoE架构的物理瓶颈与扩展限制解析", 工作原理 step 1):
+ *   logits[T, E] fp32 = float(x[T, d] bf16) @ Wr[d, E] fp32 + bias[E] fp32.
+ * bias may be NULL.  fp32 accumulation. */
+int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                      float* logits, void* ws, void* stream);
+
+/* Top-k gating from given fp32 logits (工作原理 step 1, `top_k`):
+ *   topk_idx[T, k] int32: the k largest logits of each row in descending
+ *     order, equal values ordered by ascending expert id (-0.0 == +0.0);
+ *   topk_w[T, k] fp32: softmax over the k selected logits (renormalised).
+ * A NaN logit sets MOE_ERR_DEVICE_CHECK in the status word and ranks lowest. */
+int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, float* topk_w,
+                    void* ws, void* stream);
+
+/* moe_router_logits followed by moe_topk_gating. */
+int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+              float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream);
+
+/* Stable grouping of the A = T*k assignments a = t*k + j by expert
+ * (bit-exact counting sort; rows of one expert are in ascending a):
+ *   counts[E], offsets[E+1] (exclusive prefix, offsets[E] = A)
+ *   src[A]       row -> assignment a
+ *   dst[A]       assignment a -> row
+ *   row_token[A] row -> token a / k
+ *   row_w[A]     row -> topk_w[a]
+ * topk_w may be NULL (row_w is then not written).  Uses the workspace for
+ * per-chunk histograms.  An expert id outside [0, E) sets
+ * MOE_ERR_DEVICE_CHECK and that assignment is skipped. */
+int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w,
+                int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst,
+                int32_t* row_token, float* row_w, void* ws, size_t ws_bytes, void* stream);
+
+/* Token rounding ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化", 3. Token Rounding 路由算法),
+ * mode s->round (NEAREST or UP), tile s->tile.  Each expert's count c becomes
+ * c' = tile-multiple (nearest half-up, or up), capped at tile*floor(T/tile).
+ * If c' > c the c'-c tokens not routed to e with the highest logits[t, e] join
+ * (ties: lower t first); if c' < c the c-c' routed tokens with the lowest
+ * logits leave (ties: higher t first); each expert is rounded from the original
+ * top-k sets.  Outputs (R = offsets[E] rows, R <= moe_row_capacity):
+ *   counts[E], offsets[E+1]; row_token[R], row_w[R] (softmax over the token's
+ *   final set), tok_offsets[T+1] and tok_rows[R] (token -> its rows, in the
+ *   order logits desc, expert id asc).  logits are the fp32 router logits. */
+int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk_idx,
+                    int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w,
+                    int32_t* tok_offsets, int32_t* tok_rows, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/* Up-projection grouped GEMM with the row gather fused into the operand load
+ * and SwiGLU fused into the epilogue:
+ *   for each expert e and row r in [offsets[e], offsets[e+1]):
+ *     h[r, :] = bf16( silu(x[row_token[r]] W1_e) * (x[row_token[r]] W3_e) )
+ *   silu(z) = z / (1 + exp(-z)); fp32 accumulation in tensor memory.
+ *   x [T, d] bf16; W13p from moe_prepare_weights; h [moe_row_capacity, n] bf16.
+ * gather: 0 = rows fetched by TMA gather (4 rows per copy) straight into
+ * shared memory; 1 = rows first copied into the workspace, then tiled TMA. */
+int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int32_t* counts,
+                  const int32_t* offsets, const int32_t* row_token, void* h, int gather,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* Down-projection grouped GEMM with the gate weight in the epilogue:
+ *   ys[r, :] = bf16( row_w[r] * (h[r] W2_e) ) for rows of expert e.
+ *   h [cap, n] bf16; W2p from moe_prepare_weights; ys [cap, d] bf16. */
+int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const int32_t* counts,
+                    const int32_t* offsets, const float* row_w, void* ys, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* Deterministic combine back to token order (自定义核与核融合 step 5):
+ *   y[t, :] = bf16( sum over j of ys[row_j, :] ), fp32 sum in list order,
+ * where t's rows are tok_rows[tok_offsets[t] .. tok_offsets[t+1]) or, when
+ * tok_offsets is NULL, tok_rows[t*k .. t*k+k) (the `dst` array of
+ * moe_permute).  A token with no rows gets y[t] = 0. */
+int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets,
+                const int32_t* tok_rows, void* y, void* stream);
+
+/* The whole layer: route, (round), permute, up, down, combine.
+ *   x [T, d] bf16, Wr [d, E] fp32, bias [E] fp32 or NULL,
+ *   W13p, W2p from moe_prepare_weights, y [T, d] bf16 out.
+ * ws must hold moe_workspace_bytes(s) bytes. */
+int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                const void* W13p, const void* W2p, void* y, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* Byte offsets into the moe_forward workspace of its intermediate arrays, so
+ * a caller can inspect them after a forward (all -1 for an invalid shape):
+ * [0] logits f32[T*E]  [1] topk_idx i32[T*k]  [2] topk_w f32[T*k]
+ * [3] counts i32[E]    [4] offsets i32[E+1]   [5] src i32[cap]  [6] dst i32[T*k]
+ * [7] row_token i32[cap] [8] row_w f32[cap]   [9] tok_offsets i32[T+1]
+ * [10] tok_rows i32[cap] [11] h bf16[cap*n]   [12] ys bf16[cap*d] */
+int moe_workspace_layout(const moe_shape* s, int64_t* offsets_out, int32_t n_out);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on a
+ * device flag nobody sets, giving up after `timeout_ns` nanoseconds; the
+ * kernel then records MOE_ERR_TIMEOUT in the status word of `ws` and returns. */
+int moe_selftest_timeout(void* ws, uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

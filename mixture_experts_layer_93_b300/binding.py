@@ -1,0 +1,332 @@
+"""ctypes binding of libmoe.so (declared in include/moe.h).
+
+Argument marshalling only: torch allocates device memory and supplies the
+current stream; every step of the layer runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID = 1
+MOE_ERR_CUDA = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_UNSUPPORTED = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_CHECK = 6
+
+ROUND_MODES = {"off": 0, "nearest": 1, "up": 2}
+
+# workspace_layout slots
+WS_SLOTS = ["logits", "topk_idx", "topk_w", "counts", "offsets", "src", "dst", "row_token", "row_w",
+            "tok_offsets", "tok_rows", "h", "ys"]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: int | None = None):
+        self.status = status
+        self.detail = detail
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if detail is not None:
+            msg += f", detail {detail}"
+        super().__init__(msg)
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("n", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("tile", ctypes.c_int32), ("round", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_SZ = ctypes.c_size_t
+_I = ctypes.c_int
+_SHP = ctypes.POINTER(moe_shape)
+
+_SIGNATURES = {
+    "moe_row_capacity": (ctypes.c_int64, [_SHP]),
+    "moe_workspace_bytes": (_SZ, [_SHP]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_check_device_status": (_I, [_P, ctypes.POINTER(ctypes.c_int32), _P]),
+    "moe_clear_device_status": (_I, [_P, _P]),
+    "moe_prepare_weights": (_I, [_SHP, _P, _P, _P, _P, _P, _P]),
+    "moe_router_logits": (_I, [_SHP, _P, _P, _P, _P, _P, _P]),
+    "moe_topk_gating": (_I, [_SHP, _P, _P, _P, _P, _P]),
+    "moe_route": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "moe_expert_down": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_combine": (_I, [_SHP, _P, _P, _P, _P, _P]),
+    "moe_forward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_workspace_layout": (_I, [_SHP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
+    "moe_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (built in-tree by `python -m mixture_experts_layer_93_b300.build`)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                       "`python -m mixture_experts_layer_93_b300.build`")
+                handle = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGNATURES.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def make_shape(T, d, n, E, k, tile=128, round="off") -> moe_shape:
+    mode = ROUND_MODES[round] if isinstance(round, str) else int(round)
+    return moe_shape(int(T), int(d), int(n), int(E), int(k), int(tile), mode)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device=None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("libmoe works on CUDA tensors only (no CPU fallback)")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+
+
+def moe_row_capacity(shape: moe_shape) -> int:
+    return int(lib().moe_row_capacity(ctypes.byref(shape)))
+
+
+def moe_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib().moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_workspace_layout(shape: moe_shape) -> dict:
+    arr = (ctypes.c_int64 * len(WS_SLOTS))()
+    _check(lib().moe_workspace_layout(ctypes.byref(shape), arr, len(WS_SLOTS)), "moe_workspace_layout")
+    return {name: int(arr[i]) for i, name in enumerate(WS_SLOTS)}
+
+
+class Workspace:
+    """Device workspace for one shape (status block zeroed at creation)."""
+
+    def __init__(self, shape: moe_shape, device="cuda"):
+        nbytes = moe_workspace_bytes(shape)
+        if nbytes == 0:
+            raise MoEError(MOE_ERR_INVALID, "moe_workspace_bytes")
+        self.shape = shape
+        self.nbytes = nbytes
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.buf[:256].zero_()
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def view(self, slot: str, dtype, numel: int) -> torch.Tensor:
+        off = moe_workspace_layout(self.shape)[slot]
+        esz = torch.tensor([], dtype=dtype).element_size()
+        return self.buf[off:off + numel * esz].view(dtype)
+
+
+def moe_check_device_status(ws: Workspace, raise_on_error: bool = True) -> int:
+    detail = ctypes.c_int32(0)
+    st = lib().moe_check_device_status(ws.ptr, ctypes.byref(detail), _stream(ws.buf.device))
+    if st != MOE_OK and raise_on_error:
+        raise MoEError(st, "device status", detail.value)
+    return st
+
+
+def moe_clear_device_status(ws: Workspace):
+    _check(lib().moe_clear_device_status(ws.ptr, _stream(ws.buf.device)), "moe_clear_device_status")
+
+
+def moe_prepare_weights(W1, W3, W2):
+    """Repack W1/W3 [E,d,n] and W2 [E,n,d] into (W13p [E,2n,d], W2p [E,d,n])."""
+    _need_cuda(W1, W3, W2)
+    E, d, n = W1.shape
+    shape = make_shape(1, d, n, E, 1)
+    W13p = torch.empty(E, 2 * n, d, dtype=torch.bfloat16, device=W1.device)
+    W2p = torch.empty(E, d, n, dtype=torch.bfloat16, device=W1.device)
+    _check(lib().moe_prepare_weights(ctypes.byref(shape), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(W13p), _ptr(W2p),
+                                     _stream(W1.device)), "moe_prepare_weights")
+    return W13p, W2p
+
+
+def moe_router_logits(x, Wr, bias=None, ws: Workspace | None = None):
+    _need_cuda(x, Wr, bias)
+    T, d = x.shape
+    E = Wr.shape[1]
+    shape = make_shape(T, d, 64, E, 1)
+    logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
+    _check(lib().moe_router_logits(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(logits),
+                                   ws.ptr if ws else None, _stream(x.device)), "moe_router_logits")
+    return logits
+
+
+def moe_topk_gating(logits, k: int, ws: Workspace):
+    _need_cuda(logits)
+    T, E = logits.shape
+    shape = make_shape(T, 64, 64, E, k)
+    idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _check(lib().moe_topk_gating(ctypes.byref(shape), _ptr(logits), _ptr(idx), _ptr(w), ws.ptr,
+                                 _stream(logits.device)), "moe_topk_gating")
+    return idx, w
+
+
+def moe_route(x, Wr, bias, k: int, ws: Workspace):
+    _need_cuda(x, Wr, bias)
+    T, d = x.shape
+    E = Wr.shape[1]
+    shape = make_shape(T, d, 64, E, k)
+    logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
+    idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
+    w = torch.empty(T, k, dtype=torch.float32, device=x.device)
+    _check(lib().moe_route(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(logits), _ptr(idx), _ptr(w),
+                           ws.ptr, _stream(x.device)), "moe_route")
+    return logits, idx, w
+
+
+def moe_permute(shape: moe_shape, topk_idx, topk_w, ws: Workspace) -> dict:
+    _need_cuda(topk_idx, topk_w)
+    dev = topk_idx.device
+    A = shape.T * shape.k
+    cap = moe_row_capacity(shape)
+    out = {
+        "counts": torch.empty(shape.E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(shape.E + 1, dtype=torch.int32, device=dev),
+        "src": torch.empty(cap, dtype=torch.int32, device=dev),
+        "dst": torch.empty(A, dtype=torch.int32, device=dev),
+        "row_token": torch.empty(cap, dtype=torch.int32, device=dev),
+        "row_w": torch.empty(cap, dtype=torch.float32, device=dev),
+    }
+    _check(lib().moe_permute(ctypes.byref(shape), _ptr(topk_idx), _ptr(topk_w), _ptr(out["counts"]),
+                             _ptr(out["offsets"]), _ptr(out["src"]), _ptr(out["dst"]), _ptr(out["row_token"]),
+                             _ptr(out["row_w"]) if topk_w is not None else None, ws.ptr, ws.nbytes,
+                             _stream(dev)), "moe_permute")
+    return out
+
+
+def moe_token_round(shape: moe_shape, logits, topk_idx, ws: Workspace) -> dict:
+    _need_cuda(logits, topk_idx)
+    dev = logits.device
+    cap = moe_row_capacity(shape)
+    out = {
+        "counts": torch.empty(shape.E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(shape.E + 1, dtype=torch.int32, device=dev),
+        "row_token": torch.empty(cap, dtype=torch.int32, device=dev),
+        "row_w": torch.empty(cap, dtype=torch.float32, device=dev),
+        "tok_offsets": torch.empty(shape.T + 1, dtype=torch.int32, device=dev),
+        "tok_rows": torch.empty(cap, dtype=torch.int32, device=dev),
+    }
+    _check(lib().moe_token_round(ctypes.byref(shape), _ptr(logits), _ptr(topk_idx), _ptr(out["counts"]),
+                                 _ptr(out["offsets"]), _ptr(out["row_token"]), _ptr(out["row_w"]),
+                                 _ptr(out["tok_offsets"]), _ptr(out["tok_rows"]), ws.ptr, ws.nbytes,
+                                 _stream(dev)), "moe_token_round")
+    return out
+
+
+def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Workspace, gather: bool = True,
+                  h=None):
+    _need_cuda(x, W13p, counts, offsets, row_token)
+    cap = moe_row_capacity(shape)
+    if h is None:
+        h = torch.empty(cap, shape.n, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_expert_up(ctypes.byref(shape), _ptr(x), _ptr(W13p), _ptr(counts), _ptr(offsets),
+                               _ptr(row_token), _ptr(h), 1 if gather else 0, ws.ptr, ws.nbytes,
+                               _stream(x.device)), "moe_expert_up")
+    return h
+
+
+def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Workspace, ys=None):
+    _need_cuda(h, W2p, counts, offsets, row_w)
+    cap = moe_row_capacity(shape)
+    if ys is None:
+        ys = torch.empty(cap, shape.d, dtype=torch.bfloat16, device=h.device)
+    _check(lib().moe_expert_down(ctypes.byref(shape), _ptr(h), _ptr(W2p), _ptr(counts), _ptr(offsets),
+                                 _ptr(row_w), _ptr(ys), ws.ptr, ws.nbytes, _stream(h.device)), "moe_expert_down")
+    return ys
+
+
+def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
+    _need_cuda(ys, tok_offsets, tok_rows)
+    if y is None:
+        y = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device=ys.device)
+    _check(lib().moe_combine(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
+                             _stream(ys.device)), "moe_combine")
+    return y
+
+
+def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
+    _need_cuda(x, Wr, bias, W13p, W2p)
+    if y is None:
+        y = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p), _ptr(y),
+                             ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward")
+    return y
+
+
+def moe_selftest_timeout(ws: Workspace, timeout_ns: int):
+    _check(lib().moe_selftest_timeout(ws.ptr, int(timeout_ns), _stream(ws.buf.device)), "moe_selftest_timeout")
+
+
+class MoELayer:
+    """One MoE layer with its weights packed once and a reusable workspace."""
+
+    def __init__(self, Wr, bias, W1, W3, W2, k: int, tile: int = 128, round: str = "off"):
+        self.E, self.d, self.n = W1.shape
+        self.k, self.tile, self.round = k, tile, round
+        self.Wr = Wr.contiguous()
+        self.bias = bias.contiguous() if bias is not None else None
+        self.W13p, self.W2p = moe_prepare_weights(W1.contiguous(), W3.contiguous(), W2.contiguous())
+        self._ws = {}
+
+    def shape(self, T: int) -> moe_shape:
+        return make_shape(T, self.d, self.n, self.E, self.k, self.tile, self.round)
+
+    def workspace(self, T: int, device) -> Workspace:
+        key = (T, str(device))
+        if key not in self._ws:
+            self._ws[key] = Workspace(self.shape(T), device)
+        return self._ws[key]
+
+    def forward(self, x, y=None):
+        T = x.shape[0]
+        ws = self.workspace(T, x.device)
+        return moe_forward(self.shape(T), x, self.Wr, self.bias, self.W13p, self.W2p, ws, y)
+
+    __call__ = forward

@@ -1,0 +1,276 @@
+// C ABI of libmoe.so: argument validation, workspace layout and the stage
+// sequence of the MoE-layer forward.  Every declaration is in include/moe.h.
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool shape_ok(const moe_shape* s) {
+  if (!s) return false;
+  if (s->T < 1 || s->E < 1 || s->E > 1024) return false;
+  if (s->k < 1 || s->k > s->E || s->k > 32) return false;
+  if (s->d < 64 || s->d % 64 != 0 || s->d > 65536) return false;
+  if (s->n < 64 || s->n % 64 != 0 || s->n > 65536) return false;
+  if (s->round != MOE_ROUND_OFF && s->round != MOE_ROUND_NEAREST && s->round != MOE_ROUND_UP) return false;
+  if (s->round != MOE_ROUND_OFF && s->tile != 64 && s->tile != 128 && s->tile != 256) return false;
+  // row indices and element offsets stay in range of the int32 / int64 math
+  const int64_t A = static_cast<int64_t>(s->T) * s->k;
+  const int64_t cap = A + (s->round != MOE_ROUND_OFF ? static_cast<int64_t>(s->E) * s->tile : 0);
+  if (cap >= (int64_t(1) << 31) - 1) return false;
+  return true;
+}
+
+inline int64_t row_cap(const moe_shape* s) {
+  const int64_t A = static_cast<int64_t>(s->T) * s->k;
+  return A + (s->round != MOE_ROUND_OFF ? static_cast<int64_t>(s->E) * s->tile : 0);
+}
+
+inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
+
+enum Slot {
+  kLogits, kTopkIdx, kTopkW, kCounts, kOffsets, kSrc, kDst, kRowToken, kRowW, kTokOffsets, kTokRows, kH, kYs,
+  kPermHist, kRoundScratch, kNumSlots
+};
+
+// Byte offsets of each array in the workspace; returns the total size.
+int64_t layout(const moe_shape* s, int64_t* off) {
+  const int64_t T = s->T, E = s->E, A = T * s->k, cap = row_cap(s);
+  const int64_t sizes[kNumSlots] = {
+      T * E * 4,          A * 4,     A * 4,     E * 4,   (E + 1) * 4,       cap * 4,
+      A * 4,              cap * 4,   cap * 4,   (T + 1) * 4, cap * 4,       cap * s->n * 2,
+      cap * s->d * 2,     E * perm_num_chunks(cap) * 4,
+      s->round != MOE_ROUND_OFF ? static_cast<int64_t>(round_scratch_bytes(s->T, s->E, s->k, s->tile)) : 0};
+  int64_t pos = static_cast<int64_t>(kStatusBytes);
+  for (int i = 0; i < kNumSlots; ++i) {
+    off[i] = pos;
+    pos = align256(pos + sizes[i]);
+  }
+  return pos;
+}
+
+template <typename T>
+inline T* at(void* ws, int64_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline int last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+inline int32_t* status_of(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
+  int64_t off[kNumSlots];
+  if (static_cast<int64_t>(ws_bytes) < layout(s, off)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t moe_row_capacity(const moe_shape* s) { return shape_ok(s) ? row_cap(s) : 0; }
+
+size_t moe_workspace_bytes(const moe_shape* s) {
+  if (!shape_ok(s)) return 0;
+  int64_t off[kNumSlots];
+  return static_cast<size_t>(layout(s, off));
+}
+
+int moe_workspace_layout(const moe_shape* s, int64_t* out, int32_t n_out) {
+  if (!out || n_out < 0) return MOE_ERR_INVALID;
+  if (!shape_ok(s)) {
+    for (int i = 0; i < n_out; ++i) out[i] = -1;
+    return MOE_ERR_INVALID;
+  }
+  int64_t off[kNumSlots];
+  layout(s, off);
+  for (int i = 0; i < n_out; ++i) out[i] = (i <= kYs) ? off[i] : -1;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side input check failed";
+    default: return "unknown status";
+  }
+}
+
+int moe_clear_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID;
+  return cudaMemsetAsync(ws, 0, kStatusBytes, as_stream(stream)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_check_device_status(void* ws, int32_t* detail, void* stream) {
+  if (!ws) return MOE_ERR_INVALID;
+  int32_t h[4] = {0, 0, 0, 0};
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemcpyAsync(h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return h[0];
+}
+
+int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, const void* W2, void* W13p, void* W2p,
+                        void* stream) {
+  if (!shape_ok(s) || !W1 || !W3 || !W2 || !W13p || !W2p) return MOE_ERR_INVALID;
+  if (!aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(W13p) || !aligned16(W2p))
+    return MOE_ERR_INVALID;
+  launch_prepare_weights(static_cast<const __nv_bfloat16*>(W1), static_cast<const __nv_bfloat16*>(W3),
+                         static_cast<const __nv_bfloat16*>(W2), static_cast<__nv_bfloat16*>(W13p),
+                         static_cast<__nv_bfloat16*>(W2p), s->E, s->d, s->n, as_stream(stream));
+  return last_launch();
+}
+
+int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
+                      void* ws, void* stream) {
+  (void)ws;
+  if (!shape_ok(s) || !x || !Wr || !logits || !aligned16(x)) return MOE_ERR_INVALID;
+  launch_router_logits(static_cast<const __nv_bfloat16*>(x), Wr, bias, logits, s->T, s->d, s->E, as_stream(stream));
+  return last_launch();
+}
+
+int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, float* topk_w, void* ws,
+                    void* stream) {
+  if (!shape_ok(s) || !logits || !topk_idx || !topk_w || !ws) return MOE_ERR_INVALID;
+  launch_topk_gating(logits, topk_idx, topk_w, s->T, s->E, s->k, status_of(ws), as_stream(stream));
+  return last_launch();
+}
+
+int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
+              int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
+  int st = moe_router_logits(s, x, Wr, bias, logits, ws, stream);
+  if (st != MOE_OK) return st;
+  return moe_topk_gating(s, logits, topk_idx, topk_w, ws, stream);
+}
+
+int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
+                int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token, float* row_w, void* ws,
+                size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !topk_idx || !counts || !offsets || !src || !dst || !row_token) return MOE_ERR_INVALID;
+  if (topk_w && !row_w) return MOE_ERR_INVALID;
+  const int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  const int64_t A = static_cast<int64_t>(s->T) * s->k;
+  launch_permute(topk_idx, topk_w, A, s->k, s->E, at<int32_t>(ws, off[kPermHist]), counts, offsets, src, dst,
+                 row_token, row_w, status_of(ws), as_stream(stream));
+  return last_launch();
+}
+
+int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk_idx, int32_t* counts,
+                    int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets, int32_t* tok_rows,
+                    void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || s->round == MOE_ROUND_OFF) return MOE_ERR_INVALID;
+  return MOE_ERR_UNSUPPORTED;
+  if (!logits || !topk_idx || !counts || !offsets || !row_token || !row_w || !tok_offsets || !tok_rows)
+    return MOE_ERR_INVALID;
+  const int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  launch_token_round(logits, topk_idx, s->T, s->E, s->k, s->tile, s->round, counts, offsets, row_token, row_w,
+                     tok_offsets, tok_rows, at<void>(ws, off[kRoundScratch]), status_of(ws), as_stream(stream));
+  return last_launch();
+}
+
+int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int32_t* counts, const int32_t* offsets,
+                  const int32_t* row_token, void* h, int gather, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !W13p || !counts || !offsets || !row_token || !h) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13p) || !aligned16(h)) return MOE_ERR_INVALID;
+  const int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  // the non-gather variant stages the gathered rows in the ys region, which
+  // the forward only writes after the up-projection
+  return launch_expert_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(W13p), counts,
+                          offsets, row_token, static_cast<__nv_bfloat16*>(h), s->T, s->d, s->n, s->E, row_cap(s),
+                          gather ? 1 : 0, at<__nv_bfloat16>(ws, off[kYs]), status_of(ws), kDefaultTimeoutNs,
+                          as_stream(stream));
+}
+
+int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const int32_t* counts,
+                    const int32_t* offsets, const float* row_w, void* ys, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (!shape_ok(s) || !h || !W2p || !counts || !offsets || !row_w || !ys) return MOE_ERR_INVALID;
+  if (!aligned16(h) || !aligned16(W2p) || !aligned16(ys)) return MOE_ERR_INVALID;
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
+  (void)ws_bytes;
+  return launch_expert_down(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(W2p), counts,
+                            offsets, row_w, static_cast<__nv_bfloat16*>(ys), s->d, s->n, s->E, row_cap(s),
+                            status_of(ws), kDefaultTimeoutNs, as_stream(stream));
+}
+
+int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets, const int32_t* tok_rows, void* y,
+                void* stream) {
+  if (!shape_ok(s) || !ys || !tok_rows || !y || !aligned16(ys) || !aligned16(y)) return MOE_ERR_INVALID;
+  launch_combine(static_cast<const __nv_bfloat16*>(ys), tok_offsets, tok_rows, static_cast<__nv_bfloat16*>(y), s->T,
+                 s->d, s->k, as_stream(stream));
+  return last_launch();
+}
+
+int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !W13p || !W2p || !y) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13p) || !aligned16(W2p) || !aligned16(y)) return MOE_ERR_INVALID;
+  int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  float* logits = at<float>(ws, off[kLogits]);
+  int32_t* idx = at<int32_t>(ws, off[kTopkIdx]);
+  float* w = at<float>(ws, off[kTopkW]);
+  int32_t* counts = at<int32_t>(ws, off[kCounts]);
+  int32_t* offsets = at<int32_t>(ws, off[kOffsets]);
+  int32_t* src = at<int32_t>(ws, off[kSrc]);
+  int32_t* dst = at<int32_t>(ws, off[kDst]);
+  int32_t* row_token = at<int32_t>(ws, off[kRowToken]);
+  float* row_w = at<float>(ws, off[kRowW]);
+  int32_t* tok_offsets = at<int32_t>(ws, off[kTokOffsets]);
+  int32_t* tok_rows = at<int32_t>(ws, off[kTokRows]);
+  void* h = at<void>(ws, off[kH]);
+  void* ys = at<void>(ws, off[kYs]);
+
+  if ((st = moe_route(s, x, Wr, bias, logits, idx, w, ws, stream)) != MOE_OK) return st;
+  const int32_t* combine_offsets = nullptr;
+  const int32_t* combine_rows = dst;
+  if (s->round == MOE_ROUND_OFF) {
+    if ((st = moe_permute(s, idx, w, counts, offsets, src, dst, row_token, row_w, ws, ws_bytes, stream)) != MOE_OK)
+      return st;
+  } else {
+    if ((st = moe_token_round(s, logits, idx, counts, offsets, row_token, row_w, tok_offsets, tok_rows, ws, ws_bytes,
+                              stream)) != MOE_OK)
+      return st;
+    combine_offsets = tok_offsets;
+    combine_rows = tok_rows;
+  }
+  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, h, 1, ws, ws_bytes, stream)) != MOE_OK) return st;
+  if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
+  return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
+}
+
+int moe_selftest_timeout(void* ws, uint64_t timeout_ns, void* stream) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  launch_selftest_timeout(status_of(ws), timeout_ns, as_stream(stream));
+  return last_launch();
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// Host-side launchers of the kernels in libmoe.so (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// route.cu
+void launch_router_logits(const __nv_bfloat16* x, const float* Wr, const float* bias, float* logits, int T, int d,
+                          int E, cudaStream_t stream);
+void launch_topk_gating(const float* logits, int32_t* idx, float* w, int T, int E, int k, int32_t* status,
+                        cudaStream_t stream);
+
+// permute.cu
+constexpr int kPermChunk = 2048;  // assignments per warp chunk
+inline int64_t perm_num_chunks(int64_t A) { return (A + kPermChunk - 1) / kPermChunk; }
+void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
+                    int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                    float* row_w, int32_t* status, cudaStream_t stream);
+
+// round.cu
+size_t round_scratch_bytes(int T, int E, int k, int tile);
+void launch_token_round(const float* logits, const int32_t* idx, int T, int E, int k, int tile, int mode,
+                        int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
+                        int32_t* tok_rows, void* scratch, int32_t* status, cudaStream_t stream);
+
+// gemm.cu
+struct GemmTensorMaps;
+int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
+                     const int32_t* offsets, const int32_t* row_token, __nv_bfloat16* h, int T, int d, int n, int E,
+                     int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
+                     uint64_t timeout_ns, cudaStream_t stream);
+int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
+                       const int32_t* offsets, const float* row_w, __nv_bfloat16* ys, int d, int n, int E,
+                       int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const int32_t* offsets, int E, int d,
+                        __nv_bfloat16* out, int64_t rows_cap, cudaStream_t stream);
+inline int up_half_block(int n) { return (n % 128 == 0) ? 128 : 64; }
+
+// combine.cu
+void launch_combine(const __nv_bfloat16* ys, const int32_t* tok_offsets, const int32_t* tok_rows,
+                    __nv_bfloat16* y, int T, int d, int k, cudaStream_t stream);
+
+// prepare.cu
+void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, const __nv_bfloat16* W2,
+                            __nv_bfloat16* W13p, __nv_bfloat16* W2p, int E, int d, int n, cudaStream_t stream);
+
+// selftest
+void launch_selftest_timeout(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,145 @@
+// Permutation: a stable counting sort of the T*k assignments a = t*k + j by
+// expert id, so each expert's rows are contiguous for the grouped GEMM (the
+// "contiguous packed input" mode of "SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化",
+// section "Gather 与加载融合").
+//
+// Three launches, none of which lets an atomic decide an order:
+//   hist    per-chunk expert histograms (a warp per chunk of 2048 assignments)
+//   scan    per-expert exclusive prefix over chunks, then over experts
+//   scatter each warp walks its chunk in order, 32 assignments at a time;
+//           equal experts within a step are ranked by lane (match.any), so
+//           rows of an expert come out in ascending a, i.e. ascending t.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kPermWarps = 4;
+
+__global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t A, int E,
+                                                                  int nchunks, int32_t* __restrict__ chunk_hist,
+                                                                  int32_t* status) {
+  extern __shared__ int32_t hist_s[];
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = blockIdx.x * kPermWarps + w;
+  if (c >= nchunks) return;
+  int32_t* h = hist_s + w * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int64_t a0 = static_cast<int64_t>(c) * kPermChunk;
+  const int64_t a1 = min(A, a0 + kPermChunk);
+  bool bad = false;
+  for (int64_t a = a0 + lane; a < a1; a += 32) {
+    const int e = idx[a];
+    if (e >= 0 && e < E)
+      atomicAdd(&h[e], 1);  // counts only: the order of increments does not matter
+    else
+      bad = true;
+  }
+  if (bad) report_error(status, MOE_ERR_DEVICE_CHECK, -1);
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) chunk_hist[static_cast<int64_t>(e) * nchunks + c] = h[e];
+}
+
+// One block of 1024 threads.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist, int E, int nchunks,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  __shared__ int32_t cnt_s[1024];
+  __shared__ int32_t warp_s[32];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < 1024; e += blockDim.x) cnt_s[e] = 0;
+  for (int e = tid; e < E; e += blockDim.x) {
+    int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
+    int32_t run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int32_t v = hrow[c];
+      hrow[c] = run;
+      run += v;
+    }
+    cnt_s[e] = run;
+  }
+  __syncthreads();
+  // exclusive scan of cnt_s[0..1024) (E <= 1024): one value per thread
+  const int lane = tid % 32, wid = tid / 32;
+  const int32_t v = cnt_s[tid];
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_s[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t s = warp_s[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
+    }
+    warp_s[lane] = s;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int32_t excl = incl - v + (wid > 0 ? warp_s[wid - 1] : 0);
+  __syncthreads();
+  cnt_s[tid] = excl;
+  if (tid < E) {
+    counts[tid] = v;
+    offsets[tid] = excl;
+  }
+  if (tid == E - 1) offsets[E] = excl + v;
+  __syncthreads();
+  for (int e = tid; e < E; e += blockDim.x) {
+    int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
+    const int32_t base = cnt_s[e];
+    for (int c = 0; c < nchunks; ++c) hrow[c] += base;
+  }
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32) perm_scatter_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ wts, int64_t A, int k, int E, int nchunks,
+    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ src, int32_t* __restrict__ dst,
+    int32_t* __restrict__ row_token, float* __restrict__ row_w) {
+  extern __shared__ int32_t base_s[];
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int c = blockIdx.x * kPermWarps + w;
+  if (c >= nchunks) return;
+  int32_t* base = base_s + w * E;
+  for (int e = lane; e < E; e += 32) base[e] = chunk_base[static_cast<int64_t>(e) * nchunks + c];
+  __syncwarp();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  const int64_t a0 = static_cast<int64_t>(c) * kPermChunk;
+  const int64_t a1 = min(A, a0 + kPermChunk);
+  for (int64_t ab = a0; ab < a1; ab += 32) {
+    const int64_t a = ab + lane;
+    int e = (a < a1) ? idx[a] : -1;
+    if (e >= E) e = -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    int pos = 0;
+    if (e >= 0) pos = base[e] + rank;
+    __syncwarp();
+    if (e >= 0 && rank == 0) base[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      src[pos] = static_cast<int32_t>(a);
+      dst[a] = pos;
+      row_token[pos] = static_cast<int32_t>(a / k);
+      if (wts) row_w[pos] = wts[a];
+    }
+  }
+}
+
+void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
+                    int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                    float* row_w, int32_t* status, cudaStream_t stream) {
+  const int nchunks = static_cast<int>(perm_num_chunks(A));
+  const int blocks = (nchunks + kPermWarps - 1) / kPermWarps;
+  const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
+  perm_hist_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, A, E, nchunks, chunk_hist, status);
+  perm_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, E, nchunks, counts, offsets);
+  perm_scatter_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, w, A, k, E, nchunks, chunk_hist, src, dst,
+                                                                 row_token, row_w);
+}
+
+}  // namespace moe

@@ -69,7 +69,8 @@ def _f64(a) -> np.ndarray:
     try:
         import torch
         if isinstance(a, torch.Tensor):
-            return a.detach().to("cpu", dtype=torch.float64).numpy()
+            # move in the stored dtype, widen on the host
+            return a.detach().cpu().to(torch.float64).numpy()
     except ImportError:  # pragma: no cover
         pass
     return np.asarray(a, dtype=F64)

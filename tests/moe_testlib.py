@@ -1,0 +1,57 @@
+"""Shared helpers of the parity tests: tolerances and comparisons.
+
+Floating-point outputs are bf16 with fp32 accumulation; the bar is
+  max |y - y_ref| <= 2e-2 * rms(y_ref)   and   sum|y - y_ref| / sum|y_ref| <= 5e-3
+(y_ref from the fp64 oracle).  Integer outputs (expert ids, counts, offsets,
+permutations) must be identical.
+"""
+import numpy as np
+import torch
+
+MAX_ERR_RMS = 2e-2
+MEAN_REL = 5e-3
+
+
+def to64(t) -> np.ndarray:
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def err_stats(y, y_ref):
+    y, y_ref = to64(y), to64(y_ref)
+    diff = np.abs(y - y_ref)
+    rms = float(np.sqrt(np.mean(y_ref ** 2))) if y_ref.size else 0.0
+    max_err = float(diff.max()) if diff.size else 0.0
+    denom = float(np.abs(y_ref).sum())
+    mean_rel = float(diff.sum() / denom) if denom > 0 else float(diff.sum())
+    return {"max_err": max_err, "rms": rms, "max_over_rms": max_err / rms if rms > 0 else max_err,
+            "mean_rel": mean_rel}
+
+
+def assert_moe_close(y, y_ref, what="y"):
+    s = err_stats(y, y_ref)
+    assert np.all(np.isfinite(to64(y))), f"{what}: non-finite values"
+    assert s["max_err"] <= MAX_ERR_RMS * s["rms"] + 1e-30, f"{what}: {s}"
+    assert s["mean_rel"] <= MEAN_REL, f"{what}: {s}"
+    return s
+
+
+def robust_tokens(L64: np.ndarray, k: int, margin: float) -> np.ndarray:
+    """Tokens whose top-k set is decided by more than `margin` (the gap between
+    the k-th and (k+1)-th largest fp64 logit).  For these the set cannot
+    depend on fp32 rounding of the logits."""
+    T, E = L64.shape
+    if k >= E:
+        return np.ones(T, dtype=bool)
+    part = -np.sort(-L64, axis=1)
+    return (part[:, k - 1] - part[:, k]) > margin
+
+
+def valid_topk(L64_row: np.ndarray, chosen, margin: float) -> bool:
+    """A selected set is a valid top-k under a logit perturbation <= margin."""
+    chosen = np.asarray(chosen)
+    rest = np.setdiff1d(np.arange(L64_row.size), chosen)
+    if rest.size == 0:
+        return True
+    return float(L64_row[chosen].min()) >= float(L64_row[rest].max()) - 2 * margin

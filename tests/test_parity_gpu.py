@@ -1,0 +1,268 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every input comes from the seeded generators; every expected value from the
+oracle.  Integer outputs must match exactly; floating-point outputs meet the
+bf16 / fp32-accumulation tolerance in moe_testlib."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_93_b300 import binding as B
+from mixture_experts_layer_93_b300 import inputs as I
+from oracle import moe_oracle as O
+from tests.moe_testlib import assert_moe_close, err_stats, robust_tokens, to64, valid_topk
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_MARGIN = 1e-4
+
+
+def ws_for(T, d, n, E, k, dev, tile=128, round="off"):
+    s = B.make_shape(T, d, n, E, k, tile, round)
+    return s, B.Workspace(s, dev)
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("T,d,E,bias", [(256, 128, 8, False), (1000, 512, 40, True), (300, 1024, 256, True),
+                                        (77, 64, 1, False), (130, 256, 1024, False)])
+def test_router_logits(cuda_device, T, d, E, bias):
+    cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=1, bias="normal" if bias else None, bias_scale=0.5)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=T + E, weights=False)
+    L = B.moe_router_logits(inp["x"], inp["Wr"], inp["bias"])
+    torch.cuda.synchronize()
+    L64 = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
+    err = np.abs(to64(L) - L64)
+    # rigorous fp32 dot-product bound: d * 2^-24 * sum_i |x_i w_ie| (+ bias add)
+    absdot = np.abs(to64(inp["x"])) @ np.abs(to64(inp["Wr"]))
+    assert np.all(err <= (d + 2) * 2.0 ** -24 * (absdot + np.abs(L64)) + 1e-30)
+    rms = float(np.sqrt(np.mean(L64 ** 2)))
+    assert err.max() <= 5e-5 * rms, (err.max(), rms)
+
+
+# -------------------------------------------------------------------- top-k
+@pytest.mark.parametrize("E,k", [(1, 1), (7, 2), (8, 2), (32, 8), (33, 5), (64, 8), (128, 8), (256, 8),
+                                 (1024, 32), (20, 20)])
+def test_topk_gating_identical_logits(cuda_device, E, k):
+    T = 777
+    L = I.make_logits(T, E, device="cpu", seed=E * 31 + k, ties=True)
+    s, ws = ws_for(T, 64, 64, E, k, cuda_device)
+    idx, w = B.moe_topk_gating(L.to(cuda_device), k, ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    ref_idx = O.topk(L.numpy(), k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    ref_w = O.gate_weights(L.numpy(), ref_idx)
+    assert np.abs(to64(w) - ref_w).max() <= 2e-6
+
+
+def test_topk_nan_is_reported(cuda_device):
+    T, E, k = 64, 16, 2
+    L = I.make_logits(T, E, seed=5, ties=False)
+    L[3, 7] = float("nan")
+    s, ws = ws_for(T, 64, 64, E, k, cuda_device)
+    idx, _ = B.moe_topk_gating(L.to(cuda_device), k, ws)
+    assert B.moe_check_device_status(ws, raise_on_error=False) == B.MOE_ERR_DEVICE_CHECK
+    assert 7 not in idx[3].tolist()
+
+
+# -------------------------------------------------------------- permutation
+@pytest.mark.parametrize("T,E,k,skew", [(1, 1, 1, 0.0), (777, 8, 2, 0.0), (3001, 64, 8, 1.2), (5000, 128, 8, 0.0),
+                                        (4099, 256, 8, 2.0), (999, 1024, 32, 0.0), (40, 3, 3, 0.0)])
+def test_permute_bit_exact(cuda_device, T, E, k, skew):
+    idx = I.make_topk_idx(T, E, k, seed=T * 7 + E, skew=skew)
+    w = I.make_gate_weights(T, k, seed=T)
+    s, ws = ws_for(T, 64, 64, E, k, cuda_device)
+    out = B.moe_permute(s, idx.to(cuda_device), w.to(cuda_device), ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    counts, offsets, src, dst = O.permute(idx.numpy(), E)
+    A = T * k
+    assert np.array_equal(out["counts"].cpu().numpy(), counts)
+    assert np.array_equal(out["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(out["src"][:A].cpu().numpy(), src)
+    assert np.array_equal(out["dst"].cpu().numpy(), dst)
+    assert np.array_equal(out["row_token"][:A].cpu().numpy(), src // k)
+    assert torch.equal(out["row_w"][:A].cpu(), w.reshape(-1)[torch.from_numpy(src)])
+
+
+def _synthetic_routing(T, E, k, seed, skew=0.0):
+    idx = I.make_topk_idx(T, E, k, seed=seed, skew=skew)
+    counts, offsets, src, dst = O.permute(idx.numpy(), E)
+    return idx, counts, offsets, src, dst
+
+
+# ------------------------------------------------------------ up-projection
+@pytest.mark.parametrize("gather", [True, False])
+@pytest.mark.parametrize("T,d,n,E,k,skew", [(700, 256, 192, 6, 2, 0.0), (600, 384, 256, 5, 3, 1.0),
+                                            (300, 128, 64, 8, 2, 0.0), (1100, 512, 128, 3, 1, 0.5)])
+def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=T + d + n)
+    idx, counts, offsets, src, dst = _synthetic_routing(T, E, k, seed=T + 1, skew=skew)
+    s, ws = ws_for(T, d, n, E, k, cuda_device)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    row_token = torch.from_numpy((src // k).astype(np.int32)).to(cuda_device)
+    h = B.moe_expert_up(s, inp["x"], W13p, torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
+                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=gather)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    A = T * k
+    h_gpu = to64(h[:A])
+    h_ref = np.zeros((A, n))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            h_ref[r0:r1] = O.expert_hidden(inp["x"][torch.from_numpy(src[r0:r1] // k).to(cuda_device)],
+                                           inp["W1"][e], inp["W3"][e])
+    assert_moe_close(h_gpu, h_ref, "h")
+
+
+# ---------------------------------------------------------- down-projection
+@pytest.mark.parametrize("T,d,n,E,k", [(700, 320, 128, 6, 2), (600, 384, 192, 5, 3), (500, 512, 64, 7, 2),
+                                       (256, 128, 64, 8, 2)])
+def test_expert_down_gate_weight(cuda_device, T, d, n, E, k):
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=d + n)
+    idx, counts, offsets, src, dst = _synthetic_routing(T, E, k, seed=T + 2)
+    A = T * k
+    g = torch.Generator(device="cpu").manual_seed(9)
+    h = torch.randn(A, n, generator=g).to(torch.bfloat16).to(cuda_device)
+    row_w = torch.rand(A, generator=g).to(cuda_device)
+    s, ws = ws_for(T, d, n, E, k, cuda_device)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    hcap = torch.zeros(B.moe_row_capacity(s), n, dtype=torch.bfloat16, device=cuda_device)
+    hcap[:A] = h
+    wcap = torch.zeros(B.moe_row_capacity(s), device=cuda_device)
+    wcap[:A] = row_w
+    ys = B.moe_expert_down(s, hcap, W2p, torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
+                           torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap, ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    ref = np.zeros((A, d))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = to64(row_w[r0:r1])[:, None] * O.expert_out(h[r0:r1], inp["W2"][e])
+    assert_moe_close(ys[:A], ref, "ys")
+
+
+# ------------------------------------------------------------------ combine
+@pytest.mark.parametrize("T,d,k", [(256, 128, 2), (1001, 512, 8), (3, 4096, 1)])
+def test_combine_fixed_k(cuda_device, T, d, k):
+    A = T * k
+    g = torch.Generator().manual_seed(T)
+    ys = torch.randn(A, d, generator=g).to(torch.bfloat16)
+    dst = torch.randperm(A, generator=g).to(torch.int32)
+    s = B.make_shape(T, d, 64, max(k, 1), k)
+    y = B.moe_combine(s, ys.to(cuda_device), None, dst.to(cuda_device))
+    ref = to64(ys)[dst.numpy().reshape(T, k)].sum(axis=1)
+    diff = np.abs(to64(y) - ref)
+    assert np.all(diff <= 2.0 ** -8 * np.abs(ref) + 1e-6 * k)
+
+
+def test_combine_csr_with_empty_tokens(cuda_device):
+    T, d, R = 50, 256, 120
+    g = torch.Generator().manual_seed(1)
+    lens = torch.randint(0, 5, (T,), generator=g)
+    lens[:3] = 0
+    lens[-1] = R - int(lens[:-1].sum()) if int(lens[:-1].sum()) < R else 0
+    tok_offsets = torch.cat([torch.zeros(1, dtype=torch.int64), lens.cumsum(0)]).to(torch.int32)
+    total = int(tok_offsets[-1])
+    ys = torch.randn(max(total, 1), d, generator=g).to(torch.bfloat16)
+    rows = torch.randperm(total, generator=g).to(torch.int32)
+    s = B.make_shape(T, d, 64, 8, 2)
+    y = B.moe_combine(s, ys.to(cuda_device), tok_offsets.to(cuda_device), rows.to(cuda_device))
+    y64 = to64(y)
+    for t in range(T):
+        r = rows[tok_offsets[t]:tok_offsets[t + 1]].numpy()
+        ref = to64(ys)[r].sum(axis=0) if r.size else np.zeros(d)
+        assert np.all(np.abs(y64[t] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+# ------------------------------------------------------------ whole layer
+def _forward_and_check(cfg, dev, seed=0, tokens=None, layer=None, inp=None):
+    if inp is None:
+        inp = I.make_inputs(cfg, device=dev, seed=seed)
+    if layer is None:
+        layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k)
+    y = layer.forward(inp["x"])
+    ws = layer.workspace(cfg.T, inp["x"].device)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    T = cfg.T
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    x_s = inp["x"][torch.from_numpy(toks).to(dev)]
+    L64 = O.router_logits(x_s, inp["Wr"], inp["bias"])
+    gpu_idx = ws.view("topk_idx", torch.int32, T * cfg.k).view(T, cfg.k)[torch.from_numpy(toks).to(dev)]
+    gpu_idx = gpu_idx.cpu().numpy()
+    robust = robust_tokens(L64, cfg.k, LOGIT_MARGIN)
+    # the selection is exact where fp32 rounding cannot decide it ...
+    ref_idx = O.topk(O.decision_logits(L64), cfg.k)
+    for i in np.flatnonzero(robust):
+        assert set(gpu_idx[i].tolist()) == set(ref_idx[i].tolist()), i
+    # ... and a valid top-k elsewhere
+    for i in np.flatnonzero(~robust):
+        assert valid_topk(L64[i], gpu_idx[i], LOGIT_MARGIN), i
+    keep = toks[robust]
+    y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k,
+                          tokens=keep)
+    y_gpu = y[torch.from_numpy(keep).to(dev)]
+    stats = assert_moe_close(y_gpu, y_ref)
+    return stats, float(robust.mean()), y
+
+
+def test_forward_tiny_config(cuda_device):
+    cfg = I.get_config("tiny")
+    stats, frac, _ = _forward_and_check(cfg, cuda_device)
+    assert frac > 0.95
+
+
+@pytest.mark.parametrize("T,d,n,E,k,bias", [(1000, 256, 192, 16, 4, True), (333, 128, 128, 9, 9, False),
+                                            (2049, 384, 256, 32, 8, True), (1, 64, 64, 4, 2, False),
+                                            (130, 64, 64, 1, 1, False)])
+def test_forward_ragged_shapes(cuda_device, T, d, n, E, k, bias):
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="normal" if bias else None, bias_scale=0.3)
+    _forward_and_check(cfg, cuda_device, seed=T + E)
+
+
+def test_forward_deterministic(cuda_device):
+    cfg = I.MoEConfig("t", T=1500, d=256, n=128, E=16, k=4)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=3)
+    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k)
+    y1 = layer.forward(inp["x"]).clone()
+    y2 = layer.forward(inp["x"]).clone()
+    assert torch.equal(y1, y2)
+
+
+def test_device_timeout_is_reported_and_context_survives(cuda_device):
+    cfg = I.get_config("tiny")
+    s, ws = ws_for(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cuda_device)
+    B.moe_selftest_timeout(ws, 2_000_000)   # 2 ms wait on a flag nobody sets
+    detail = torch.zeros(1)
+    st = B.moe_check_device_status(ws, raise_on_error=False)
+    assert st == B.MOE_ERR_TIMEOUT
+    assert B.moe_check_device_status(ws) == B.MOE_OK   # cleared by the read
+    _forward_and_check(cfg, cuda_device)                 # context still usable
+
+
+# ----------------------------------------------- full-size configurations
+# sampled tokens per configuration: bounded by the expert weights the fp64
+# oracle has to widen (every expert a sampled token uses)
+SAMPLE = {"mixtral": 48, "dsv3": 16, "b7": 64, "skew": 32}
+
+
+def _sample_tokens(T, size, seed):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(T, size=min(size, T), replace=False))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral", "dsv3", "b7", "skew"])
+def test_forward_full_size_sampled(cuda_device, name):
+    cfg = I.get_config(name)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=0)
+    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k)
+    toks = _sample_tokens(cfg.T, SAMPLE[name], 1)
+    stats, frac, y = _forward_and_check(cfg, cuda_device, tokens=toks, layer=layer, inp=inp)
+    assert frac > 0.9
+    # every token's output is finite and the whole batch is deterministic
+    assert torch.isfinite(y.float()).all()
+    y2 = layer.forward(inp["x"])
+    assert torch.equal(y, y2)
+    del layer, inp
+    torch.cuda.empty_cache()
