@@ -245,8 +245,8 @@ def run_ours(args, world, rank, local):
     tok_offsets = view("tok_offsets", torch.int32, T + 1)
     tok_rows = view("tok_rows", torch.int32, cap)
     h = view("h", torch.bfloat16, cap * n)
-    ys = view("ys", torch.bfloat16, cap * d)
-    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    ys = view("ys", torch.float16, cap * d)
+    y = torch.empty(T, d, dtype=torch.float32, device=dev)
     L = B.lib()
     import ctypes
     sp = ctypes.byref(shape)
@@ -254,7 +254,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     stages = ["route", "permute", "up", "down", "combine"]
-    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + 1 + 1
+    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + (0 if args.gather else 1) + 1 + 1
 
     def check(rc, what):
         if rc != 0:
@@ -276,7 +276,7 @@ def run_ours(args, world, rank, local):
             c_off, c_rows = tok_offsets, tok_rows
         if ev:
             ev[2].record(stream)
-        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(h), 1, ws.ptr,
+        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(h), args.gather, ws.ptr,
                               ws.nbytes, st), "up")
         if ev:
             ev[3].record(stream)
@@ -319,7 +319,7 @@ def run_ours(args, world, rank, local):
     # ------------------------------------------------ e2e: through moe_forward, host buffers
     x_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
-    y_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    y_host = torch.empty(T, d, dtype=torch.float32, pin_memory=True)
     x_dev = torch.empty_like(x)
     y_dev = torch.empty_like(y)
 
@@ -358,7 +358,7 @@ def run_ours(args, world, rank, local):
                 "algorithmic_flops_per_launch": up_flops}
     # HBM-bound stages: algorithmic bytes / time
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    comb_bytes = R * d * 2 + T * d * 2 + A * 4
+    comb_bytes = R * d * 2 + T * d * 4 + A * 4
     comb_gbs = comb_bytes / (statistics.mean(stage_ms["combine"]) * 1e-3) / 1e9
     down_flops = 2.0 * R * n * d
     stage_summary = {s: round(statistics.mean(v), 4) for s, v in stage_ms.items()}
@@ -373,6 +373,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
+                   "up_gather": "tma_gather4" if args.gather else "gather_kernel+tma",
                    "tile": cfg.tile if mode != "off" else None,
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},
@@ -381,7 +382,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline,
         "stages": extra,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "tokens_per_s": world * T * args.steps / (e2e_ms * 1e-3),
-                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 4},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -406,6 +407,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gather", type=int, default=1, choices=[0, 1],
+                    help="up-projection A operand: 1 = TMA gather4 of token rows, 0 = gather kernel then tiled TMA")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -14,6 +14,9 @@
  *   ys[r]  = w_r * (h[r] W2_e)                          down-projection    (moe_expert_down)
  *   y[t]   = sum over t's rows of ys[r], fixed order    combine            (moe_combine)
  *
+ * Precision: x, the expert weights and h are bf16; every product accumulates
+ * in fp32 (tensor memory); ys is stored as fp16 and y is fp32.
+ *
  * The gather of token rows into the up-projection and the SwiGLU activation
  * are fused into the grouped GEMM ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化",
  * sections "Gather 与加载融合" and the "关键 Kernel 对比" table).  The optional
@@ -169,14 +172,17 @@ int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int
                   void* ws, size_t ws_bytes, void* stream);
 
 /* Down-projection grouped GEMM with the gate weight in the epilogue:
- *   ys[r, :] = bf16( row_w[r] * (h[r] W2_e) ) for rows of expert e.
- *   h [cap, n] bf16; W2p from moe_prepare_weights; ys [cap, d] bf16. */
+ *   ys[r, :] = fp16( row_w[r] * (h[r] W2_e) ) for rows of expert e.
+ *   h [cap, n] bf16; W2p from moe_prepare_weights; ys [cap, d] fp16.
+ * A value beyond the fp16 range (|v| > 65504) is saturated and sets
+ * MOE_ERR_DEVICE_CHECK (detail 16) in the status word. */
 int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const int32_t* counts,
                     const int32_t* offsets, const float* row_w, void* ys, void* ws,
                     size_t ws_bytes, void* stream);
 
 /* Deterministic combine back to token order (自定义核与核融合 step 5):
- *   y[t, :] = bf16( sum over j of ys[row_j, :] ), fp32 sum in list order,
+ *   y[t, :] = sum over j of ys[row_j, :]: ys fp16 [cap, d], fp32 sum in list
+ *   order, y fp32 [T, d],
  * where t's rows are tok_rows[tok_offsets[t] .. tok_offsets[t+1]) or, when
  * tok_offsets is NULL, tok_rows[t*k .. t*k+k) (the `dst` array of
  * moe_permute).  A token with no rows gets y[t] = 0. */
@@ -185,7 +191,7 @@ int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets,
 
 /* The whole layer: route, (round), permute, up, down, combine.
  *   x [T, d] bf16, Wr [d, E] fp32, bias [E] fp32 or NULL,
- *   W13p, W2p from moe_prepare_weights, y [T, d] bf16 out.
+ *   W13p, W2p from moe_prepare_weights, y [T, d] fp32 out.
  * ws must hold moe_workspace_bytes(s) bytes. */
 int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                 const void* W13p, const void* W2p, void* y, void* ws, size_t ws_bytes,
@@ -196,7 +202,7 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
  * [0] logits f32[T*E]  [1] topk_idx i32[T*k]  [2] topk_w f32[T*k]
  * [3] counts i32[E]    [4] offsets i32[E+1]   [5] src i32[cap]  [6] dst i32[T*k]
  * [7] row_token i32[cap] [8] row_w f32[cap]   [9] tok_offsets i32[T+1]
- * [10] tok_rows i32[cap] [11] h bf16[cap*n]   [12] ys bf16[cap*d] */
+ * [10] tok_rows i32[cap] [11] h bf16[cap*n]   [12] ys fp16[cap*d] */
 int moe_workspace_layout(const moe_shape* s, int64_t* offsets_out, int32_t n_out);
 
 /* Self-test of the bounded-wait machinery: launches one block that waits on a

@@ -276,7 +276,7 @@ def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Worksp
     _need_cuda(h, W2p, counts, offsets, row_w)
     cap = moe_row_capacity(shape)
     if ys is None:
-        ys = torch.empty(cap, shape.d, dtype=torch.bfloat16, device=h.device)
+        ys = torch.empty(cap, shape.d, dtype=torch.float16, device=h.device)
     _check(lib().moe_expert_down(ctypes.byref(shape), _ptr(h), _ptr(W2p), _ptr(counts), _ptr(offsets),
                                  _ptr(row_w), _ptr(ys), ws.ptr, ws.nbytes, _stream(h.device)), "moe_expert_down")
     return ys
@@ -285,7 +285,7 @@ def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Worksp
 def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
     _need_cuda(ys, tok_offsets, tok_rows)
     if y is None:
-        y = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device=ys.device)
+        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=ys.device)
     _check(lib().moe_combine(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
                              _stream(ys.device)), "moe_combine")
     return y
@@ -294,7 +294,7 @@ def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
 def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
     _need_cuda(x, Wr, bias, W13p, W2p)
     if y is None:
-        y = torch.empty(shape.T, shape.d, dtype=torch.bfloat16, device=x.device)
+        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=x.device)
     _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p), _ptr(y),
                              ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward")
     return y

@@ -214,15 +214,15 @@ int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const in
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
   (void)ws_bytes;
   return launch_expert_down(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(W2p), counts,
-                            offsets, row_w, static_cast<__nv_bfloat16*>(ys), s->d, s->n, s->E, row_cap(s),
+                            offsets, row_w, static_cast<__half*>(ys), s->d, s->n, s->E, row_cap(s),
                             status_of(ws), kDefaultTimeoutNs, as_stream(stream));
 }
 
 int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets, const int32_t* tok_rows, void* y,
                 void* stream) {
   if (!shape_ok(s) || !ys || !tok_rows || !y || !aligned16(ys) || !aligned16(y)) return MOE_ERR_INVALID;
-  launch_combine(static_cast<const __nv_bfloat16*>(ys), tok_offsets, tok_rows, static_cast<__nv_bfloat16*>(y), s->T,
-                 s->d, s->k, as_stream(stream));
+  launch_combine(static_cast<const __half*>(ys), tok_offsets, tok_rows, static_cast<float*>(y), s->T, s->d, s->k,
+                 as_stream(stream));
   return last_launch();
 }
 

@@ -4,17 +4,18 @@
 // "MoE架构的物理瓶颈与扩展限制解析", section 工作原理, done in place on one GPU).
 //
 // The gate weight is already applied by the down-projection epilogue, so
-// y[t] = bf16( sum_j ys[row_j] ) with the fp32 sum in the token's list order:
-// deterministic, no atomics.  Each thread owns 8 columns (16-byte loads/stores).
+// y[t] = sum_j ys[row_j] (ys fp16, sum and y in fp32) in the token's list
+// order: deterministic, no atomics.  Each thread owns 8 columns: one 16-byte
+// load per row, two 16-byte stores.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
-__global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __restrict__ ys,
+__global__ void __launch_bounds__(256) combine_kernel(const __half* __restrict__ ys,
                                                       const int32_t* __restrict__ tok_offsets,
-                                                      const int32_t* __restrict__ tok_rows,
-                                                      __nv_bfloat16* __restrict__ y, int T, int d, int k) {
+                                                      const int32_t* __restrict__ tok_rows, float* __restrict__ y,
+                                                      int T, int d, int k) {
   const int groups = d / 8;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(T) * groups) return;
@@ -37,20 +38,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const __nv_bfloat16* __res
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      acc[2 * q] += bf16_lo(w[q]);
-      acc[2 * q + 1] += bf16_hi(w[q]);
+      const float2 f = unpack_half2(w[q]);
+      acc[2 * q] += f.x;
+      acc[2 * q + 1] += f.y;
     }
   }
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  reinterpret_cast<uint4*>(y + static_cast<int64_t>(t) * d)[g] = o;
+  float4* out = reinterpret_cast<float4*>(y + static_cast<int64_t>(t) * d) + 2 * g;
+  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-void launch_combine(const __nv_bfloat16* ys, const int32_t* tok_offsets, const int32_t* tok_rows,
-                    __nv_bfloat16* y, int T, int d, int k, cudaStream_t stream) {
+void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, float* y, int T, int d,
+                    int k, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * (d / 8);
   const int blocks = static_cast<int>((total + 255) / 256);
   combine_kernel<<<blocks, 256, 0, stream>>>(ys, tok_offsets, tok_rows, y, T, d, k);

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,7 +25,10 @@ enum : int32_t {
   kWaitMmaTmemEmpty = 3,
   kWaitEpiTmemFull = 4,
   kWaitSelftest = 5,
+  kYsOverflow = 16,  // a down-projection output exceeded the fp16 range
 };
+
+constexpr float kHalfMax = 65504.0f;
 
 __device__ __forceinline__ void report_error(int32_t* status, int32_t code, int32_t detail) {
   if (status == nullptr) return;
@@ -221,6 +225,15 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_half2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<__half2*>(&v));
 }
 
 }  // namespace moe

@@ -1,7 +1,7 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // Up-projection:   h[r]  = bf16( silu(x[t_r] W1_e) * (x[t_r] W3_e) )
-// Down-projection: ys[r] = bf16( w_r * (h[r] W2_e) )
+// Down-projection: ys[r] = fp16( w_r * (h[r] W2_e) )
 //
 // The row gather is fused into the operand load, the SwiGLU activation and the
 // gate weight into the epilogue, and loads overlap the MMAs ("SonicMoE: 加速
@@ -38,7 +38,8 @@ struct GemmParams {
   const int32_t* offsets;    // [E+1]
   const int32_t* row_token;  // [cap] token of each row (gathered A only)
   const float* row_w;        // [cap] gate weight of each row (down only)
-  __nv_bfloat16* out;        // [cap, out_ld]
+  __nv_bfloat16* out;        // up: h [cap, out_ld] bf16
+  __half* out_h;             // down: ys [cap, out_ld] fp16
   int64_t out_ld;
   int E;
   int num_kb;                // K / 64
@@ -271,8 +272,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       } else {
+        // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
+        // same traffic); values past the fp16 range saturate and are reported
         const float wr = valid ? p.row_w[row] : 0.f;
-        __nv_bfloat16* dst = p.out + row * p.out_ld + static_cast<int64_t>(nb) * BN;
+        __half* dst = p.out_h + row * p.out_ld + static_cast<int64_t>(nb) * BN;
+        bool overflow = false;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t v[32];
@@ -280,14 +284,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_wait_ld();
           uint32_t o[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            o[q] = pack_bf16x2(wr * __uint_as_float(v[2 * q]), wr * __uint_as_float(v[2 * q + 1]));
+          for (int q = 0; q < 16; ++q) {
+            float a = wr * __uint_as_float(v[2 * q]), b = wr * __uint_as_float(v[2 * q + 1]);
+            overflow |= !(fabsf(a) <= kHalfMax) || !(fabsf(b) <= kHalfMax);
+            a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
+            b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
+            o[q] = pack_half2(a, b);
+          }
           if (valid) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
             for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
         }
+        if (overflow && valid) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
       }
       tc_fence_before();
       __syncwarp();
@@ -400,6 +410,7 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   p.row_token = row_token;
   p.row_w = nullptr;
   p.out = h;
+  p.out_h = nullptr;
   p.out_ld = n;
   p.E = E;
   p.num_kb = d / 64;
@@ -413,7 +424,7 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
-                       const int32_t* offsets, const float* row_w, __nv_bfloat16* ys, int d, int n, int E,
+                       const int32_t* offsets, const float* row_w, __half* ys, int d, int n, int E,
                        int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
   const int BN = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   CUtensorMap tmA, tmB;
@@ -424,7 +435,8 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.offsets = offsets;
   p.row_token = nullptr;
   p.row_w = row_w;
-  p.out = ys;
+  p.out = nullptr;
+  p.out_h = ys;
   p.out_ld = d;
   p.E = E;
   p.num_kb = n / 64;

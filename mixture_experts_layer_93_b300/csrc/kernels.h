@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,15 +35,15 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
                      int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
                      uint64_t timeout_ns, cudaStream_t stream);
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
-                       const int32_t* offsets, const float* row_w, __nv_bfloat16* ys, int d, int n, int E,
+                       const int32_t* offsets, const float* row_w, __half* ys, int d, int n, int E,
                        int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const int32_t* offsets, int E, int d,
                         __nv_bfloat16* out, int64_t rows_cap, cudaStream_t stream);
 inline int up_half_block(int n) { return (n % 128 == 0) ? 128 : 64; }
 
 // combine.cu
-void launch_combine(const __nv_bfloat16* ys, const int32_t* tok_offsets, const int32_t* tok_rows,
-                    __nv_bfloat16* y, int T, int d, int k, cudaStream_t stream);
+void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, float* y, int T, int d,
+                    int k, cudaStream_t stream);
 
 // prepare.cu
 void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, const __nv_bfloat16* W2,

@@ -111,7 +111,10 @@ def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
         if r1 > r0:
             h_ref[r0:r1] = O.expert_hidden(inp["x"][torch.from_numpy(src[r0:r1] // k).to(cuda_device)],
                                            inp["W1"][e], inp["W3"][e])
-    assert_moe_close(h_gpu, h_ref, "h")
+    # h is a bf16 intermediate: within one bf16 rounding (2^-8 relative) of
+    # the exact value, plus fp32 accumulation noise
+    rms = float(np.sqrt(np.mean(h_ref ** 2)))
+    assert np.all(np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-5 * rms), err_stats(h_gpu, h_ref)
 
 
 # ---------------------------------------------------------- down-projection
@@ -139,7 +142,10 @@ def test_expert_down_gate_weight(cuda_device, T, d, n, E, k):
         r0, r1 = offsets[e], offsets[e + 1]
         if r1 > r0:
             ref[r0:r1] = to64(row_w[r0:r1])[:, None] * O.expert_out(h[r0:r1], inp["W2"][e])
-    assert_moe_close(ys[:A], ref, "ys")
+    # ys is an fp16 intermediate: within one fp16 rounding (2^-11 relative)
+    got = to64(ys[:A])
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-5 * rms), err_stats(got, ref)
 
 
 # ------------------------------------------------------------------ combine
@@ -147,13 +153,15 @@ def test_expert_down_gate_weight(cuda_device, T, d, n, E, k):
 def test_combine_fixed_k(cuda_device, T, d, k):
     A = T * k
     g = torch.Generator().manual_seed(T)
-    ys = torch.randn(A, d, generator=g).to(torch.bfloat16)
+    ys = torch.randn(A, d, generator=g).to(torch.float16)
     dst = torch.randperm(A, generator=g).to(torch.int32)
     s = B.make_shape(T, d, 64, max(k, 1), k)
     y = B.moe_combine(s, ys.to(cuda_device), None, dst.to(cuda_device))
-    ref = to64(ys)[dst.numpy().reshape(T, k)].sum(axis=1)
+    parts = to64(ys)[dst.numpy().reshape(T, k)]
+    ref = parts.sum(axis=1)
     diff = np.abs(to64(y) - ref)
-    assert np.all(diff <= 2.0 ** -8 * np.abs(ref) + 1e-6 * k)
+    # fp32 sum of k terms: k * 2^-24 * sum |terms|
+    assert np.all(diff <= k * 2.0 ** -24 * np.abs(parts).sum(axis=1))
 
 
 def test_combine_csr_with_empty_tokens(cuda_device):
@@ -164,7 +172,7 @@ def test_combine_csr_with_empty_tokens(cuda_device):
     lens[-1] = R - int(lens[:-1].sum()) if int(lens[:-1].sum()) < R else 0
     tok_offsets = torch.cat([torch.zeros(1, dtype=torch.int64), lens.cumsum(0)]).to(torch.int32)
     total = int(tok_offsets[-1])
-    ys = torch.randn(max(total, 1), d, generator=g).to(torch.bfloat16)
+    ys = torch.randn(max(total, 1), d, generator=g).to(torch.float16)
     rows = torch.randperm(total, generator=g).to(torch.int32)
     s = B.make_shape(T, d, 64, 8, 2)
     y = B.moe_combine(s, ys.to(cuda_device), tok_offsets.to(cuda_device), rows.to(cuda_device))
@@ -172,7 +180,8 @@ def test_combine_csr_with_empty_tokens(cuda_device):
     for t in range(T):
         r = rows[tok_offsets[t]:tok_offsets[t + 1]].numpy()
         ref = to64(ys)[r].sum(axis=0) if r.size else np.zeros(d)
-        assert np.all(np.abs(y64[t] - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+        bound = len(r) * 2.0 ** -24 * np.abs(to64(ys)[r]).sum(axis=0) if r.size else 0.0
+        assert np.all(np.abs(y64[t] - ref) <= bound)
 
 
 # ------------------------------------------------------------ whole layer
