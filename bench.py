@@ -254,7 +254,7 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     stages = ["route", "permute", "up", "down", "combine"]
-    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + (0 if args.gather else 1) + 1 + 1
+    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + (1 if args.gather == 0 else 0) + 1 + 1
 
     def check(rc, what):
         if rc != 0:
@@ -373,7 +373,7 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
-                   "up_gather": "tma_gather4" if args.gather else "gather_kernel+tma",
+                   "up_gather": ["gather_kernel+tma", "tma_gather4", "cp_async"][args.gather],
                    "tile": cfg.tile if mode != "off" else None,
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},
@@ -407,8 +407,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gather", type=int, default=1, choices=[0, 1],
-                    help="up-projection A operand: 1 = TMA gather4 of token rows, 0 = gather kernel then tiled TMA")
+    ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
+                    help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
+                         "rows, 2 = per-lane cp.async of token rows")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":

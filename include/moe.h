@@ -114,7 +114,10 @@ int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, cons
 
 /* Router logits (gate network; "MoE架构的物理瓶颈与扩展限制解析", 工作原理 step 1):
  *   logits[T, E] fp32 = float(x[T, d] bf16) @ Wr[d, E] fp32 + bias[E] fp32.
- * bias may be NULL.  fp32 accumulation. */
+ * bias may be NULL.  Runs on the tensor cores: Wr is split into three bf16
+ * terms hi + mid + lo (equal to Wr within 2^-27 relative; the split is kept
+ * in the workspace, which must hold moe_workspace_bytes(s) bytes), each
+ * product with the bf16 x is exact and accumulates in fp32. */
 int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                       float* logits, void* ws, void* stream);
 
@@ -165,8 +168,12 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
  *     h[r, :] = bf16( silu(x[row_token[r]] W1_e) * (x[row_token[r]] W3_e) )
  *   silu(z) = z / (1 + exp(-z)); fp32 accumulation in tensor memory.
  *   x [T, d] bf16; W13p from moe_prepare_weights; h [moe_row_capacity, n] bf16.
- * gather: 0 = rows fetched by TMA gather (4 rows per copy) straight into
- * shared memory; 1 = rows first copied into the workspace, then tiled TMA. */
+ * gather selects how token rows reach shared memory:
+ *   0 = a gather kernel copies the rows into the workspace (ys region), then
+ *       tiled TMA loads them;
+ *   1 = TMA tile::gather4 (four token rows per copy) straight from x;
+ *   2 = per-lane 16-byte cp.async straight from x into the swizzled tile.
+ * Any other value returns MOE_ERR_INVALID. */
 int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int32_t* counts,
                   const int32_t* offsets, const int32_t* row_token, void* h, int gather,
                   void* ws, size_t ws_bytes, void* stream);

@@ -186,14 +186,14 @@ def moe_prepare_weights(W1, W3, W2):
     return W13p, W2p
 
 
-def moe_router_logits(x, Wr, bias=None, ws: Workspace | None = None):
+def moe_router_logits(x, Wr, bias, ws: Workspace):
     _need_cuda(x, Wr, bias)
     T, d = x.shape
     E = Wr.shape[1]
     shape = make_shape(T, d, 64, E, 1)
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device)
     _check(lib().moe_router_logits(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(logits),
-                                   ws.ptr if ws else None, _stream(x.device)), "moe_router_logits")
+                                   ws.ptr, _stream(x.device)), "moe_router_logits")
     return logits
 
 
@@ -260,14 +260,14 @@ def moe_token_round(shape: moe_shape, logits, topk_idx, ws: Workspace) -> dict:
     return out
 
 
-def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Workspace, gather: bool = True,
+def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Workspace, gather: int = 2,
                   h=None):
     _need_cuda(x, W13p, counts, offsets, row_token)
     cap = moe_row_capacity(shape)
     if h is None:
         h = torch.empty(cap, shape.n, dtype=torch.bfloat16, device=x.device)
     _check(lib().moe_expert_up(ctypes.byref(shape), _ptr(x), _ptr(W13p), _ptr(counts), _ptr(offsets),
-                               _ptr(row_token), _ptr(h), 1 if gather else 0, ws.ptr, ws.nbytes,
+                               _ptr(row_token), _ptr(h), int(gather), ws.ptr, ws.nbytes,
                                _stream(x.device)), "moe_expert_up")
     return h
 

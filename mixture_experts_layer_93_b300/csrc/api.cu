@@ -35,7 +35,7 @@ inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
 
 enum Slot {
   kLogits, kTopkIdx, kTopkW, kCounts, kOffsets, kSrc, kDst, kRowToken, kRowW, kTokOffsets, kTokRows, kH, kYs,
-  kPermHist, kRoundScratch, kNumSlots
+  kPermHist, kRoundScratch, kRouterW, kNumSlots
 };
 
 // Byte offsets of each array in the workspace; returns the total size.
@@ -45,7 +45,8 @@ int64_t layout(const moe_shape* s, int64_t* off) {
       T * E * 4,          A * 4,     A * 4,     E * 4,   (E + 1) * 4,       cap * 4,
       A * 4,              cap * 4,   cap * 4,   (T + 1) * 4, cap * 4,       cap * s->n * 2,
       cap * s->d * 2,     E * perm_num_chunks(cap) * 4,
-      s->round != MOE_ROUND_OFF ? static_cast<int64_t>(round_scratch_bytes(s->T, s->E, s->k, s->tile)) : 0};
+      s->round != MOE_ROUND_OFF ? static_cast<int64_t>(round_scratch_bytes(s->T, s->E, s->k, s->tile)) : 0,
+      static_cast<int64_t>(router_split_elems(s->d, s->E)) * 2};
   int64_t pos = static_cast<int64_t>(kStatusBytes);
   for (int i = 0; i < kNumSlots; ++i) {
     off[i] = pos;
@@ -64,6 +65,9 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 inline int last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 inline int32_t* status_of(void* ws) { return reinterpret_cast<int32_t*>(ws); }
+
+// A-operand path moe_forward uses for the up-projection (see moe_expert_up).
+constexpr int kForwardGather = 0;
 
 int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
@@ -139,10 +143,14 @@ int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, cons
 
 int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
                       void* ws, void* stream) {
-  (void)ws;
-  if (!shape_ok(s) || !x || !Wr || !logits || !aligned16(x)) return MOE_ERR_INVALID;
-  launch_router_logits(static_cast<const __nv_bfloat16*>(x), Wr, bias, logits, s->T, s->d, s->E, as_stream(stream));
-  return last_launch();
+  if (!shape_ok(s) || !x || !Wr || !logits || !ws || !aligned16(x) || !aligned16(ws)) return MOE_ERR_INVALID;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
+  launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream));
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E, status_of(ws),
+                          kDefaultTimeoutNs, as_stream(stream));
 }
 
 int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, float* topk_w, void* ws,
@@ -194,6 +202,7 @@ int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int
                   const int32_t* row_token, void* h, int gather, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !x || !W13p || !counts || !offsets || !row_token || !h) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(W13p) || !aligned16(h)) return MOE_ERR_INVALID;
+  if (gather < 0 || gather > 2) return MOE_ERR_INVALID;
   const int st = check_ws(s, ws, ws_bytes);
   if (st != MOE_OK) return st;
   int64_t off[kNumSlots];
@@ -202,7 +211,7 @@ int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int
   // the forward only writes after the up-projection
   return launch_expert_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(W13p), counts,
                           offsets, row_token, static_cast<__nv_bfloat16*>(h), s->T, s->d, s->n, s->E, row_cap(s),
-                          gather ? 1 : 0, at<__nv_bfloat16>(ws, off[kYs]), status_of(ws), kDefaultTimeoutNs,
+                          gather, at<__nv_bfloat16>(ws, off[kYs]), status_of(ws), kDefaultTimeoutNs,
                           as_stream(stream));
 }
 
@@ -261,7 +270,8 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
     combine_offsets = tok_offsets;
     combine_rows = tok_rows;
   }
-  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, h, 1, ws, ws_bytes, stream)) != MOE_OK) return st;
+  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, h, kForwardGather, ws, ws_bytes, stream)) != MOE_OK)
+    return st;
   if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
 }

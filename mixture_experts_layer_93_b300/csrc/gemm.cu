@@ -1,23 +1,27 @@
-// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+// Grouped GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // Up-projection:   h[r]  = bf16( silu(x[t_r] W1_e) * (x[t_r] W3_e) )
 // Down-projection: ys[r] = fp16( w_r * (h[r] W2_e) )
+// Router:          L[t]  = x[t] Wr + b, with Wr split exactly into three
+//                  bf16 terms (hi, mid, lo) held as three column groups of B
 //
 // The row gather is fused into the operand load, the SwiGLU activation and the
 // gate weight into the epilogue, and loads overlap the MMAs ("SonicMoE: 加速
 // MoE 模型的 IO 与 Tile 感知优化": sections "2. IO 与计算重叠的 GPU Kernel",
 // "Gather 与加载融合" and the "关键 Kernel 对比" table, rows "Gather 融合",
 // "SwiGLU 融合", "MMA 与 IO 重叠").  The page's kernels use cp.async on
-// Hopper; here the same roles map onto Blackwell hardware:
+// Hopper; here the roles map onto Blackwell hardware:
 //
-//   warp 0      TMA producer.  A rows come either by `tile::gather4` (four
-//               arbitrary token rows per copy, 32 lanes x 4 = 128 rows per
-//               tile) or by a tiled 2-D copy of contiguous rows; B tiles by a
-//               tiled 2-D copy.  128-byte swizzle, a ring of STAGES slots.
-//   warp 1      TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=BN,
-//               K=16, bf16 -> fp32) and tcgen05.commit to free slots.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (each warp owns
-//               32 TMEM lanes = 32 rows), fused SwiGLU or gate scaling, bf16
+//   warps 0..3  producers.  B tiles (and A tiles of contiguous rows) come by
+//               tiled TMA, issued by warp 0.  Gathered A rows come either by
+//               TMA `tile::gather4` (warp 0, four token rows per copy) or by
+//               16-byte cp.async from all four warps, written straight into
+//               the 128-byte-swizzled layout, each lane arriving on the stage
+//               barrier when its copies land (non-blocking).
+//   warp 4      TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=BN,
+//               K=16, bf16 -> fp32 in tensor memory) and tcgen05.commit.
+//   warps 5..8  epilogue: tcgen05.ld of the accumulator (warp w owns TMEM
+//               lanes 32*(w%4)..+31 = 32 rows), fused activation / scaling,
 //               stores.  Two accumulators in TMEM so the epilogue of one tile
 //               overlaps the MMAs of the next.
 //
@@ -29,26 +33,42 @@
 #include "common.cuh"
 #include "kernels.h"
 
-#include <mutex>
+#include <algorithm>
 
 namespace moe {
 
+enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2 };
+
 struct GemmParams {
-  const int32_t* counts;     // [E]
-  const int32_t* offsets;    // [E+1]
+  const int32_t* counts;     // [E] rows per group (ignored when single_rows > 0)
+  const int32_t* offsets;    // [E+1] first row of each group
+  int single_rows;           // > 0: one group of this many rows starting at row 0
   const int32_t* row_token;  // [cap] token of each row (gathered A only)
-  const float* row_w;        // [cap] gate weight of each row (down only)
-  __nv_bfloat16* out;        // up: h [cap, out_ld] bf16
-  __half* out_h;             // down: ys [cap, out_ld] fp16
+  const float* row_w;        // [cap] gate weight of each row (down)
+  const float* bias;         // [E_out] router bias or nullptr
+  __nv_bfloat16* out_bf16;   // up: h [cap, out_ld]
+  __half* out_f16;           // down: ys [cap, out_ld]
+  float* out_f32;            // router: logits [T, out_ld]
   int64_t out_ld;
-  int E;
+  int out_cols;              // router: number of valid output columns (E)
+  int E;                     // groups
   int num_kb;                // K / 64
-  int n_blocks;              // N tiles per expert
-  int b_rows_per_expert;     // rows of packed B per expert
-  int gather;                // 1: A rows gathered by token id, 0: contiguous rows
+  int n_blocks;              // N tiles per group
+  int b_rows_per_expert;     // rows of packed B per group
+  int gather;                // A rows: 0 contiguous (tiled TMA), 1 TMA gather4 by token,
+                             // 2 16-byte cp.async by token
+  const __nv_bfloat16* x;    // gather 2: token rows
+  int64_t lda;
   int32_t* status;
   uint64_t timeout_ns;
 };
+
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = 4;
+constexpr int kEpiWarp0 = 5;
+constexpr int kGemmThreads = 9 * 32;
+
+__host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 256 ? 256 : 512))); }
 
 template <int BN>
 struct GemmCfg {
@@ -56,14 +76,14 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  static constexpr int TMEM_COLS = tmem_cols_for(2 * BN);
   static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
   static constexpr int PREFIX_BYTES = 1025 * 4;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES;
+  static constexpr int TOK_BYTES = BM * 4;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES;
+  static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
 };
-
-constexpr int kGemmThreads = 192;
 
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
                                             int& mb) {
@@ -82,7 +102,17 @@ __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int 
   mb = local - nb * me;
 }
 
-template <int BN, int MODE>  // MODE 0: up-projection + SwiGLU, MODE 1: down-projection + gate weight
+__device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_start, int& count) {
+  if (p.single_rows > 0) {
+    row_start = 0;
+    count = p.single_rows;
+  } else {
+    row_start = p.offsets[e];
+    count = p.counts[e];
+  }
+}
+
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
@@ -99,12 +129,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(base + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+  int32_t* tok_s = prefix + 1025;  // gather 2: token of each row of the current tile
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_groups = p.single_rows > 0 ? 1 : p.E;
 
   if (warp == 0 && lane == 0) {
+    // gather 2: one arrival per producer lane (when its copies land) plus
+    // warp 0's expect-tx arrival for the B tile
+    const uint32_t full_count = p.gather == 2 ? 1 + 32 * kProducerWarps : 1;
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&full_bar[s]), full_count);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -115,78 +150,109 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
     tmem_relinquish();
     tc_fence_before();
-  } else if (warp == 2) {
-    // prefix[e] = number of 128-row tiles of experts < e
-    int running = 0;
-    if (lane == 0) prefix[0] = 0;
-    for (int b = 0; b < p.E; b += 32) {
-      const int e = b + lane;
-      int m = 0;
-      if (e < p.E) m = (p.counts[e] + C::BM - 1) / C::BM;
-      int incl = m;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+  } else if (warp == kEpiWarp0) {
+    // prefix[e] = number of 128-row tiles of groups < e
+    if (p.single_rows > 0) {
+      if (lane == 0) {
+        prefix[0] = 0;
+        prefix[1] = (p.single_rows + C::BM - 1) / C::BM;
       }
-      if (e < p.E) prefix[e + 1] = running + incl;
-      running += __shfl_sync(0xffffffffu, incl, 31);
+    } else {
+      int running = 0;
+      if (lane == 0) prefix[0] = 0;
+      for (int b = 0; b < p.E; b += 32) {
+        const int e = b + lane;
+        int m = 0;
+        if (e < p.E) m = (p.counts[e] + C::BM - 1) / C::BM;
+        int incl = m;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (e < p.E) prefix[e + 1] = running + incl;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total_tiles = prefix[p.E] * p.n_blocks;
+  const int total_tiles = prefix[n_groups] * p.n_blocks;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol_a = policy_evict_last();    // A rows are re-read by every n-block
-    const uint64_t pol_b = policy_evict_normal();  // B tiles are re-read by the m-blocks of one expert
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
-      int e, nb, mb;
-      decode_tile(tau, prefix, p.E, p.n_blocks, e, nb, mb);
-      const int row0 = p.offsets[e] + mb * C::BM;
-      const int rows_valid = min(C::BM, p.counts[e] - mb * C::BM);
-      int tok[4] = {0, 0, 0, 0};
-      if (p.gather) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tok[q] = p.row_token[row0 + min(lane * 4 + q, rows_valid - 1)];
-      }
-      const int brow = e * p.b_rows_per_expert + nb * BN;
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    const bool issuer = (warp == 0);
+    if (issuer || p.gather == 2) {
+      const uint64_t pol_a = policy_evict_last();    // A rows are re-read by every n-block
+      const uint64_t pol_b = policy_evict_normal();  // B tiles are re-read by the m-blocks of one group
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        int w = 1;
-        if (lane == 0)
-          w = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status, kWaitProducerEmpty,
-                                p.timeout_ns);
-        if (!__shfl_sync(0xffffffffu, w, 0)) {
-          ok = false;
-          break;
+      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
+        int e, nb, mb, gstart, gcount;
+        decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mb);
+        group_rows(p, e, gstart, gcount);
+        const int row0 = gstart + mb * C::BM;
+        const int rows_valid = min(C::BM, gcount - mb * C::BM);
+        int tok[4] = {0, 0, 0, 0};
+        if (p.gather == 1) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) tok[q] = p.row_token[row0 + min(lane * 4 + q, rows_valid - 1)];
+        } else if (p.gather == 2) {
+          // this warp's 32 rows; rows past the group repeat its last row
+          __syncwarp();
+          const int r = warp * 32 + lane;
+          tok_s[r] = p.row_token[row0 + min(r, rows_valid - 1)];
+          __syncwarp();
         }
-        const uint32_t fb = smem_u32(&full_bar[stage]);
-        if (lane == 0) mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        __syncwarp();
-        const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
-        if (p.gather) {
-          tma_gather4(a_dst + lane * 512, &tmA, kb * C::BK, tok[0], tok[1], tok[2], tok[3], fb, pol_a);
-        } else if (lane == 0) {
-          tma_load_2d(a_dst, &tmA, kb * C::BK, row0, fb, pol_a);
-        }
-        if (lane == 0) tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * C::BK, brow, fb, pol_b);
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        const int brow = e * p.b_rows_per_expert + nb * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          int w = 1;
+          if (lane == 0)
+            w = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status,
+                                  kWaitProducerEmpty, p.timeout_ns);
+          if (!__shfl_sync(0xffffffffu, w, 0)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
+          if (issuer) {
+            if (lane == 0) mbar_arrive_expect_tx(fb, p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES);
+            __syncwarp();
+            if (p.gather == 1) {
+              tma_gather4(a_dst + lane * 512, &tmA, kb * C::BK, tok[0], tok[1], tok[2], tok[3], fb, pol_a);
+            } else if (p.gather == 0 && lane == 0) {
+              tma_load_2d(a_dst, &tmA, kb * C::BK, row0, fb, pol_a);
+            }
+            if (lane == 0) tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * C::BK, brow, fb, pol_b);
+          }
+          if (p.gather == 2) {
+            // lane owns 16-byte chunk c of rows r = 32*warp + lane/8 + 4i; the
+            // chunk goes to its swizzled slot (c ^ (r mod 8)) of row r
+            const int c = lane & 7;
+            const __nv_bfloat16* xk = p.x + static_cast<int64_t>(kb) * C::BK + c * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = warp * 32 + (lane >> 3) + 4 * i;
+              cp_async_16(a_dst + r * 128 + ((c ^ (r & 7)) << 4), xk + static_cast<int64_t>(tok_s[r]) * p.lda);
+            }
+            cp_async_arrive_noinc(fb);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-      if (!ok) break;
+      if (p.gather == 2) cp_async_wait_all();  // nothing of ours in flight at exit
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(C::BM, BN);
@@ -207,6 +273,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          // A rows written by cp.async (generic proxy) become visible to
+          // the tensor core's operand reads (async proxy)
+          if (p.gather == 2) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
@@ -234,10 +303,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
-      int e, nb, mb;
-      decode_tile(tau, prefix, p.E, p.n_blocks, e, nb, mb);
-      const int row0 = p.offsets[e] + mb * C::BM;
-      const int rows_valid = min(C::BM, p.counts[e] - mb * C::BM);
+      int e, nb, mb, gstart, gcount;
+      decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mb);
+      group_rows(p, e, gstart, gcount);
+      const int row0 = gstart + mb * C::BM;
+      const int rows_valid = min(C::BM, gcount - mb * C::BM);
       int w = 1;
       if (lane == 0)
         w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
@@ -247,9 +317,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const bool valid = r_in_tile < rows_valid;
       const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
-      if constexpr (MODE == 0) {
+      if constexpr (MODE == kModeUp) {
         constexpr int H = BN / 2;
-        __nv_bfloat16* dst = p.out + row * p.out_ld + static_cast<int64_t>(nb) * H;
+        __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
 #pragma unroll 1
         for (int c = 0; c < H; c += 32) {
           uint32_t g[32], u[32];
@@ -271,11 +341,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
           }
         }
-      } else {
+      } else if constexpr (MODE == kModeDown) {
         // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
         // same traffic); values past the fp16 range saturate and are reported
         const float wr = valid ? p.row_w[row] : 0.f;
-        __half* dst = p.out_h + row * p.out_ld + static_cast<int64_t>(nb) * BN;
+        __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
         bool overflow = false;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
@@ -298,6 +368,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (overflow && valid) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
+      } else {
+        // router: the three column groups hold x*hi, x*mid, x*lo of the same
+        // EB experts; their fp32 sum plus the bias is the logit
+        constexpr int EB = BN / 3;
+        const int e0 = nb * EB;
+        float* dst = p.out_f32 + row * p.out_ld;
+#pragma unroll 1
+        for (int c = 0; c < EB; c += 16) {
+          uint32_t a[16], b[16], q[16];
+          tmem_ld16(taddr + c, a);
+          tmem_ld16(taddr + EB + c, b);
+          tmem_ld16(taddr + 2 * EB + c, q);
+          tc_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int ecol = e0 + c + j;
+              if (ecol < p.out_cols) {
+                float v = (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(q[j]);
+                if (p.bias) v += p.bias[ecol];
+                dst[ecol] = v;
+              }
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -317,7 +412,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncthreads();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
@@ -354,7 +449,7 @@ static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint6
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int num_sms() {
+int num_sms() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -390,6 +485,13 @@ void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const 
   gather_rows_kernel<<<num_sms() * 8, 256, 0, stream>>>(x, row_token, offsets, E, d, out, rows_cap);
 }
 
+static GemmParams base_params(int32_t* status, uint64_t timeout_ns) {
+  GemmParams p{};
+  p.status = status;
+  p.timeout_ns = timeout_ns;
+  return p;
+}
+
 int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
                      const int32_t* offsets, const int32_t* row_token, __nv_bfloat16* h, int T, int d, int n, int E,
                      int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
@@ -397,30 +499,30 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   const int H = up_half_block(n);
   const int BN = 2 * H;
   CUtensorMap tmA, tmB;
-  if (gather) {
+  if (gather == 1) {
     if (!make_map_bf16(&tmA, x, d, T, 1)) return MOE_ERR_CUDA;
+  } else if (gather == 2) {
+    if (!make_map_bf16(&tmA, x, d, T, 128)) return MOE_ERR_CUDA;  // not read by the kernel
   } else {
     launch_gather_rows(x, row_token, offsets, E, d, xperm_scratch, rows_cap, stream);
     if (!make_map_bf16(&tmA, xperm_scratch, d, rows_cap, 128)) return MOE_ERR_CUDA;
   }
   if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
-  GemmParams p{};
+  GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
   p.row_token = row_token;
-  p.row_w = nullptr;
-  p.out = h;
-  p.out_h = nullptr;
+  p.out_bf16 = h;
   p.out_ld = n;
   p.E = E;
   p.num_kb = d / 64;
   p.n_blocks = n / H;
   p.b_rows_per_expert = 2 * n;
-  p.gather = gather ? 1 : 0;
-  p.status = status;
-  p.timeout_ns = timeout_ns;
-  if (BN == 256) return launch_gemm<256, 0>(tmA, tmB, p, stream);
-  return launch_gemm<128, 0>(tmA, tmB, p, stream);
+  p.gather = gather;
+  p.x = x;
+  p.lda = d;
+  if (BN == 256) return launch_gemm<256, kModeUp>(tmA, tmB, p, stream);
+  return launch_gemm<128, kModeUp>(tmA, tmB, p, stream);
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
@@ -430,24 +532,86 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, h, n, rows_cap, 128)) return MOE_ERR_CUDA;
   if (!make_map_bf16(&tmB, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;
-  GemmParams p{};
+  GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
-  p.row_token = nullptr;
   p.row_w = row_w;
-  p.out = nullptr;
-  p.out_h = ys;
+  p.out_f16 = ys;
   p.out_ld = d;
   p.E = E;
   p.num_kb = n / 64;
   p.n_blocks = d / BN;
   p.b_rows_per_expert = d;
   p.gather = 0;
-  p.status = status;
-  p.timeout_ns = timeout_ns;
-  if (BN == 256) return launch_gemm<256, 1>(tmA, tmB, p, stream);
-  if (BN == 128) return launch_gemm<128, 1>(tmA, tmB, p, stream);
-  return launch_gemm<64, 1>(tmA, tmB, p, stream);
+  if (BN == 256) return launch_gemm<256, kModeDown>(tmA, tmB, p, stream);
+  if (BN == 128) return launch_gemm<128, kModeDown>(tmA, tmB, p, stream);
+  return launch_gemm<64, kModeDown>(tmA, tmB, p, stream);
+}
+
+int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }
+
+int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
+                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  const int EB = router_expert_block(E);
+  const int BN = 3 * EB;
+  const int nblk = (E + EB - 1) / EB;
+  CUtensorMap tmA, tmB;
+  if (!make_map_bf16(&tmA, x, d, T, 128)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, Wr3, d, static_cast<uint64_t>(nblk) * BN, BN)) return MOE_ERR_CUDA;
+  GemmParams p = base_params(status, timeout_ns);
+  p.single_rows = T;
+  p.bias = bias;
+  p.out_f32 = logits;
+  p.out_ld = E;
+  p.out_cols = E;
+  p.E = 1;
+  p.num_kb = d / 64;
+  p.n_blocks = nblk;
+  p.b_rows_per_expert = 0;
+  p.gather = 0;
+  if (BN == 48) return launch_gemm<48, kModeRouter>(tmA, tmB, p, stream);
+  if (BN == 96) return launch_gemm<96, kModeRouter>(tmA, tmB, p, stream);
+  return launch_gemm<192, kModeRouter>(tmA, tmB, p, stream);
+}
+
+// Wr [d, E] fp32 -> Wr3 [nblk * 3EB, d] bf16: for expert block b, rows
+// 3EB*b + g*EB + c hold part g (hi, mid, lo) of column e = EB*b + c, where
+// hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid); both differences
+// are exact in fp32, so hi + mid + lo equals w to within 2^-27 |w|.  Columns
+// past E are zero.
+__global__ void split_router_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ Wr3, int d, int E,
+                                    int EB, int nblk) {
+  const int64_t total = static_cast<int64_t>(nblk) * EB * d;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int k = static_cast<int>(i % d);
+    const int col = static_cast<int>(i / d);  // expert slot 0 .. nblk*EB-1
+    const int b = col / EB, c = col % EB;
+    const float w = (col < E) ? Wr[static_cast<int64_t>(k) * E + col] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+    const int64_t rbase = static_cast<int64_t>(b) * 3 * EB + c;
+    Wr3[(rbase + 0 * EB) * d + k] = hi;
+    Wr3[(rbase + 1 * EB) * d + k] = mid;
+    Wr3[(rbase + 2 * EB) * d + k] = lo;
+  }
+}
+
+size_t router_split_elems(int d, int E) {
+  const int EB = router_expert_block(E);
+  const int nblk = (E + EB - 1) / EB;
+  return static_cast<size_t>(nblk) * 3 * EB * d;
+}
+
+void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream) {
+  const int EB = router_expert_block(E);
+  const int nblk = (E + EB - 1) / EB;
+  const int64_t total = static_cast<int64_t>(nblk) * EB * d;
+  const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, num_sms() * 16));
+  split_router_kernel<<<blocks, 256, 0, stream>>>(Wr, Wr3, d, E, EB, nblk);
 }
 
 // ------------------------------------------------------------- selftest

@@ -10,8 +10,6 @@
 namespace moe {
 
 // route.cu
-void launch_router_logits(const __nv_bfloat16* x, const float* Wr, const float* bias, float* logits, int T, int d,
-                          int E, cudaStream_t stream);
 void launch_topk_gating(const float* logits, int32_t* idx, float* w, int T, int E, int k, int32_t* status,
                         cudaStream_t stream);
 
@@ -29,7 +27,6 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
                         int32_t* tok_rows, void* scratch, int32_t* status, cudaStream_t stream);
 
 // gemm.cu
-struct GemmTensorMaps;
 int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
                      const int32_t* offsets, const int32_t* row_token, __nv_bfloat16* h, int T, int d, int n, int E,
                      int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
@@ -40,6 +37,13 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
 void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const int32_t* offsets, int E, int d,
                         __nv_bfloat16* out, int64_t rows_cap, cudaStream_t stream);
 inline int up_half_block(int n) { return (n % 128 == 0) ? 128 : 64; }
+int num_sms();
+// router on the tensor cores: Wr split into three bf16 terms (see gemm.cu)
+int router_expert_block(int E);
+size_t router_split_elems(int d, int E);
+void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream);
+int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
+                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 // combine.cu
 void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, float* y, int T, int d,

@@ -1,4 +1,5 @@
-// Router: gate-network logits and top-k gating.
+// Router: top-k gating over the gate-network logits (the logits themselves
+// come from the tensor-core GEMM in gemm.cu).
 //
 // Gate network and top_k of the moe_forward pseudocode
 // ("MoE架构的物理瓶颈与扩展限制解析", section 工作原理, step 1) and steps 1-2 of
@@ -7,89 +8,6 @@
 #include "kernels.h"
 
 namespace moe {
-
-// ---------------------------------------------------------------------------
-// logits[T, E] = float(x[T, d]) @ Wr[d, E] + bias[E]   (fp32 FMA, K ascending)
-//
-// Block tile: 64 tokens x BE experts, K step 32.  256 threads; each thread owns
-// 4 tokens x (BE/16) experts.  x is converted bf16 -> fp32 (exact) on the way
-// into shared memory.
-template <int BE>
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16* __restrict__ x,
-                                                            const float* __restrict__ Wr,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits, int T, int d, int E) {
-  constexpr int BM = 64, BK = 32, RE = BE / 16;
-  __shared__ float xs[BK][BM + 4];
-  __shared__ float ws[BK][BE];
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * BM;
-  const int e0 = blockIdx.y * BE;
-  const int ty = tid / 16, tx = tid % 16;
-  float acc[4][RE];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < RE; ++j) acc[i][j] = 0.f;
-
-  for (int k0 = 0; k0 < d; k0 += BK) {
-    // x tile: 64 tokens x 32 k = 256 threads x 8 elements (one 16-byte load)
-    {
-      const int r = tid / 4, c = (tid % 4) * 8;
-      const int t = t0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = *reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0 + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[c + 2 * q][r] = bf16_lo(w[q]);
-        xs[c + 2 * q + 1][r] = bf16_hi(w[q]);
-      }
-    }
-    // Wr tile: 32 k x BE experts
-    for (int i = tid; i < BK * BE; i += 256) {
-      const int kk = i / BE, ee = i % BE;
-      const int e = e0 + ee;
-      ws[kk][ee] = (e < E) ? Wr[static_cast<size_t>(k0 + kk) * E + e] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < BK; ++kk) {
-      float a[4], b[RE];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < RE; ++j) b[j] = ws[kk][tx * RE + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < RE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < RE; ++j) {
-      const int e = e0 + tx * RE + j;
-      if (e < E) logits[static_cast<size_t>(t) * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
-    }
-  }
-}
-
-void launch_router_logits(const __nv_bfloat16* x, const float* Wr, const float* bias, float* logits, int T, int d,
-                          int E, cudaStream_t stream) {
-  const int gx = (T + 63) / 64;
-  if (E <= 16) {
-    router_logits_kernel<16><<<dim3(gx, 1), 256, 0, stream>>>(x, Wr, bias, logits, T, d, E);
-  } else if (E <= 32) {
-    router_logits_kernel<32><<<dim3(gx, 1), 256, 0, stream>>>(x, Wr, bias, logits, T, d, E);
-  } else {
-    router_logits_kernel<64><<<dim3(gx, (E + 63) / 64), 256, 0, stream>>>(x, Wr, bias, logits, T, d, E);
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Top-k gating: one warp per token.  Lane l holds logits of experts

@@ -116,4 +116,4 @@ def test_product_refuses_cpu_tensors():
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     Wr = torch.zeros(64, 4)
     with pytest.raises(ValueError, match="CUDA"):
-        B.moe_router_logits(x, Wr)
+        B.moe_router_logits(x, Wr, None, None)

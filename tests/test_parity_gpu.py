@@ -28,13 +28,17 @@ def ws_for(T, d, n, E, k, dev, tile=128, round="off"):
 def test_router_logits(cuda_device, T, d, E, bias):
     cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=1, bias="normal" if bias else None, bias_scale=0.5)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T + E, weights=False)
-    L = B.moe_router_logits(inp["x"], inp["Wr"], inp["bias"])
+    s, ws = ws_for(T, d, 64, E, 1, cuda_device)
+    L = B.moe_router_logits(inp["x"], inp["Wr"], inp["bias"], ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
     torch.cuda.synchronize()
     L64 = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
     err = np.abs(to64(L) - L64)
-    # rigorous fp32 dot-product bound: d * 2^-24 * sum_i |x_i w_ie| (+ bias add)
+    # rigorous bound for an fp32-accumulated dot product of 3d exact terms
+    # (hi/mid/lo split, each product exact), rounding toward zero allowed:
+    # (3d + 3) * 2^-23 * sum_i |x_i w_ie|, plus the split residue 2^-27
     absdot = np.abs(to64(inp["x"])) @ np.abs(to64(inp["Wr"]))
-    assert np.all(err <= (d + 2) * 2.0 ** -24 * (absdot + np.abs(L64)) + 1e-30)
+    assert np.all(err <= (3 * d + 3) * 2.0 ** -23 * (absdot + np.abs(L64)) + 1e-30)
     rms = float(np.sqrt(np.mean(L64 ** 2)))
     assert err.max() <= 5e-5 * rms, (err.max(), rms)
 
@@ -90,7 +94,7 @@ def _synthetic_routing(T, E, k, seed, skew=0.0):
 
 
 # ------------------------------------------------------------ up-projection
-@pytest.mark.parametrize("gather", [True, False])
+@pytest.mark.parametrize("gather", [0, 1, 2])
 @pytest.mark.parametrize("T,d,n,E,k,skew", [(700, 256, 192, 6, 2, 0.0), (600, 384, 256, 5, 3, 1.0),
                                             (300, 128, 64, 8, 2, 0.0), (1100, 512, 128, 3, 1, 0.5)])
 def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
