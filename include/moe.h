@@ -147,6 +147,34 @@ int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w
                 int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst,
                 int32_t* row_token, float* row_w, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory: code running inside a host engine that owns every device byte (a
+ * serving runtime with a fixed memory arena, or a plugin loaded into another
+ * framework) and is not allowed to call cudaMalloc once it is running, since
+ * an allocation there can synchronise the device and bypasses the engine's
+ * memory accounting.  The published method has no counterpart of this entry
+ * point; it exists for those callers only.
+ *
+ * Same arguments and results as moe_permute, minus (ws, ws_bytes).  The
+ * per-chunk histograms live in a 1 MiB array compiled into the library (a
+ * file-scope __device__ array that every GPU loading the library holds until
+ * the process exits), so the shape must satisfy E * ceil(T*k / 2048) <=
+ * 262144; larger shapes return MOE_ERR_WORKSPACE and launch nothing.  No
+ * allocation or free of any kind happens in this call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - All calls share the one array: two calls whose kernels overlap on the
+ *     GPU (different streams, or different host threads) race and give wrong
+ *     results.  Serialise them.
+ *   - Every histogram entry a call reads is written earlier in that call, so
+ *     what an earlier call left in the array never matters.
+ *   - Expert ids outside [0, E) are skipped, as in moe_permute, but are not
+ *     reported (there is no status word). */
+int moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, const float* topk_w,
+                        int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst,
+                        int32_t* row_token, float* row_w, void* stream);
+
 /* Token rounding ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化", 3. Token Rounding 路由算法),
  * mode s->round (NEAREST or UP), tile s->tile.  Each expert's count c becomes
  * c' = tile-multiple (nearest half-up, or up), capped at tile*floor(T/tile).

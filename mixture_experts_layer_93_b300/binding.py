@@ -62,6 +62,7 @@ _SIGNATURES = {
     "moe_topk_gating": (_I, [_SHP, _P, _P, _P, _P, _P]),
     "moe_route": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_noalloc": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),

@@ -12,6 +12,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <mutex>
+
 namespace moe {
 
 constexpr int kPermWarps = 4;
@@ -143,3 +145,55 @@ void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E,
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the permutation.
+//
+// Its chunk histograms live in a file-scope device array instead of a
+// caller-provided workspace.  The host cannot pass that array's name to a
+// kernel (in host code it is only a stand-in symbol), so the device address is
+// looked up once per device with cudaGetSymbolAddress and cached.
+namespace moe {
+
+constexpr int64_t kNoAllocScratchInts = 262144;  // 1 MiB
+static __device__ __align__(256) int32_t g_perm_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_scratch_mutex;
+static int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_perm_scratch on the current device (looked up on the
+// first call for that device); nullptr if the lookup fails.
+static int32_t* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_perm_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
+  }
+  return g_scratch_ptr[dev];
+}
+
+}  // namespace moe
+
+extern "C" int moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
+                                   int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token, float* row_w,
+                                   void* stream) {
+  using namespace moe;
+  if (!s || s->T < 1 || s->E < 1 || s->E > 1024 || s->k < 1 || s->k > s->E || s->k > 32) return MOE_ERR_INVALID;
+  if (!topk_idx || !counts || !offsets || !src || !dst || !row_token) return MOE_ERR_INVALID;
+  if (topk_w && !row_w) return MOE_ERR_INVALID;
+  const int64_t A = static_cast<int64_t>(s->T) * s->k;
+  if (A >= (int64_t(1) << 31) - 1) return MOE_ERR_INVALID;
+  // the histograms need E * ceil(A / 2048) ints of the fixed array
+  if (static_cast<int64_t>(s->E) * perm_num_chunks(A) > kNoAllocScratchInts) return MOE_ERR_WORKSPACE;
+  int32_t* scratch = noalloc_scratch();
+  if (!scratch) return MOE_ERR_CUDA;
+  // every histogram entry the scan reads is written by this call's first
+  // kernel, so nothing left over from an earlier call is ever read
+  launch_permute(topk_idx, topk_w, A, s->k, s->E, scratch, counts, offsets, src, dst, row_token, row_w, nullptr,
+                 reinterpret_cast<cudaStream_t>(stream));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
