@@ -254,7 +254,9 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     stages = ["route", "permute", "up", "down", "combine"]
-    launches_per_step = 2 + (3 if mode == "off" else 0) + 1 + (1 if args.gather == 0 else 0) + 1 + 1
+    # route: Wr split + router GEMM + top-k; permute: 3; rounding: 5 + a
+    # 3-launch permutation; up: GEMM (+ row gather in mode 0); down; combine
+    launches_per_step = 3 + (3 if mode == "off" else 8) + 1 + (1 if args.gather == 0 else 0) + 1 + 1
 
     def check(rc, what):
         if rc != 0:

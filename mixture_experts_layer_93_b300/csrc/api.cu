@@ -186,7 +186,6 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
                     int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets, int32_t* tok_rows,
                     void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || s->round == MOE_ROUND_OFF) return MOE_ERR_INVALID;
-  return MOE_ERR_UNSUPPORTED;
   if (!logits || !topk_idx || !counts || !offsets || !row_token || !row_w || !tok_offsets || !tok_rows)
     return MOE_ERR_INVALID;
   const int st = check_ws(s, ws, ws_bytes);

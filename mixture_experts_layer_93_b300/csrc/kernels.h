@@ -19,6 +19,11 @@ inline int64_t perm_num_chunks(int64_t A) { return (A + kPermChunk - 1) / kPermC
 void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
                     int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
                     float* row_w, int32_t* status, cudaStream_t stream);
+// The same sort over a list of `*len` (<= cap, read on the device) assignments
+// with explicit tokens: rows of an expert keep list order; dst[a] = row.
+void launch_permute_list(const int32_t* expert_of, const float* w, const int32_t* token_of, const int32_t* len,
+                         int64_t cap, int E, int32_t* chunk_hist, int32_t* counts, int32_t* offsets, int32_t* dst,
+                         int32_t* row_token, float* row_w, int32_t* status, cudaStream_t stream);
 
 // round.cu
 size_t round_scratch_bytes(int T, int E, int k, int tile);

@@ -18,13 +18,20 @@ namespace moe {
 
 constexpr int kPermWarps = 4;
 
-__global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t A, int E,
+// A list's length is A, or min(A, *len) when the length lives on the device.
+__device__ __forceinline__ int64_t list_length(int64_t A, const int32_t* len) {
+  return len ? min(A, static_cast<int64_t>(*len)) : A;
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t A,
+                                                                  const int32_t* __restrict__ len, int E,
                                                                   int nchunks, int32_t* __restrict__ chunk_hist,
                                                                   int32_t* status) {
   extern __shared__ int32_t hist_s[];
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = blockIdx.x * kPermWarps + w;
   if (c >= nchunks) return;
+  A = list_length(A, len);
   int32_t* h = hist_s + w * E;
   for (int e = lane; e < E; e += 32) h[e] = 0;
   __syncwarp();
@@ -98,20 +105,24 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   }
 }
 
+// token_of == nullptr: the token of assignment a is a / k.  src may be null.
 __global__ void __launch_bounds__(kPermWarps * 32) perm_scatter_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ wts, int64_t A, int k, int E, int nchunks,
-    const int32_t* __restrict__ chunk_base, int32_t* __restrict__ src, int32_t* __restrict__ dst,
-    int32_t* __restrict__ row_token, float* __restrict__ row_w) {
+    const int32_t* __restrict__ idx, const float* __restrict__ wts, const int32_t* __restrict__ token_of, int64_t A,
+    const int32_t* __restrict__ len, int k, int E, int nchunks, const int32_t* __restrict__ chunk_base,
+    int32_t* __restrict__ src, int32_t* __restrict__ dst, int32_t* __restrict__ row_token,
+    float* __restrict__ row_w) {
   extern __shared__ int32_t base_s[];
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = blockIdx.x * kPermWarps + w;
   if (c >= nchunks) return;
+  A = list_length(A, len);
   int32_t* base = base_s + w * E;
   for (int e = lane; e < E; e += 32) base[e] = chunk_base[static_cast<int64_t>(e) * nchunks + c];
   __syncwarp();
   const uint32_t lt_mask = (1u << lane) - 1u;
   const int64_t a0 = static_cast<int64_t>(c) * kPermChunk;
   const int64_t a1 = min(A, a0 + kPermChunk);
+  if (a0 >= a1) return;
   for (int64_t ab = a0; ab < a1; ab += 32) {
     const int64_t a = ab + lane;
     int e = (a < a1) ? idx[a] : -1;
@@ -124,24 +135,38 @@ __global__ void __launch_bounds__(kPermWarps * 32) perm_scatter_kernel(
     if (e >= 0 && rank == 0) base[e] += __popc(peers);
     __syncwarp();
     if (e >= 0) {
-      src[pos] = static_cast<int32_t>(a);
+      if (src) src[pos] = static_cast<int32_t>(a);
       dst[a] = pos;
-      row_token[pos] = static_cast<int32_t>(a / k);
+      row_token[pos] = token_of ? token_of[a] : static_cast<int32_t>(a / k);
       if (wts) row_w[pos] = wts[a];
     }
   }
 }
 
-void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
-                    int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
-                    float* row_w, int32_t* status, cudaStream_t stream) {
+static void permute_impl(const int32_t* idx, const float* w, const int32_t* token_of, int64_t A, const int32_t* len,
+                         int k, int E, int32_t* chunk_hist, int32_t* counts, int32_t* offsets, int32_t* src,
+                         int32_t* dst, int32_t* row_token, float* row_w, int32_t* status, cudaStream_t stream) {
   const int nchunks = static_cast<int>(perm_num_chunks(A));
   const int blocks = (nchunks + kPermWarps - 1) / kPermWarps;
   const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
-  perm_hist_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, A, E, nchunks, chunk_hist, status);
+  perm_hist_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, A, len, E, nchunks, chunk_hist, status);
   perm_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, E, nchunks, counts, offsets);
-  perm_scatter_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, w, A, k, E, nchunks, chunk_hist, src, dst,
-                                                                 row_token, row_w);
+  perm_scatter_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, w, token_of, A, len, k, E, nchunks, chunk_hist,
+                                                                 src, dst, row_token, row_w);
+}
+
+void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
+                    int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                    float* row_w, int32_t* status, cudaStream_t stream) {
+  permute_impl(idx, w, nullptr, A, nullptr, k, E, chunk_hist, counts, offsets, src, dst, row_token, row_w, status,
+               stream);
+}
+
+void launch_permute_list(const int32_t* expert_of, const float* w, const int32_t* token_of, const int32_t* len,
+                         int64_t cap, int E, int32_t* chunk_hist, int32_t* counts, int32_t* offsets, int32_t* dst,
+                         int32_t* row_token, float* row_w, int32_t* status, cudaStream_t stream) {
+  permute_impl(expert_of, w, token_of, cap, len, 1, E, chunk_hist, counts, offsets, nullptr, dst, row_token, row_w,
+               status, stream);
 }
 
 }  // namespace moe

@@ -279,3 +279,92 @@ def test_forward_full_size_sampled(cuda_device, name):
     assert torch.equal(y, y2)
     del layer, inp
     torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------- token rounding
+def _expected_rounding(L, idx, tile, mode):
+    r = O.token_round(L, idx, tile, mode)
+    T, E = L.shape
+    counts = r["counts"]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    row_token = np.zeros(offsets[-1], dtype=np.int64)
+    rowpos = {}
+    for e in range(E):
+        ts = np.flatnonzero(r["member"][:, e])
+        row_token[offsets[e]:offsets[e + 1]] = ts
+        for i, t in enumerate(ts):
+            rowpos[(int(t), e)] = offsets[e] + i
+    sizes = [len(s) for s in r["sets"]]
+    tok_offsets = np.concatenate([[0], np.cumsum(sizes)])
+    tok_rows = np.array([rowpos[(t, int(e))] for t in range(T) for e in r["sets"][t]], dtype=np.int64)
+    row_w = np.zeros(offsets[-1])
+    for t in range(T):
+        s = r["sets"][t]
+        if len(s):
+            w = O.softmax(np.asarray(L, np.float64)[t, s])
+            for e, we in zip(s, w):
+                row_w[rowpos[(t, int(e))]] = we
+    return counts, offsets, row_token, tok_offsets, tok_rows, row_w
+
+
+@pytest.mark.parametrize("T,E,k,tile,mode,zipf", [(1000, 16, 2, 64, "nearest", 0.0), (777, 8, 2, 128, "nearest", 0.0),
+                                                 (4099, 64, 4, 128, "nearest", 1.1), (100, 4, 1, 128, "nearest", 0.0),
+                                                 (300, 32, 8, 64, "up", 0.0), (2000, 128, 8, 128, "up", 1.1),
+                                                 (513, 5, 5, 256, "nearest", 0.0)])
+def test_token_round_bit_exact(cuda_device, T, E, k, tile, mode, zipf):
+    L = I.make_logits(T, E, seed=T + E + tile, ties=True)
+    if zipf:
+        L = L - zipf * torch.log(torch.arange(1, E + 1, dtype=torch.float32))[None, :]
+        L = (torch.round(L * 4) / 4).contiguous()
+    Lnp = L.numpy()
+    idx = torch.from_numpy(O.topk(Lnp, k))
+    s, ws = ws_for(T, 64, 64, E, k, cuda_device, tile=tile, round=mode)
+    out = B.moe_token_round(s, L.to(cuda_device), idx.to(cuda_device), ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    counts, offsets, row_token, tok_offsets, tok_rows, row_w = _expected_rounding(Lnp, idx.numpy(), tile, mode)
+    R = int(offsets[-1])
+    assert np.array_equal(out["counts"].cpu().numpy(), counts)
+    assert np.all(counts % tile == 0)
+    assert np.array_equal(out["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(out["row_token"][:R].cpu().numpy(), row_token)
+    assert np.array_equal(out["tok_offsets"].cpu().numpy(), tok_offsets)
+    assert np.array_equal(out["tok_rows"][:R].cpu().numpy(), tok_rows)
+    assert np.abs(to64(out["row_w"][:R]) - row_w).max(initial=0.0) <= 2e-6
+
+
+def _gpu_sets(ws, shape, T):
+    cap = B.moe_row_capacity(shape)
+    offsets = ws.view("offsets", torch.int32, shape.E + 1).cpu().numpy()
+    tok_offsets = ws.view("tok_offsets", torch.int32, T + 1).cpu().numpy()
+    tok_rows = ws.view("tok_rows", torch.int32, cap).cpu().numpy()
+    sets = []
+    for t in range(T):
+        rows = tok_rows[tok_offsets[t]:tok_offsets[t + 1]]
+        sets.append(np.searchsorted(offsets, rows, side="right") - 1)
+    return sets
+
+
+@pytest.mark.parametrize("T,d,n,E,k,tile,mode", [(256, 128, 64, 8, 2, 64, "nearest"), (1500, 256, 128, 16, 4, 128, "nearest"),
+                                                 (700, 128, 192, 12, 3, 64, "up")])
+def test_forward_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="zipf", bias_scale=1.1)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=T)
+    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile, round=mode)
+    y = layer.forward(inp["x"])
+    ws = layer.workspace(T, cuda_device)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    gsets = _gpu_sets(ws, layer.shape(T), T)
+    counts = ws.view("counts", torch.int32, E).cpu().numpy()
+    assert np.all(counts % tile == 0)
+    toks, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], k, tile=tile, mode=mode)
+    same = np.array([np.array_equal(a, b) for a, b in zip(gsets, osets)])
+    # fp32 logits on the GPU vs fp64 ones in the oracle can flip a selection
+    # only at a near-tie between two tokens' logits
+    assert same.mean() > 0.97, same.mean()
+    keep = np.flatnonzero(same)
+    y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile,
+                          mode=mode, tokens=keep)
+    assert_moe_close(y[torch.from_numpy(keep).to(cuda_device)], y_ref)
+    empty = [t for t in keep if len(osets[t]) == 0]
+    if empty:
+        assert torch.all(y[torch.tensor(empty, device=cuda_device)] == 0)
