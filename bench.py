@@ -41,6 +41,12 @@ from mixture_experts_layer_93_b300 import inputs as I  # noqa: E402
 METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
+# DRAM bytes (read + write) of one up-projection launch from an ncu capture of
+# the current kernel (profiles/moe_gemm_mixtral.md), keyed by workload, A path
+# and kernel revision; a kernel change bumps GEMM_REV and drops stale entries.
+GEMM_REV = "persistent-1cta-v3"
+UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2013502720 + 458782208}
+
 
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -355,7 +361,10 @@ def run_ours(args, world, rank, local):
     up_tflops = up_flops / (up_ms * 1e-3) / 1e12
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up, SwiGLU>", "achieved": up_tflops,
-                "peak": peak_t, "unit": "TFLOP/s", "frac": up_tflops / peak_t, "traffic": None,
+                "peak": peak_t, "unit": "TFLOP/s", "frac": up_tflops / peak_t,
+                "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV)) if T == I.get_config(cfg.name).T
+                else None,
+                "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "algorithmic_flops_per_launch": up_flops}
     # HBM-bound stages: algorithmic bytes / time
