@@ -70,19 +70,31 @@ constexpr int kGemmThreads = 9 * 32;
 
 __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 256 ? 256 : 512))); }
 
-template <int BN>
+// PAIR: two CTAs of a cluster run one 256-row tile with tcgen05 cta_group::2.
+// CTA rank r holds A rows 128r..128r+127 and B rows r*BN/2..r*BN/2+BN/2-1 in
+// its own shared memory; the even CTA issues M=256 MMAs that read both CTAs'
+// operands; D rows 128r.. land in CTA r's TMEM.  Each SM thus stores and feeds
+// half of B: per k-block 32 KB of shared-memory writes and reads instead of
+// 48 KB, which is what keeps a 1-CTA M=128 x N=256 MMA from full rate.
+template <int BN, bool PAIR>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows held per CTA
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
   static constexpr int TMEM_COLS = tmem_cols_for(2 * BN);
   static constexpr int BAR_BYTES = (2 * STAGES + 4) * 8 + 16;
   static constexpr int PREFIX_BYTES = 1025 * 4;
   static constexpr int TOK_BYTES = BM * 4;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES;
+  // slack after the last tile: a pair MMA reading past a B half stays inside
+  // this CTA's allocation
+  static constexpr int SLACK_BYTES = PAIR ? B_BYTES : 0;
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES + SLACK_BYTES;
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
@@ -112,11 +124,12 @@ __device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_
   }
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, PAIR>;
+  constexpr int kPer = PAIR ? 2 : 1;  // 128-row blocks per tile unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -133,10 +146,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_groups = p.single_rows > 0 ? 1 : p.E;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = (rank == 0);  // issues the MMAs
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
 
   if (warp == 0 && lane == 0) {
     // gather 2: one arrival per producer lane (when its copies land) plus
-    // warp 0's expect-tx arrival for the B tile
+    // warp 0's expect-tx arrival for the B tile.  PAIR: the even CTA's full
+    // barrier counts the bytes of both CTAs' copies; its tmem-empty barrier
+    // takes the four epilogue warps of both CTAs.
     const uint32_t full_count = p.gather == 2 ? 1 + 32 * kProducerWarps : 1;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), full_count);
@@ -144,22 +163,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull_bar[a]), 1);
-      mbar_init(smem_u32(&tempty_bar[a]), 4);
+      mbar_init(smem_u32(&tempty_bar[a]), 4 * kPer);
     }
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   } else if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+      tmem_relinquish();
+    }
     tc_fence_before();
   } else if (warp == kEpiWarp0) {
-    // prefix[e] = number of 128-row tiles of groups < e
+    // prefix[e] = number of tile units (kPer 128-row blocks) of groups < e
     if (p.single_rows > 0) {
       if (lane == 0) {
         prefix[0] = 0;
-        prefix[1] = (p.single_rows + C::BM - 1) / C::BM;
+        prefix[1] = ((p.single_rows + C::BM - 1) / C::BM + kPer - 1) / kPer;
       }
     } else {
       int running = 0;
@@ -167,7 +191,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int b = 0; b < p.E; b += 32) {
         const int e = b + lane;
         int m = 0;
-        if (e < p.E) m = (p.counts[e] + C::BM - 1) / C::BM;
+        if (e < p.E) m = ((p.counts[e] + C::BM - 1) / C::BM + kPer - 1) / kPer;
         int incl = m;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -180,6 +204,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   __syncthreads();
+  // the peer's copies, commits and arrivals target our barriers: both CTAs'
+  // barriers are initialised before either starts
+  if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total_tiles = prefix[n_groups] * p.n_blocks;
@@ -193,24 +220,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
-        int e, nb, mb, gstart, gcount;
-        decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mb);
+      for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
+        int e, nb, mu, gstart, gcount;
+        decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, e, gstart, gcount);
+        const int mb = mu * kPer + rank;
         const int row0 = gstart + mb * C::BM;
-        const int rows_valid = min(C::BM, gcount - mb * C::BM);
+        const int rows_valid = min(C::BM, gcount - mb * C::BM);  // <= 0: a pair's empty half
+        // gathered rows past the group repeat a row of the group
+        const int last = max(rows_valid, 1) - 1;
+        const int tok_base = rows_valid > 0 ? row0 : gstart;
         int tok[4] = {0, 0, 0, 0};
         if (p.gather == 1) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) tok[q] = p.row_token[row0 + min(lane * 4 + q, rows_valid - 1)];
+          for (int q = 0; q < 4; ++q) tok[q] = p.row_token[tok_base + min(lane * 4 + q, last)];
         } else if (p.gather == 2) {
-          // this warp's 32 rows; rows past the group repeat its last row
           __syncwarp();
           const int r = warp * 32 + lane;
-          tok_s[r] = p.row_token[row0 + min(r, rows_valid - 1)];
+          tok_s[r] = p.row_token[tok_base + min(r, last)];
           __syncwarp();
         }
-        const int brow = e * p.b_rows_per_expert + nb * BN;
+        const int brow = e * p.b_rows_per_expert + nb * BN + rank * C::B_ROWS;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           int w = 1;
           if (lane == 0)
@@ -222,17 +252,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t fb = smem_u32(&full_bar[stage]);
           const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
           if (issuer) {
-            if (lane == 0) mbar_arrive_expect_tx(fb, p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES);
-            __syncwarp();
-            if (p.gather == 1) {
-              tma_gather4(a_dst + lane * 512, &tmA, kb * C::BK, tok[0], tok[1], tok[2], tok[3], fb, pol_a);
-            } else if (p.gather == 0 && lane == 0) {
-              tma_load_2d(a_dst, &tmA, kb * C::BK, row0, fb, pol_a);
+            if (PAIR) {
+              // both CTAs' copies complete on the even CTA's barrier
+              const uint32_t fb0 = map_to_cta(fb, 0);
+              if (lane == 0) {
+                if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+                tma_load_2d_pair(a_dst, &tmA, kb * C::BK, row0, fb0, pol_a);
+                tma_load_2d_pair(b_dst, &tmB, kb * C::BK, brow, fb0, pol_b);
+              }
+            } else {
+              if (lane == 0) mbar_arrive_expect_tx(fb, p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES);
+              __syncwarp();
+              if (p.gather == 1) {
+                tma_gather4(a_dst + lane * 512, &tmA, kb * C::BK, tok[0], tok[1], tok[2], tok[3], fb, pol_a);
+              } else if (p.gather == 0 && lane == 0) {
+                tma_load_2d(a_dst, &tmA, kb * C::BK, row0, fb, pol_a);
+              }
+              if (lane == 0) tma_load_2d(b_dst, &tmB, kb * C::BK, brow, fb, pol_b);
             }
-            if (lane == 0) tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmB, kb * C::BK, brow, fb, pol_b);
           }
-          if (p.gather == 2) {
+          if (!PAIR && p.gather == 2) {
             // lane owns 16-byte chunk c of rows r = 32*warp + lane/8 + 4i; the
             // chunk goes to its swizzled slot (c ^ (r mod 8)) of row r
             const int c = lane & 7;
@@ -250,18 +291,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (p.gather == 2) cp_async_wait_all();  // nothing of ours in flight at exit
+      if (!PAIR && p.gather == 2) cp_async_wait_all();  // nothing of ours in flight at exit
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(C::BM, BN);
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kPer * C::BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tau = blockIdx.x; tau < total_tiles && ok; tau += gridDim.x) {
+      for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status,
                                kWaitMmaTmemEmpty, p.timeout_ns))
           break;
@@ -275,23 +316,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           // A rows written by cp.async (generic proxy) become visible to
           // the tensor core's operand reads (async proxy)
-          if (p.gather == 2) fence_proxy_async_smem();
+          if (!PAIR && p.gather == 2) fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, smem_desc_k128(a0 + kk * 32), smem_desc_k128(b0 + kk * 32), idesc,
-                        (kb > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t ad = smem_desc_k128(a0 + kk * 32), bd = smem_desc_k128(b0 + kk * 32);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            if (PAIR)
+              tc_mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+            else
+              tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
           }
-          tc_commit(smem_u32(&empty_bar[stage]));
+          // the slot is free in both CTAs once these MMAs have read it
+          if (PAIR)
+            tc_commit_pair_multicast(smem_u32(&empty_bar[stage]), 0x3);
+          else
+            tc_commit(smem_u32(&empty_bar[stage]));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&tfull_bar[acc]));
+        if (PAIR)
+          tc_commit_pair_multicast(smem_u32(&tfull_bar[acc]), 0x3);
+        else
+          tc_commit(smem_u32(&tfull_bar[acc]));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -302,10 +354,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r_in_tile = ew * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tau = blockIdx.x; tau < total_tiles; tau += gridDim.x) {
-      int e, nb, mb, gstart, gcount;
-      decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mb);
+    for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
+      int e, nb, mu, gstart, gcount;
+      decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
       group_rows(p, e, gstart, gcount);
+      const int mb = mu * kPer + rank;
       const int row0 = gstart + mb * C::BM;
       const int rows_valid = min(C::BM, gcount - mb * C::BM);
       int w = 1;
@@ -396,7 +449,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's MMA waits on it
+        else
+          mbar_arrive(smem_u32(&tempty_bar[acc]));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -412,9 +470,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncthreads();
   }
+  // no CTA leaves while its peer may still read its operands or arrive on it
+  if (PAIR) cluster_sync();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -456,13 +519,34 @@ int num_sms() {
   return sms > 0 ? sms : 1;
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool PAIR>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t stream) {
-  using C = GemmCfg<BN>;
-  auto kern = moe_gemm_kernel<BN, MODE>;
+  using C = GemmCfg<BN, PAIR>;
+  auto kern = moe_gemm_kernel<BN, MODE, PAIR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return MOE_ERR_CUDA;
-  kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, p);
+  if (!PAIR) {
+    kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many clusters as can be resident at once (SM pairs that
+  // share a GPC), so no cluster waits for a second wave
+  int clusters = 0;
+  cfg.gridDim = dim3(num_sms() & ~1);
+  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) clusters = num_sms() / 2;
+  cfg.gridDim = dim3(2 * std::min(clusters, num_sms() / 2));
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -507,7 +591,8 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
     launch_gather_rows(x, row_token, offsets, E, d, xperm_scratch, rows_cap, stream);
     if (!make_map_bf16(&tmA, xperm_scratch, d, rows_cap, 128)) return MOE_ERR_CUDA;
   }
-  if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
+  const bool pair = (gather == 0);
+  if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, pair ? BN / 2 : BN)) return MOE_ERR_CUDA;
   GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
@@ -521,8 +606,12 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   p.gather = gather;
   p.x = x;
   p.lda = d;
-  if (BN == 256) return launch_gemm<256, kModeUp>(tmA, tmB, p, stream);
-  return launch_gemm<128, kModeUp>(tmA, tmB, p, stream);
+  if (pair) {
+    if (BN == 256) return launch_gemm<256, kModeUp, true>(tmA, tmB, p, stream);
+    return launch_gemm<128, kModeUp, true>(tmA, tmB, p, stream);
+  }
+  if (BN == 256) return launch_gemm<256, kModeUp, false>(tmA, tmB, p, stream);
+  return launch_gemm<128, kModeUp, false>(tmA, tmB, p, stream);
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
@@ -531,7 +620,7 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   const int BN = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, h, n, rows_cap, 128)) return MOE_ERR_CUDA;
-  if (!make_map_bf16(&tmB, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, W2p, n, static_cast<uint64_t>(E) * d, BN / 2)) return MOE_ERR_CUDA;
   GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
@@ -543,9 +632,9 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.n_blocks = d / BN;
   p.b_rows_per_expert = d;
   p.gather = 0;
-  if (BN == 256) return launch_gemm<256, kModeDown>(tmA, tmB, p, stream);
-  if (BN == 128) return launch_gemm<128, kModeDown>(tmA, tmB, p, stream);
-  return launch_gemm<64, kModeDown>(tmA, tmB, p, stream);
+  if (BN == 256) return launch_gemm<256, kModeDown, true>(tmA, tmB, p, stream);
+  if (BN == 128) return launch_gemm<128, kModeDown, true>(tmA, tmB, p, stream);
+  return launch_gemm<64, kModeDown, true>(tmA, tmB, p, stream);
 }
 
 int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }
@@ -569,9 +658,9 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   p.n_blocks = nblk;
   p.b_rows_per_expert = 0;
   p.gather = 0;
-  if (BN == 48) return launch_gemm<48, kModeRouter>(tmA, tmB, p, stream);
-  if (BN == 96) return launch_gemm<96, kModeRouter>(tmA, tmB, p, stream);
-  return launch_gemm<192, kModeRouter>(tmA, tmB, p, stream);
+  if (BN == 48) return launch_gemm<48, kModeRouter, false>(tmA, tmB, p, stream);
+  if (BN == 96) return launch_gemm<96, kModeRouter, false>(tmA, tmB, p, stream);
+  return launch_gemm<192, kModeRouter, false>(tmA, tmB, p, stream);
 }
 
 // Wr [d, E] fp32 -> Wr3 [nblk * 3EB, d] bf16: for expert block b, rows
