@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one up-projection launch from an ncu capture of
 # the current kernel (profiles/moe_gemm_mixtral.md), keyed by workload, A path
 # and kernel revision; a kernel change bumps GEMM_REV and drops stale entries.
-GEMM_REV = "persistent-1cta-v3"
+GEMM_REV = "cta-pair-v4"
 UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2013502720 + 458782208}
 
 
@@ -218,6 +218,9 @@ def run_ours(args, world, rank, local):
     cfg = I.get_config(args.config)
     if args.tokens:
         cfg = cfg.with_tokens(args.tokens)
+    if args.experts:
+        from dataclasses import replace
+        cfg = replace(cfg, E=args.experts)
     mode = args.round
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode)
     inp = I.make_inputs(cfg, device=dev, seed=rank)
@@ -261,8 +264,10 @@ def run_ours(args, world, rank, local):
     st = ctypes.c_void_p(stream.cuda_stream)
     stages = ["route", "permute", "up", "down", "combine"]
     # route: Wr split + router GEMM + top-k; permute: 3; rounding: 5 + a
-    # 3-launch permutation; up: GEMM (+ row gather in mode 0); down; combine
-    launches_per_step = 3 + (3 if mode == "off" else 8) + 1 + (1 if args.gather == 0 else 0) + 1 + 1
+    # 3-launch permutation; up: row gather + SM-pair GEMM + odd-block GEMM
+    # (A path 0) or one GEMM (paths 1, 2); down: SM-pair + odd-block GEMMs;
+    # combine: 1
+    launches_per_step = 3 + (3 if mode == "off" else 8) + (3 if args.gather == 0 else 1) + 2 + 1
 
     def check(rc, what):
         if rc != 0:
@@ -362,8 +367,8 @@ def run_ours(args, world, rank, local):
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up, SwiGLU>", "achieved": up_tflops,
                 "peak": peak_t, "unit": "TFLOP/s", "frac": up_tflops / peak_t,
-                "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV)) if T == I.get_config(cfg.name).T
-                else None,
+                "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV))
+                if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) else None,
                 "traffic_unit": "bytes per launch (ncu dram read+write)",
                 "peak_source": f"{peak_src} bf16_tflops (burst)",
                 "algorithmic_flops_per_launch": up_flops}
@@ -413,7 +418,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="mixtral", choices=sorted(I.CONFIGS))
     ap.add_argument("--round", default="off", choices=["off", "nearest", "up"])
-    ap.add_argument("--tokens", type=int, default=0, help="override T (parity/debug only)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (profiling of small cases only)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiling of small cases only)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)

@@ -55,6 +55,8 @@ struct GemmParams {
   int num_kb;                // K / 64
   int n_blocks;              // N tiles per group
   int b_rows_per_expert;     // rows of packed B per group
+  int units;                 // tiles per group: 0 every 128-row block, 1 complete pairs of
+                             // blocks (PAIR kernels), 2 the odd last block of each group
   int gather;                // A rows: 0 contiguous (tiled TMA), 1 TMA gather4 by token,
                              // 2 16-byte cp.async by token
   const __nv_bfloat16* x;    // gather 2: token rows
@@ -114,6 +116,18 @@ __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int 
   mb = local - nb * me;
 }
 
+// Tile units of a group with mblocks 128-row blocks.
+__device__ __forceinline__ int tile_units(int units, int mblocks) {
+  return units == 0 ? mblocks : (units == 1 ? mblocks / 2 : (mblocks & 1));
+}
+
+// 128-row block of unit mu handled by CTA `rank`.
+__device__ __forceinline__ int unit_block(int units, int mu, int rank, int gcount) {
+  if (units == 1) return 2 * mu + rank;
+  if (units == 2) return (gcount + 127) / 128 - 1;
+  return mu;
+}
+
 __device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_start, int& count) {
   if (p.single_rows > 0) {
     row_start = 0;
@@ -129,7 +143,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmParams p) {
   using C = GemmCfg<BN, PAIR>;
-  constexpr int kPer = PAIR ? 2 : 1;  // 128-row blocks per tile unit
+  constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -179,11 +193,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before();
   } else if (warp == kEpiWarp0) {
-    // prefix[e] = number of tile units (kPer 128-row blocks) of groups < e
+    // prefix[e] = number of tile units of groups < e
     if (p.single_rows > 0) {
       if (lane == 0) {
         prefix[0] = 0;
-        prefix[1] = ((p.single_rows + C::BM - 1) / C::BM + kPer - 1) / kPer;
+        prefix[1] = tile_units(p.units, (p.single_rows + C::BM - 1) / C::BM);
       }
     } else {
       int running = 0;
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int b = 0; b < p.E; b += 32) {
         const int e = b + lane;
         int m = 0;
-        if (e < p.E) m = ((p.counts[e] + C::BM - 1) / C::BM + kPer - 1) / kPer;
+        if (e < p.E) m = tile_units(p.units, (p.counts[e] + C::BM - 1) / C::BM);
         int incl = m;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -224,9 +238,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int e, nb, mu, gstart, gcount;
         decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, e, gstart, gcount);
-        const int mb = mu * kPer + rank;
+        const int mb = unit_block(p.units, mu, rank, gcount);
         const int row0 = gstart + mb * C::BM;
-        const int rows_valid = min(C::BM, gcount - mb * C::BM);  // <= 0: a pair's empty half
+        const int rows_valid = min(C::BM, gcount - mb * C::BM);
         // gathered rows past the group repeat a row of the group
         const int last = max(rows_valid, 1) - 1;
         const int tok_base = rows_valid > 0 ? row0 : gstart;
@@ -358,7 +372,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int e, nb, mu, gstart, gcount;
       decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
       group_rows(p, e, gstart, gcount);
-      const int mb = mu * kPer + rank;
+      const int mb = unit_block(p.units, mu, rank, gcount);
       const int row0 = gstart + mb * C::BM;
       const int rows_valid = min(C::BM, gcount - mb * C::BM);
       int w = 1;
@@ -607,9 +621,19 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   p.x = x;
   p.lda = d;
   if (pair) {
-    if (BN == 256) return launch_gemm<256, kModeUp, true>(tmA, tmB, p, stream);
-    return launch_gemm<128, kModeUp, true>(tmA, tmB, p, stream);
+    // complete pairs of 128-row blocks on SM pairs, then each expert's odd
+    // last block on single SMs (so no pair runs half empty)
+    p.units = 1;
+    int st = (BN == 256) ? launch_gemm<256, kModeUp, true>(tmA, tmB, p, stream)
+                         : launch_gemm<128, kModeUp, true>(tmA, tmB, p, stream);
+    if (st != MOE_OK) return st;
+    CUtensorMap tmB1;
+    if (!make_map_bf16(&tmB1, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
+    p.units = 2;
+    return (BN == 256) ? launch_gemm<256, kModeUp, false>(tmA, tmB1, p, stream)
+                       : launch_gemm<128, kModeUp, false>(tmA, tmB1, p, stream);
   }
+  p.units = 0;
   if (BN == 256) return launch_gemm<256, kModeUp, false>(tmA, tmB, p, stream);
   return launch_gemm<128, kModeUp, false>(tmA, tmB, p, stream);
 }
@@ -632,9 +656,17 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.n_blocks = d / BN;
   p.b_rows_per_expert = d;
   p.gather = 0;
-  if (BN == 256) return launch_gemm<256, kModeDown, true>(tmA, tmB, p, stream);
-  if (BN == 128) return launch_gemm<128, kModeDown, true>(tmA, tmB, p, stream);
-  return launch_gemm<64, kModeDown, true>(tmA, tmB, p, stream);
+  p.units = 1;
+  int st = (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, p, stream)
+           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, p, stream)
+                         : launch_gemm<64, kModeDown, true>(tmA, tmB, p, stream);
+  if (st != MOE_OK) return st;
+  CUtensorMap tmB1;
+  if (!make_map_bf16(&tmB1, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;
+  p.units = 2;
+  return (BN == 256)   ? launch_gemm<256, kModeDown, false>(tmA, tmB1, p, stream)
+         : (BN == 128) ? launch_gemm<128, kModeDown, false>(tmA, tmB1, p, stream)
+                       : launch_gemm<64, kModeDown, false>(tmA, tmB1, p, stream);
 }
 
 int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }
