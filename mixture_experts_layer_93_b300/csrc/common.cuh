@@ -25,6 +25,8 @@ enum : int32_t {
   kWaitMmaTmemEmpty = 3,
   kWaitEpiTmemFull = 4,
   kWaitSelftest = 5,
+  kWaitMmaRowsLanded = 6,
+  kWaitRelay = 7,
   kYsOverflow = 16,  // a down-projection output exceeded the fp16 range
 };
 
@@ -81,18 +83,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with cluster-scope acquire: for phases completed by arrivals or
+// copies issued from the peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with parity `parity` of the barrier has completed.
 // Gives up when *abort becomes nonzero (another role gave up) or after
 // timeout_ns; on a timeout it records MOE_ERR_TIMEOUT and raises *abort.
 // Returns true when the phase completed.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   int32_t* status, int32_t where, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
