@@ -16,60 +16,79 @@
 
 namespace moe {
 
-constexpr int kPermWarps = 4;
+// A block of kPermWarps warps owns kPermChunk consecutive assignments; warp w
+// owns the sub-chunk [w*kSub, (w+1)*kSub) of it.
+constexpr int kPermWarps = 8;
+constexpr int kSub = kPermChunk / kPermWarps;  // 256 assignments per warp
+constexpr int kPerLane = kSub / 32;            // 8 per lane
+static_assert(kPermChunk % (kPermWarps * 32) == 0, "chunk layout");
 
 // A list's length is A, or min(A, *len) when the length lives on the device.
 __device__ __forceinline__ int64_t list_length(int64_t A, const int32_t* len) {
   return len ? min(A, static_cast<int64_t>(*len)) : A;
 }
 
+// Per-block expert histogram -> chunk_hist[e][block].
 __global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t A,
                                                                   const int32_t* __restrict__ len, int E,
                                                                   int nchunks, int32_t* __restrict__ chunk_hist,
                                                                   int32_t* status) {
   extern __shared__ int32_t hist_s[];
-  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int c = blockIdx.x * kPermWarps + w;
-  if (c >= nchunks) return;
+  const int c = blockIdx.x;
   A = list_length(A, len);
-  int32_t* h = hist_s + w * E;
-  for (int e = lane; e < E; e += 32) h[e] = 0;
-  __syncwarp();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist_s[e] = 0;
+  __syncthreads();
   const int64_t a0 = static_cast<int64_t>(c) * kPermChunk;
-  const int64_t a1 = min(A, a0 + kPermChunk);
   bool bad = false;
-  for (int64_t a = a0 + lane; a < a1; a += 32) {
-    const int e = idx[a];
-    if (e >= 0 && e < E)
-      atomicAdd(&h[e], 1);  // counts only: the order of increments does not matter
+  int ev[kPermChunk / (kPermWarps * 32)];
+#pragma unroll
+  for (int i = 0; i < kPermChunk / (kPermWarps * 32); ++i) {
+    const int64_t a = a0 + threadIdx.x + static_cast<int64_t>(i) * blockDim.x;
+    ev[i] = (a < A) ? idx[a] : -1;
+  }
+#pragma unroll
+  for (int i = 0; i < kPermChunk / (kPermWarps * 32); ++i) {
+    const int64_t a = a0 + threadIdx.x + static_cast<int64_t>(i) * blockDim.x;
+    if (a >= A) continue;
+    if (ev[i] >= 0 && ev[i] < E)
+      atomicAdd(&hist_s[ev[i]], 1);  // counts only: the order of increments does not matter
     else
       bad = true;
   }
   if (bad) report_error(status, MOE_ERR_DEVICE_CHECK, -1);
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) chunk_hist[static_cast<int64_t>(e) * nchunks + c] = h[e];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[static_cast<int64_t>(e) * nchunks + c] = hist_s[e];
 }
 
-// One block of 1024 threads.
+// One block of 1024 threads: warp w scans the chunk counts of experts
+// w, w+32, ... (32 chunks at a time, warp shuffles), then the expert totals
+// are scanned and added back as each expert's base.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist, int E, int nchunks,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
   __shared__ int32_t cnt_s[1024];
   __shared__ int32_t warp_s[32];
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   for (int e = tid; e < 1024; e += blockDim.x) cnt_s[e] = 0;
-  for (int e = tid; e < E; e += blockDim.x) {
+  __syncthreads();
+  for (int e = wid; e < E; e += 32) {
     int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
     int32_t run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int32_t v = hrow[c];
-      hrow[c] = run;
-      run += v;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int32_t v = (c < nchunks) ? hrow[c] : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nchunks) hrow[c] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    cnt_s[e] = run;
+    if (lane == 0) cnt_s[e] = run;
   }
   __syncthreads();
   // exclusive scan of cnt_s[0..1024) (E <= 1024): one value per thread
-  const int lane = tid % 32, wid = tid / 32;
   const int32_t v = cnt_s[tid];
   int32_t incl = v;
 #pragma unroll
@@ -98,41 +117,64 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   }
   if (tid == E - 1) offsets[E] = excl + v;
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
+  for (int e = wid; e < E; e += 32) {
     int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
     const int32_t base = cnt_s[e];
-    for (int c = 0; c < nchunks; ++c) hrow[c] += base;
+    for (int c = lane; c < nchunks; c += 32) hrow[c] += base;
   }
 }
 
 // token_of == nullptr: the token of assignment a is a / k.  src may be null.
+// Warp w of block c places its 256 assignments, in order, after (a) every
+// earlier block's rows of the same expert (chunk_base, from the scan) and (b)
+// the rows of warps < w of this block; within 32 consecutive assignments,
+// equal experts are ranked by lane (match.any).  So rows of an expert come out
+// in ascending assignment order.
 __global__ void __launch_bounds__(kPermWarps * 32) perm_scatter_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ wts, const int32_t* __restrict__ token_of, int64_t A,
     const int32_t* __restrict__ len, int k, int E, int nchunks, const int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ src, int32_t* __restrict__ dst, int32_t* __restrict__ row_token,
     float* __restrict__ row_w) {
-  extern __shared__ int32_t base_s[];
+  extern __shared__ int32_t wbase[];  // [kPermWarps][E]
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int c = blockIdx.x * kPermWarps + w;
-  if (c >= nchunks) return;
+  const int c = blockIdx.x;
   A = list_length(A, len);
-  int32_t* base = base_s + w * E;
-  for (int e = lane; e < E; e += 32) base[e] = chunk_base[static_cast<int64_t>(e) * nchunks + c];
-  __syncwarp();
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  const int64_t a0 = static_cast<int64_t>(c) * kPermChunk;
-  const int64_t a1 = min(A, a0 + kPermChunk);
-  if (a0 >= a1) return;
-  for (int64_t ab = a0; ab < a1; ab += 32) {
-    const int64_t a = ab + lane;
-    int e = (a < a1) ? idx[a] : -1;
+  for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) wbase[i] = 0;
+  __syncthreads();
+  const int64_t a0 = static_cast<int64_t>(c) * kPermChunk + static_cast<int64_t>(w) * kSub;
+  int ev[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int64_t a = a0 + lane + 32 * i;
+    int e = (a < A) ? idx[a] : -1;
     if (e >= E) e = -1;
+    ev[i] = e;
+  }
+  int32_t* mybase = wbase + w * E;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i)
+    if (ev[i] >= 0) atomicAdd(&mybase[ev[i]], 1);  // per-warp counts
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = chunk_base[static_cast<int64_t>(e) * nchunks + c];
+    for (int ww = 0; ww < kPermWarps; ++ww) {
+      const int32_t cnt = wbase[ww * E + e];
+      wbase[ww * E + e] = run;
+      run += cnt;
+    }
+  }
+  __syncthreads();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int64_t a = a0 + lane + 32 * i;
+    const int e = ev[i];
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     int pos = 0;
-    if (e >= 0) pos = base[e] + rank;
+    if (e >= 0) pos = mybase[e] + rank;
     __syncwarp();
-    if (e >= 0 && rank == 0) base[e] += __popc(peers);
+    if (e >= 0 && rank == 0) mybase[e] += __popc(peers);
     __syncwarp();
     if (e >= 0) {
       if (src) src[pos] = static_cast<int32_t>(a);
@@ -147,12 +189,11 @@ static void permute_impl(const int32_t* idx, const float* w, const int32_t* toke
                          int k, int E, int32_t* chunk_hist, int32_t* counts, int32_t* offsets, int32_t* src,
                          int32_t* dst, int32_t* row_token, float* row_w, int32_t* status, cudaStream_t stream) {
   const int nchunks = static_cast<int>(perm_num_chunks(A));
-  const int blocks = (nchunks + kPermWarps - 1) / kPermWarps;
-  const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
-  perm_hist_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, A, len, E, nchunks, chunk_hist, status);
+  perm_hist_kernel<<<nchunks, kPermWarps * 32, static_cast<size_t>(E) * sizeof(int32_t), stream>>>(
+      idx, A, len, E, nchunks, chunk_hist, status);
   perm_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, E, nchunks, counts, offsets);
-  perm_scatter_kernel<<<blocks, kPermWarps * 32, smem, stream>>>(idx, w, token_of, A, len, k, E, nchunks, chunk_hist,
-                                                                 src, dst, row_token, row_w);
+  perm_scatter_kernel<<<nchunks, kPermWarps * 32, static_cast<size_t>(kPermWarps) * E * sizeof(int32_t), stream>>>(
+      idx, w, token_of, A, len, k, E, nchunks, chunk_hist, src, dst, row_token, row_w);
 }
 
 void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,

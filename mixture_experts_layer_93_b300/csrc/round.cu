@@ -14,9 +14,9 @@
 // Launches (all deterministic; the only atomics are bitwise ORs):
 //   member   bitmap of the top-k sets, expert-major [E][ceil(T/32)]
 //   select   one block per expert: exact selection of the joining / staying
-//            tokens by bisection on the (logit, token) order -> final bitmap
-//   count    per-token size of the final set
-//   scan     exclusive prefix over tokens -> tok_offsets
+//            tokens by radix select on the (logit, token) order -> final bitmap
+//   transpose  the final bitmap to token-major words (warp ballots)
+//   offsets  per-token set sizes and their exclusive prefix -> tok_offsets
 //   sets     per token (a warp each): its experts in (logit desc, id asc)
 //            order and their softmax weights, written in token order
 //   permute  the stable counting sort of moe_permute over that list
@@ -35,13 +35,14 @@ inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
 struct RoundScratch {
   uint32_t* member;     // [E][W]
   uint32_t* final_set;  // [E][W]
-  int32_t* tok_count;   // [T + 1]
+  uint32_t* tok_bits;   // [T][EW] token-major final membership
   int32_t* tok_expert;  // [cap]
   float* tok_w;         // [cap]
   int32_t* tok_token;   // [cap]
   int32_t* new_counts;  // [E]
   int32_t* chunk_hist;  // [E][nchunks(cap)]
   uint32_t* keys;       // [E][T] when a column does not fit in shared memory
+  int32_t* block_sums;  // [ceil(T/1024)]
 };
 
 constexpr int kSmemKeyLimit = 49152;  // tokens whose keys fit in shared memory
@@ -55,8 +56,8 @@ RoundScratch carve(void* base, int T, int E, int64_t cap) {
   off = align256(off + E * W * 4);
   s.final_set = reinterpret_cast<uint32_t*>(p + off);
   off = align256(off + E * W * 4);
-  s.tok_count = reinterpret_cast<int32_t*>(p + off);
-  off = align256(off + (T + 1) * 4);
+  s.tok_bits = reinterpret_cast<uint32_t*>(p + off);
+  off = align256(off + static_cast<int64_t>(T) * ((E + 31) / 32) * 4);
   s.tok_expert = reinterpret_cast<int32_t*>(p + off);
   off = align256(off + cap * 4);
   s.tok_w = reinterpret_cast<float*>(p + off);
@@ -67,14 +68,18 @@ RoundScratch carve(void* base, int T, int E, int64_t cap) {
   off = align256(off + E * 4);
   s.chunk_hist = reinterpret_cast<int32_t*>(p + off);
   off = align256(off + E * perm_num_chunks(cap) * 4);
+  s.block_sums = reinterpret_cast<int32_t*>(p + off);
+  off = align256(off + ((T + 1023) / 1024) * 4);
   s.keys = reinterpret_cast<uint32_t*>(p + off);
   return s;
 }
 
 int64_t scratch_size(int T, int E, int64_t cap) {
   const int64_t W = words_per_row(T);
-  return align256(E * W * 4) * 2 + align256((T + 1) * 4) + align256(cap * 4) * 3 + align256(E * 4) +
-         align256(E * perm_num_chunks(cap) * 4) + (T > kSmemKeyLimit ? align256(int64_t(E) * T * 4) : 0);
+  return align256(E * W * 4) * 2 + align256(static_cast<int64_t>(T) * ((E + 31) / 32) * 4) + align256(cap * 4) * 3 +
+         align256(E * 4) +
+         align256(E * perm_num_chunks(cap) * 4) + align256(((T + 1023) / 1024) * 4) +
+         (T > kSmemKeyLimit ? align256(int64_t(E) * T * 4) : 0);
 }
 
 // Total order key of a logit: larger float -> larger key; -0.0 and +0.0 equal.
@@ -116,25 +121,13 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
   return red[32];
 }
 
-// Keys of the candidates of one expert (0 for non-candidates; every real key
-// is > 0), cached in shared memory or, for long columns, in a global row.
-__device__ int count_ge(const uint32_t* keys, int T, uint32_t v, int* red) {
-  int c = 0;
-  for (int t = threadIdx.x; t < T; t += kSelectThreads) c += keys[t] >= v;
-  return block_sum(c, red);
-}
-
-__device__ int count_eq_upto(const uint32_t* keys, uint32_t v, int tmax, int* red) {
-  int c = 0;
-  for (int t = threadIdx.x; t <= tmax; t += kSelectThreads) c += keys[t] == v;
-  return block_sum(c, red);
-}
-
 // One block per expert.  Among the candidates (members when dropping,
-// non-members when adding) finds the m best in the order (L desc, t asc):
-// v* = the m-th largest key (bisection on the 32-bit key), then among
-// candidates with key == v* the lowest t up to t* (bisection on t).  Writes
-// the final membership row and the rounded count.
+// non-members when adding) keeps the m best in the order (L desc, t asc):
+// a 4-pass radix select (8 bits a pass, from the top) finds v* = the m-th
+// largest 32-bit key and how many keys equal to v* to take; one ordered pass
+// over t then finds t*, the last tie taken (lowest t first).  Keys of
+// non-candidates are 0 (every real key is > 0).  Writes the final membership
+// row and the rounded count.
 __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const float* __restrict__ L, int T, int E,
                                                                       int64_t W, int tile, int mode,
                                                                       const uint32_t* __restrict__ member,
@@ -144,6 +137,9 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
                                                                       int keys_in_smem) {
   extern __shared__ uint32_t smem_keys[];
   __shared__ int red[33];
+  __shared__ int hist[256];
+  __shared__ int sel[2];  // chosen digit, remaining rank
+  __shared__ int tstar_s;
   const int e = blockIdx.x;
   const uint32_t* mrow = member + static_cast<int64_t>(e) * W;
   uint32_t* frow = final_set + static_cast<int64_t>(e) * W;
@@ -166,32 +162,110 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
   uint32_t vstar = 0xFFFFFFFFu;
   int tstar = -1;
   if (select) {
-    for (int t = threadIdx.x; t < T; t += kSelectThreads) {
-      const uint32_t mbit = (mrow[t >> 5] >> (t & 31)) & 1u;
-      keys[t] = (mbit == want) ? order_key(L[static_cast<int64_t>(t) * E + e]) : 0u;
+    // the column L[:, e] is strided in memory: issue 8 loads before using any
+    for (int tb = 0; tb < T; tb += 8 * kSelectThreads) {
+      float lv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = tb + j * kSelectThreads + threadIdx.x;
+        lv[j] = (t < T) ? L[static_cast<int64_t>(t) * E + e] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int t = tb + j * kSelectThreads + threadIdx.x;
+        if (t < T) {
+          const uint32_t mbit = (mrow[t >> 5] >> (t & 31)) & 1u;
+          keys[t] = (mbit == want) ? order_key(lv[j]) : 0u;
+        }
+      }
+    }
+    uint32_t prefix = 0, pmask = 0;
+    int rem = m;  // rank still to find among keys matching the prefix
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kSelectThreads) hist[i] = 0;
+      __syncthreads();
+      // counts only: the order of the additions does not matter
+      for (int t = threadIdx.x; t < T; t += kSelectThreads) {
+        const uint32_t kk = keys[t];
+        if (kk != 0u && (kk & pmask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        // lane l owns digits 255-8l .. 248-8l (descending)
+        const int lane = threadIdx.x;
+        int mine = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine += hist[255 - 8 * lane - j];
+        int incl = mine;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        const int before = incl - mine;
+        if (before < rem && rem <= incl) {
+          int cum = before;
+          for (int j = 0; j < 8; ++j) {
+            const int dgt = 255 - 8 * lane - j;
+            if (cum + hist[dgt] >= rem) {
+              sel[0] = dgt;
+              sel[1] = rem - cum;
+              break;
+            }
+            cum += hist[dgt];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(sel[0]) << shift;
+      pmask |= 255u << shift;
+      rem = sel[1];
+      __syncthreads();
+    }
+    vstar = prefix;
+    // the rem lowest-t keys equal to v* are taken.  Warp w owns the t range
+    // [w*R, (w+1)*R) and reads it 32 at a time (coalesced); ballots keep t
+    // order; a scan over the warp totals finds the warp holding the rem-th tie.
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    constexpr int kWarps = kSelectThreads / 32;
+    const int R = (T + kWarps - 1) / kWarps;
+    const int tb = wid * R, te = min(T, tb + R);
+    int cnt = 0;
+    for (int base = tb; base < te; base += 32) {
+      const int t = base + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, t < te && keys[t] == vstar));
+    }
+    if (threadIdx.x == 0) tstar_s = -1;
+    __syncthreads();
+    if (lane == 0) red[wid] = cnt;
+    __syncthreads();
+    int wbefore = 0;
+    for (int i = 0; i < wid; ++i) wbefore += red[i];
+    if (wbefore < rem && rem <= wbefore + cnt) {
+      int running = wbefore;
+      for (int base = tb; base < te; base += 32) {
+        const int t = base + lane;
+        const uint32_t bal = __ballot_sync(0xffffffffu, t < te && keys[t] == vstar);
+        const int nb = __popc(bal);
+        if (running + nb >= rem) {
+          // the (rem - running)-th set bit of bal, counted from bit 0
+          int need = rem - running, pos = -1;
+          for (int bit = 0; bit < 32; ++bit) {
+            if ((bal >> bit) & 1u) {
+              if (--need == 0) {
+                pos = bit;
+                break;
+              }
+            }
+          }
+          if (lane == 0) tstar_s = base + pos;
+          break;
+        }
+        running += nb;
+      }
     }
     __syncthreads();
-    // largest v with count(key >= v) >= m
-    uint32_t lo = 1, hi = 0xFFFFFFFFu;
-    while (lo < hi) {
-      const uint32_t mid = lo + (hi - lo + 1) / 2;
-      if (count_ge(keys, T, mid, red) >= m)
-        lo = mid;
-      else
-        hi = mid - 1;
-    }
-    vstar = lo;
-    const int greater = (vstar == 0xFFFFFFFFu) ? 0 : count_ge(keys, T, vstar + 1, red);
-    const int need = m - greater;  // ties at v* to take, lowest t first
-    int tlo = 0, thi = T - 1;
-    while (tlo < thi) {
-      const int mid = (tlo + thi) / 2;
-      if (count_eq_upto(keys, vstar, mid, red) >= need)
-        thi = mid;
-      else
-        tlo = mid + 1;
-    }
-    tstar = tlo;
+    tstar = tstar_s;
   }
   for (int64_t w = threadIdx.x; w < W; w += kSelectThreads) {
     const uint32_t mw = mrow[w];
@@ -213,59 +287,89 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
   if (threadIdx.x == 0) new_counts[e] = c2;
 }
 
-__global__ void token_count_kernel(const uint32_t* __restrict__ final_set, int T, int E, int64_t W,
-                                   int32_t* __restrict__ tok_count) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T) return;
-  int c = 0;
-  for (int e = 0; e < E; ++e) c += (final_set[static_cast<int64_t>(e) * W + (t >> 5)] >> (t & 31)) & 1u;
-  tok_count[t] = c;
+// Expert-major membership bits [E][W] -> token-major [T][EW] (EW = E/32
+// rounded up): one warp per 32 experts x 32 tokens block; lane i holds expert
+// 32*eb+i's word, and a ballot over lanes of bit j is token j's 32 experts.
+__global__ void bits_transpose_kernel(const uint32_t* __restrict__ final_set, int T, int E, int64_t W, int EW,
+                                      uint32_t* __restrict__ tok_bits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nblk = static_cast<int64_t>(EW) * W;
+  if (wg >= nblk) return;
+  const int eb = static_cast<int>(wg / W);
+  const int64_t tw = wg % W;
+  const int e = eb * 32 + lane;
+  const uint32_t word = (e < E) ? final_set[static_cast<int64_t>(e) * W + tw] : 0u;
+  uint32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t col = __ballot_sync(0xffffffffu, (word >> j) & 1u);
+    if (lane == j) mine = col;
+  }
+  const int64_t t = tw * 32 + lane;
+  if (t < T) tok_bits[t * EW + eb] = mine;
 }
 
-// Exclusive scan of tok_count[0..T) into tok_offsets[0..T]; one block.
-__global__ void __launch_bounds__(1024) token_scan_kernel(const int32_t* __restrict__ tok_count, int T,
-                                                          int32_t* __restrict__ tok_offsets) {
+// Per-token set sizes and their exclusive prefix, in two launches: block b
+// scans the sizes of tokens [1024b, 1024b+1024) (coalesced, warp shuffles)
+// into tok_offsets and its total into block_sums[b]; then every block adds
+// the sum of the earlier blocks' totals.
+__global__ void __launch_bounds__(1024) token_offsets_local_kernel(const uint32_t* __restrict__ tok_bits, int T,
+                                                                   int EW, int32_t* __restrict__ tok_offsets,
+                                                                   int32_t* __restrict__ block_sums) {
   __shared__ int32_t warp_s[32];
-  __shared__ int32_t carry_s;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) carry_s = 0;
+  const int t = blockIdx.x * 1024 + tid;
+  int32_t v = 0;
+  if (t < T)
+    for (int w = 0; w < EW; ++w) v += __popc(tok_bits[static_cast<int64_t>(t) * EW + w]);
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_s[wid] = incl;
   __syncthreads();
-  for (int base = 0; base < T; base += 1024) {
-    const int t = base + tid;
-    const int32_t v = (t < T) ? tok_count[t] : 0;
-    int32_t incl = v;
+  if (wid == 0) {
+    int32_t s = warp_s[lane];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+      const int32_t o = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += o;
     }
-    if (lane == 31) warp_s[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      int32_t s = warp_s[lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int32_t o = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s += o;
-      }
-      warp_s[lane] = s;
-    }
-    __syncthreads();
-    const int32_t carry = carry_s;
-    const int32_t excl = carry + incl - v + (wid > 0 ? warp_s[wid - 1] : 0);
-    if (t < T) tok_offsets[t] = excl;
-    __syncthreads();
-    if (tid == 1023) carry_s = excl + v;
-    __syncthreads();
+    warp_s[lane] = s;
   }
-  if (tid == 0) tok_offsets[T] = carry_s;
+  __syncthreads();
+  const int32_t excl = incl - v + (wid > 0 ? warp_s[wid - 1] : 0);
+  if (t < T) tok_offsets[t] = excl;
+  if (tid == 1023) block_sums[blockIdx.x] = excl + v;
 }
 
-// One warp per token: its final experts in (logit desc, id asc) order, and
+__global__ void __launch_bounds__(1024) token_offsets_add_kernel(int T, int32_t* __restrict__ tok_offsets,
+                                                                 const int32_t* __restrict__ block_sums) {
+  __shared__ int32_t base_s;
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int32_t s = 0;
+    for (int i = tid; i < static_cast<int>(blockIdx.x); i += 32) s += block_sums[i];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (tid == 0) base_s = s;
+  }
+  __syncthreads();
+  const int t = blockIdx.x * 1024 + tid;
+  if (t < T) tok_offsets[t] += base_s;
+  if (t == T - 1) tok_offsets[T] = base_s + block_sums[blockIdx.x];
+}
+
+// One warp per token: its final experts in (logit desc, id asc) order and
 // softmax weights over them (fp32, exp of the logit minus the set's max,
-// summed in list order).
-__global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict__ L, const uint32_t* __restrict__ final_set,
-                                                         int T, int E, int64_t W,
+// summed in list order).  Lane l holds experts l, l+32, ... (membership bit
+// and logit in registers), as in the top-k kernel.
+template <int NV>
+__global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict__ L,
+                                                         const uint32_t* __restrict__ tok_bits, int T, int E, int EW,
                                                          const int32_t* __restrict__ tok_offsets,
                                                          int32_t* __restrict__ tok_expert, float* __restrict__ tok_w,
                                                          int32_t* __restrict__ tok_token) {
@@ -276,23 +380,28 @@ __global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict
   const int cnt = tok_offsets[t + 1] - off;
   if (cnt == 0) return;
   const float* row = L + static_cast<int64_t>(t) * E;
+  const uint32_t* bits = tok_bits + static_cast<int64_t>(t) * EW;
+  float v[NV];
+  uint32_t eligible = 0;  // bit i: expert lane + 32*i is in the final set
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = -INFINITY;
+    if (e < E && i < EW && ((bits[i] >> lane) & 1u)) {
+      eligible |= 1u << i;
+      const float x = row[e];
+      v[i] = (x != x) ? -INFINITY : x;
+    }
+  }
   float vmax = 0.f, sum = 0.f;
-  // rounds of a warp arg-max over the experts still eligible; experts are
-  // visited lane + 32*i, eligibility re-read from the bitmap each round
-  uint32_t taken = 0;  // bit i: expert lane + 32*i already placed
   for (int j = 0; j < cnt; ++j) {
     float bv = -INFINITY;
     int bid = 0x7fffffff;
-    for (int i = 0; 32 * i < E; ++i) {
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      if (e >= E) break;
-      const bool in = ((final_set[static_cast<int64_t>(e) * W + (t >> 5)] >> (t & 31)) & 1u) &&
-                      !((taken >> i) & 1u);
-      if (!in) continue;
-      float v = row[e];
-      if (v != v) v = -INFINITY;
-      if (v > bv || (v == bv && e < bid)) {
-        bv = v;
+      if (((eligible >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bid))) {
+        bv = v[i];
         bid = e;
       }
     }
@@ -305,7 +414,7 @@ __global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict
         bid = oid;
       }
     }
-    if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+    if ((bid & 31) == lane) eligible &= ~(1u << (bid >> 5));
     if (j == 0) vmax = bv;
     const float ex = expf(bv - vmax);
     sum += ex;
@@ -317,6 +426,26 @@ __global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict
   }
   __syncwarp();
   for (int j = lane; j < cnt; j += 32) tok_w[off + j] = tok_w[off + j] / sum;
+}
+
+void launch_token_sets(const float* L, const uint32_t* tok_bits, int T, int E, int EW, const int32_t* tok_offsets,
+                       int32_t* tok_expert, float* tok_w, int32_t* tok_token, cudaStream_t stream) {
+  const int blocks = (T + 7) / 8;
+#define MOE_SETS(NV) \
+  token_sets_kernel<NV><<<blocks, 256, 0, stream>>>(L, tok_bits, T, E, EW, tok_offsets, tok_expert, tok_w, tok_token)
+  if (EW <= 1)
+    MOE_SETS(1);
+  else if (EW <= 2)
+    MOE_SETS(2);
+  else if (EW <= 4)
+    MOE_SETS(4);
+  else if (EW <= 8)
+    MOE_SETS(8);
+  else if (EW <= 16)
+    MOE_SETS(16);
+  else
+    MOE_SETS(32);
+#undef MOE_SETS
 }
 
 }  // namespace
@@ -341,10 +470,14 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
                        static_cast<int>(kSmemKeyLimit) * 4);
   round_select_kernel<<<E, kSelectThreads, key_smem, stream>>>(logits, T, E, W, tile, mode, s.member, s.final_set,
                                                               s.new_counts, s.keys, in_smem);
-  token_count_kernel<<<(T + 255) / 256, 256, 0, stream>>>(s.final_set, T, E, W, s.tok_count);
-  token_scan_kernel<<<1, 1024, 0, stream>>>(s.tok_count, T, tok_offsets);
-  token_sets_kernel<<<(T + 7) / 8, 256, 0, stream>>>(logits, s.final_set, T, E, W, tok_offsets, s.tok_expert,
-                                                     s.tok_w, s.tok_token);
+  const int EW = (E + 31) / 32;
+  const int64_t tblocks = static_cast<int64_t>(EW) * W;  // warps
+  bits_transpose_kernel<<<static_cast<int>((tblocks * 32 + 255) / 256), 256, 0, stream>>>(s.final_set, T, E, W, EW,
+                                                                                         s.tok_bits);
+  const int tb = (T + 1023) / 1024;
+  token_offsets_local_kernel<<<tb, 1024, 0, stream>>>(s.tok_bits, T, EW, tok_offsets, s.block_sums);
+  token_offsets_add_kernel<<<tb, 1024, 0, stream>>>(T, tok_offsets, s.block_sums);
+  launch_token_sets(logits, s.tok_bits, T, E, EW, tok_offsets, s.tok_expert, s.tok_w, s.tok_token, stream);
   // stable grouping by expert of the token-ordered list: rows of an expert
   // come out in ascending t; tok_rows is the list's row map (moe_permute's dst)
   launch_permute_list(s.tok_expert, s.tok_w, s.tok_token, tok_offsets + T, cap, E, s.chunk_hist, counts, offsets,
