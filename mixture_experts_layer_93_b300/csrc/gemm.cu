@@ -91,11 +91,10 @@ struct GemmCfg {
   static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
   static constexpr int PREFIX_BYTES = 1025 * 4;
   static constexpr int TOK_BYTES = BM * 4;
-  // slack after the last tile: a pair MMA reading past a B half stays inside
-  // this CTA's allocation
-  static constexpr int SLACK_BYTES = PAIR ? B_BYTES : 0;
+  // epilogue staging for TMA stores: per epilogue warp two 32 x 64-byte boxes
+  static constexpr int STAGE_OUT_BYTES = 4 * 2 * 32 * 64;
   static constexpr int SMEM_BYTES =
-      1024 + STAGES * STAGE_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES + SLACK_BYTES;
+      1024 + STAGES * STAGE_BYTES + STAGE_OUT_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES;
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -146,14 +145,15 @@ __device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_
 template <int BN, int MODE, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN, PAIR>;
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
   uint8_t* sB = base + C::STAGES * C::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::STAGES * C::STAGE_BYTES);
+  uint8_t* sOut = base + C::STAGES * C::STAGE_BYTES;  // 1024-aligned: STAGE_BYTES is a multiple of 1024
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + C::STAGE_OUT_BYTES);
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + C::STAGES;
   uint64_t* tfull_bar = bars + 2 * C::STAGES;
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* afull_bar = bars + 2 * C::STAGES + 4;  // PAIR + gather 2: this CTA's rows landed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * C::STAGES + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int32_t* prefix = reinterpret_cast<int32_t*>(base + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+  int32_t* prefix = reinterpret_cast<int32_t*>(sOut + C::STAGE_OUT_BYTES + C::BAR_BYTES);
   int32_t* tok_s = prefix + 1025;  // gather 2: token of each row of the current tile
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (MODE != kModeRouter) tma_prefetch_desc(&tmC);
   } else if (warp == kMmaWarp) {
     if (PAIR) {
       tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -404,6 +405,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r_in_tile = ew * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // 32 rows x 32 columns of 16-bit outputs per chunk go through one of this
+    // warp's two staging boxes (64-byte rows, 64-byte swizzle) to a TMA store
+    uint8_t* stage_out = sOut + ew * (2 * 32 * 64);
+    int out_buf = 0;
+    auto store_chunk = [&](const uint32_t (&o)[16], int col, int64_t row_w0, int warp_rows, int64_t row,
+                           auto* dst_row) {
+      if (warp_rows == 32) {
+        uint8_t* buf = stage_out + out_buf * (32 * 64);
+        if (lane == 0) bulk_wait_read<1>();  // the box used two chunks ago was read
+        __syncwarp();
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ sw) << 4)) =
+              make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, col, static_cast<int32_t>(row_w0), smem_u32(buf));
+          bulk_commit();
+        }
+        out_buf ^= 1;
+      } else if (lane < warp_rows) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      }
+      (void)row;
+    };
     for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
       int e, nb, mu, gstart, gcount;
       decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
@@ -420,6 +450,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
       const bool valid = r_in_tile < rows_valid;
       const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
+      const int warp_rows = max(0, min(32, rows_valid - ew * 32));
+      const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
       if constexpr (MODE == kModeUp) {
         constexpr int H = BN / 2;
         __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
@@ -438,11 +470,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
             o[q] = pack_bf16x2(h0, h1);
           }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
+          if (warp_rows > 0) store_chunk(o, nb * H + c, row_w0, warp_rows, row, dst + c);
         }
       } else if constexpr (MODE == kModeDown) {
         // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
@@ -464,11 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
             o[q] = pack_half2(a, b);
           }
-          if (valid) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) d4[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
+          if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
         }
         if (overflow && valid) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
       } else {
@@ -508,6 +532,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();  // our TMA stores have landed before the CTA exits
+    __syncwarp();
   }
 
   __syncthreads();
@@ -549,17 +575,28 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] (inner contiguous), box [box_outer, 64], 128-byte swizzle.
-static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+// 2-D 16-bit tensor [outer, inner] (inner contiguous).
+static bool make_map_16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Operand tile: bf16 box [box_outer rows, 64], 128-byte swizzle.
+static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  return make_map_16(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, inner, outer, 64, box_outer,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Output tile for the epilogue's TMA stores: box [32 rows, 32], 64-byte swizzle.
+static bool make_map_out(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner, uint64_t outer) {
+  return make_map_16(m, dt, ptr, inner, outer, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int num_sms() {
@@ -570,13 +607,14 @@ int num_sms() {
 }
 
 template <int BN, int MODE, bool PAIR>
-static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p, cudaStream_t stream) {
+static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
+                       cudaStream_t stream) {
   using C = GemmCfg<BN, PAIR>;
   auto kern = moe_gemm_kernel<BN, MODE, PAIR>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!PAIR) {
-    kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, p);
+    kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -596,7 +634,7 @@ static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gem
   cfg.gridDim = dim3(num_sms() & ~1);
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) clusters = num_sms() / 2;
   cfg.gridDim = dim3(2 * std::min(clusters, num_sms() / 2));
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, p) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p) != cudaSuccess) return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -642,6 +680,8 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
     if (!make_map_bf16(&tmA, xperm_scratch, d, rows_cap, 128)) return MOE_ERR_CUDA;
   }
   const bool pair = (gather == 0 || gather == 2) && BN == 256;
+  CUtensorMap tmC;
+  if (!make_map_out(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, n, rows_cap)) return MOE_ERR_CUDA;
   if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, pair ? BN / 2 : BN)) return MOE_ERR_CUDA;
   GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
@@ -660,18 +700,18 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
     // complete pairs of 128-row blocks on SM pairs, then each expert's odd
     // last block on single SMs (so no pair runs half empty)
     p.units = 1;
-    int st = (BN == 256) ? launch_gemm<256, kModeUp, true>(tmA, tmB, p, stream)
-                         : launch_gemm<128, kModeUp, true>(tmA, tmB, p, stream);
+    int st = (BN == 256) ? launch_gemm<256, kModeUp, true>(tmA, tmB, tmC, p, stream)
+                         : launch_gemm<128, kModeUp, true>(tmA, tmB, tmC, p, stream);
     if (st != MOE_OK) return st;
     CUtensorMap tmB1;
     if (!make_map_bf16(&tmB1, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
     p.units = 2;
-    return (BN == 256) ? launch_gemm<256, kModeUp, false>(tmA, tmB1, p, stream)
-                       : launch_gemm<128, kModeUp, false>(tmA, tmB1, p, stream);
+    return (BN == 256) ? launch_gemm<256, kModeUp, false>(tmA, tmB1, tmC, p, stream)
+                       : launch_gemm<128, kModeUp, false>(tmA, tmB1, tmC, p, stream);
   }
   p.units = 0;
-  if (BN == 256) return launch_gemm<256, kModeUp, false>(tmA, tmB, p, stream);
-  return launch_gemm<128, kModeUp, false>(tmA, tmB, p, stream);
+  if (BN == 256) return launch_gemm<256, kModeUp, false>(tmA, tmB, tmC, p, stream);
+  return launch_gemm<128, kModeUp, false>(tmA, tmB, tmC, p, stream);
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
@@ -681,6 +721,8 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, h, n, rows_cap, 128)) return MOE_ERR_CUDA;
   if (!make_map_bf16(&tmB, W2p, n, static_cast<uint64_t>(E) * d, BN / 2)) return MOE_ERR_CUDA;
+  CUtensorMap tmC;
+  if (!make_map_out(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ys, d, rows_cap)) return MOE_ERR_CUDA;
   GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
@@ -693,16 +735,16 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.b_rows_per_expert = d;
   p.gather = 0;
   p.units = 1;
-  int st = (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, p, stream)
-           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, p, stream)
-                         : launch_gemm<64, kModeDown, true>(tmA, tmB, p, stream);
+  int st = (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, tmC, p, stream)
+           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, tmC, p, stream)
+                         : launch_gemm<64, kModeDown, true>(tmA, tmB, tmC, p, stream);
   if (st != MOE_OK) return st;
   CUtensorMap tmB1;
   if (!make_map_bf16(&tmB1, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;
   p.units = 2;
-  return (BN == 256)   ? launch_gemm<256, kModeDown, false>(tmA, tmB1, p, stream)
-         : (BN == 128) ? launch_gemm<128, kModeDown, false>(tmA, tmB1, p, stream)
-                       : launch_gemm<64, kModeDown, false>(tmA, tmB1, p, stream);
+  return (BN == 256)   ? launch_gemm<256, kModeDown, false>(tmA, tmB1, tmC, p, stream)
+         : (BN == 128) ? launch_gemm<128, kModeDown, false>(tmA, tmB1, tmC, p, stream)
+                       : launch_gemm<64, kModeDown, false>(tmA, tmB1, tmC, p, stream);
 }
 
 int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }
@@ -715,6 +757,7 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, x, d, T, 128)) return MOE_ERR_CUDA;
   if (!make_map_bf16(&tmB, Wr3, d, static_cast<uint64_t>(nblk) * BN, BN)) return MOE_ERR_CUDA;
+  const CUtensorMap& tmC = tmA;  // the router epilogue stores fp32 logits directly
   GemmParams p = base_params(status, timeout_ns);
   p.single_rows = T;
   p.bias = bias;
@@ -726,9 +769,9 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   p.n_blocks = nblk;
   p.b_rows_per_expert = 0;
   p.gather = 0;
-  if (BN == 48) return launch_gemm<48, kModeRouter, false>(tmA, tmB, p, stream);
-  if (BN == 96) return launch_gemm<96, kModeRouter, false>(tmA, tmB, p, stream);
-  return launch_gemm<192, kModeRouter, false>(tmA, tmB, p, stream);
+  if (BN == 48) return launch_gemm<48, kModeRouter, false>(tmA, tmB, tmC, p, stream);
+  if (BN == 96) return launch_gemm<96, kModeRouter, false>(tmA, tmB, tmC, p, stream);
+  return launch_gemm<192, kModeRouter, false>(tmA, tmB, tmC, p, stream);
 }
 
 // Wr [d, E] fp32 -> Wr3 [nblk * 3EB, d] bf16: for expert block b, rows
