@@ -44,8 +44,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one up-projection launch from an ncu capture of
 # the current kernel (profiles/moe_gemm_mixtral.md), keyed by workload, A path
 # and kernel revision; a kernel change bumps GEMM_REV and drops stale entries.
-GEMM_REV = "cta-pair-v4"
-UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2013502720 + 458782208}
+GEMM_REV = "cta-pair-tma-store-v6"
+UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2118082048 + 459504128}
 
 
 def load_peaks():
@@ -267,7 +267,11 @@ def run_ours(args, world, rank, local):
     # select, transpose, 2 offsets, sets + a 3-launch permutation (9); up: row gather + SM-pair GEMM + odd-block GEMM
     # (A path 0) or one GEMM (paths 1, 2); down: SM-pair + odd-block GEMMs;
     # combine: 1
-    launches_per_step = 3 + (3 if mode == "off" else 9) + (3 if args.gather == 0 else 1) + 2 + 1
+    # SM-pair GEMMs run an expert's odd last block in the same launch when
+    # odd blocks are a small share (128 E <= 0.15 rows), else in a second one
+    gemm_launches = 1 if 128.0 * E <= 0.15 * cap else 2
+    up_launches = (1 + gemm_launches) if args.gather == 0 else (gemm_launches if d % 1 == 0 and n % 128 == 0 else 1)
+    launches_per_step = 3 + (3 if mode == "off" else 9) + up_launches + gemm_launches + 1
 
     def check(rc, what):
         if rc != 0:

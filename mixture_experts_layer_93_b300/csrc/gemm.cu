@@ -117,17 +117,18 @@ __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int 
 }
 
 // Tile units of a group with mblocks 128-row blocks: 0 every block, 1
-// complete pairs, 2 the odd last block.  (Running the odd block as a
-// half-empty pair instead measured 3 % slower on the DeepSeek-V3 shape.)
+// complete pairs, 2 the odd last block, 3 pairs with the odd last block run as
+// a half-empty pair.
 __device__ __forceinline__ int tile_units(int units, int mblocks) {
   if (units == 0) return mblocks;
   if (units == 1) return mblocks / 2;
-  return mblocks & 1;
+  if (units == 2) return mblocks & 1;
+  return (mblocks + 1) / 2;
 }
 
 // 128-row block of unit mu handled by CTA `rank`.
 __device__ __forceinline__ int unit_block(int units, int mu, int rank, int gcount) {
-  if (units == 1) return 2 * mu + rank;
+  if (units == 1 || units == 3) return 2 * mu + rank;
   if (units == 2) return (gcount + 127) / 128 - 1;
   return mu;
 }
@@ -657,6 +658,15 @@ void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const 
   gather_rows_kernel<<<num_sms() * 8, 256, 0, stream>>>(x, row_token, offsets, E, d, out, rows_cap);
 }
 
+// How SM-pair GEMMs treat an expert's odd last 128-row block.  Run as a
+// half-empty pair inside the main kernel, it costs one pair tile of MMA time
+// but reuses the expert's weights from L2; run by a separate single-SM launch,
+// it costs half that MMA time but streams those weights from HBM again.  With
+// about half the experts odd, odd blocks are ~128*E/rows of all pair tiles:
+// measured, half-empty pairs win at 6 % (Mixtral-style +5.5 %, 7B-style
+// +1.5 %) and lose at 25 % (DeepSeek-V3-style -3.5 %).
+static bool tails_in_pairs(int E, int64_t rows) { return 128.0 * E <= 0.15 * static_cast<double>(rows); }
+
 static GemmParams base_params(int32_t* status, uint64_t timeout_ns) {
   GemmParams p{};
   p.status = status;
@@ -696,6 +706,11 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   p.gather = gather;
   p.x = x;
   p.lda = d;
+  if (pair && tails_in_pairs(E, rows_cap)) {
+    p.units = 3;
+    return (BN == 256) ? launch_gemm<256, kModeUp, true>(tmA, tmB, tmC, p, stream)
+                       : launch_gemm<128, kModeUp, true>(tmA, tmB, tmC, p, stream);
+  }
   if (pair) {
     // complete pairs of 128-row blocks on SM pairs, then each expert's odd
     // last block on single SMs (so no pair runs half empty)
@@ -734,6 +749,12 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.n_blocks = d / BN;
   p.b_rows_per_expert = d;
   p.gather = 0;
+  if (tails_in_pairs(E, rows_cap)) {
+    p.units = 3;
+    return (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, tmC, p, stream)
+           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, tmC, p, stream)
+                         : launch_gemm<64, kModeDown, true>(tmA, tmB, tmC, p, stream);
+  }
   p.units = 1;
   int st = (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, tmC, p, stream)
            : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, tmC, p, stream)
