@@ -38,7 +38,9 @@ Readings of the pages (where they are silent or at odds):
     multiple, for at most one tile of deviation from top-k, and for an
     unchanged expected total.  Always rounding up raises the total, so the
     default mode rounds to the NEAREST multiple (half up); "up" is kept as the
-    literal variant.  Counts are capped at tile*floor(T/tile).  When the
+    literal variant, and "stochastic" rounds up with probability
+    (c mod tile)/tile (SplitMix64 on the counter seed*2^32+e), which keeps the
+    expected total exactly.  Counts are capped at tile*floor(T/tile).  When the
     rounded count c' exceeds c, the c'-c not-yet-routed tokens with the
     highest L[t,e] join (ties: lower t first); when c' < c, the c-c' routed
     tokens with the lowest L[t,e] leave (ties: higher t leaves first).  Each
@@ -62,6 +64,27 @@ F64 = np.float64
 ROUND_OFF = "off"
 ROUND_NEAREST = "nearest"
 ROUND_UP = "up"
+ROUND_STOCHASTIC = "stochastic"
+
+MASK64 = (1 << 64) - 1
+
+
+def splitmix64(state: int) -> int:
+    """One output of SplitMix64 (Steele, Lea, Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014) for the given 64-bit state:
+    the state is advanced by the golden-ratio increment, then mixed."""
+    z = (state + 0x9E3779B97F4A7C15) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def stochastic_round_up(c: int, tile: int, seed: int, e: int) -> bool:
+    """Whether expert e's count rounds up in the stochastic mode: with
+    probability (c mod tile) / tile, decided by the top 32 bits h of
+    SplitMix64(seed * 2^32 + e) as h * tile < (c mod tile) * 2^32."""
+    h = splitmix64(((seed & 0xFFFFFFFF) << 32) | (e & 0xFFFFFFFF)) >> 32
+    return h * tile < (c % tile) << 32
 
 
 def _f64(a) -> np.ndarray:
@@ -152,20 +175,24 @@ def permute(idx, E: int):
 # --------------------------------------------------------------------------
 # 6. token rounding
 # --------------------------------------------------------------------------
-def rounded_count(c: int, tile: int, mode: str, T: int) -> int:
-    """Per-expert token count after rounding to a multiple of `tile`."""
+def rounded_count(c: int, tile: int, mode: str, T: int, e: int = 0, seed: int = 0) -> int:
+    """Per-expert token count after rounding to a multiple of `tile`.  The
+    stochastic mode rounds up with probability (c mod tile)/tile, so the
+    expected count, and total, is unchanged."""
     if mode == ROUND_OFF:
         return int(c)
     if mode == ROUND_NEAREST:
         c2 = tile * ((c + tile // 2) // tile)
     elif mode == ROUND_UP:
         c2 = tile * (-(-c // tile))
+    elif mode == ROUND_STOCHASTIC:
+        c2 = tile * (c // tile) + (tile if stochastic_round_up(c, tile, seed, e) else 0)
     else:
         raise ValueError(mode)
     return int(min(c2, tile * (T // tile)))
 
 
-def token_round(L, idx, tile: int, mode: str):
+def token_round(L, idx, tile: int, mode: str, seed: int = 0):
     """Token rounding (SonicMoE page, "3. Token Rounding 路由算法").
 
     Returns a dict with
@@ -184,7 +211,7 @@ def token_round(L, idx, tile: int, mode: str):
     added, dropped = [], []
     for e in range(E):
         c = int(counts0[e])
-        c2 = rounded_count(c, tile, mode, T)
+        c2 = rounded_count(c, tile, mode, T, e, seed)
         add = np.zeros(0, np.int64)
         drop = np.zeros(0, np.int64)
         if c2 > c:
@@ -232,7 +259,7 @@ def expert_out(h, W2e) -> np.ndarray:
 # 5. full layer forward
 # --------------------------------------------------------------------------
 def route(x, Wr, bias, k: int, tile: int = 128, mode: str = ROUND_OFF, tokens=None,
-          logits=None):
+          logits=None, seed: int = 0):
     """Per-token expert sets and gate weights.
 
     Without rounding only the tokens in `tokens` (all when None) are routed.
@@ -257,20 +284,20 @@ def route(x, Wr, bias, k: int, tile: int = 128, mode: str = ROUND_OFF, tokens=No
     L64 = router_logits(x64, Wr, bias) if logits is None else np.asarray(logits, dtype=F64)
     Ld = decision_logits(L64)
     idx = topk(Ld, k)
-    r = token_round(Ld, idx, tile, mode)
+    r = token_round(Ld, idx, tile, mode, seed)
     sets = [r["sets"][t] for t in tokens]
     weights = [softmax(L64[t, s]) for t, s in zip(tokens, sets)]
     return tokens, sets, weights
 
 
 def moe_forward(x, Wr, bias, W1, W3, W2, k: int, tile: int = 128, mode: str = ROUND_OFF,
-                tokens=None, return_routing: bool = False):
+                tokens=None, return_routing: bool = False, seed: int = 0):
     """y[t] = sum_{e in S_t} w_te * FFN_e(x[t]) for the requested tokens, fp64.
 
     Dataflow of the moe_forward pseudocode ("MoE架构的物理瓶颈与扩展限制解析",
     section 工作原理) with both all-to-all steps removed (one GPU), and the
     five steps of the fused kernel ("硬件加速的考量", section 自定义核与核融合)."""
-    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, tokens)
+    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, tokens, seed=seed)
     x64 = _f64(x)
     d = x64.shape[1]
     y = np.zeros((len(tokens), d), dtype=F64)

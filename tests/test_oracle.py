@@ -242,9 +242,9 @@ def test_router_logits_one_hot_rows():
 
 
 # ------------------------------------------------------- token rounding
-def _check_rounding(L, idx, tile, mode):
+def _check_rounding(L, idx, tile, mode, seed=0):
     T, E = L.shape
-    r = O.token_round(L, idx, tile, mode)
+    r = O.token_round(L, idx, tile, mode, seed=seed)
     member0 = np.zeros((T, E), bool)
     member0[np.repeat(np.arange(T), idx.shape[1]), idx.reshape(-1)] = True
     c0 = member0.sum(0)
@@ -324,3 +324,39 @@ def test_rounded_forward_weights_and_empty_sets():
         if sz == 0:
             assert np.all(y[t] == 0.0)
     assert sum(sizes) % 16 == 0
+
+
+def test_splitmix64_published_sequence():
+    # the first outputs of SplitMix64 started from state 0 (each call adds the
+    # golden-ratio increment to the state before mixing)
+    expected = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+    state = 0
+    for want in expected:
+        assert O.splitmix64(state) == want
+        state = (state + 0x9E3779B97F4A7C15) & O.MASK64
+
+
+def test_stochastic_rounding_keeps_expected_count():
+    tile, big = 128, 10 ** 6
+    for c in (0, 1, 37, 64, 127, 128, 300):
+        vals = [O.rounded_count(c, tile, O.ROUND_STOCHASTIC, big, e=e, seed=s) for s in range(8) for e in range(512)]
+        lo = tile * (c // tile)
+        assert set(vals) <= {lo, lo + tile}
+        if c % tile == 0:
+            assert set(vals) == {c}
+        mean = sum(vals) / len(vals)
+        # 4096 Bernoulli draws: std of the mean <= tile * 0.5 / 64
+        assert abs(mean - c) <= 4 * tile * 0.5 / 64, (c, mean)
+
+
+@pytest.mark.parametrize("T,E,k,tile,seed", [(40, 5, 2, 8, 0), (64, 6, 3, 8, 7), (200, 9, 2, 16, 3)])
+def test_stochastic_token_rounding_brute_force(T, E, k, tile, seed):
+    L = grid_logits(T, E, seed=300 + seed)
+    idx = O.topk(L, k)
+    r = _check_rounding(L, idx, tile, O.ROUND_STOCHASTIC, seed=seed)
+    assert np.all(r["counts"] % tile == 0)
+    member0 = np.zeros((T, E), bool)
+    member0[np.repeat(np.arange(T), k), idx.reshape(-1)] = True
+    c0 = member0.sum(0)
+    for e in range(E):
+        assert abs(int(r["counts"][e]) - int(c0[e])) < tile
