@@ -217,7 +217,7 @@ def run_ours(args, world, rank, local):
         from dataclasses import replace
         cfg = replace(cfg, E=args.experts)
     mode = args.round
-    shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode)
+    shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
     inp = I.make_inputs(cfg, device=dev, seed=rank)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     inp_host = None
@@ -439,7 +439,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="mixtral", choices=sorted(I.CONFIGS))
-    ap.add_argument("--round", default="off", choices=["off", "nearest", "up"])
+    ap.add_argument("--round", default="off", choices=["off", "nearest", "up", "stochastic"])
+    ap.add_argument("--seed", type=int, default=0, help="seed of the stochastic rounding draws")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling of small cases only)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling of small cases only)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

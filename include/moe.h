@@ -67,7 +67,12 @@ typedef enum {
 typedef enum {
   MOE_ROUND_OFF = 0,        /* plain top-k routing */
   MOE_ROUND_NEAREST = 1,    /* each count to the nearest tile multiple, half up */
-  MOE_ROUND_UP = 2          /* each count up to a tile multiple */
+  MOE_ROUND_UP = 2,         /* each count up to a tile multiple */
+  MOE_ROUND_STOCHASTIC = 3  /* down, or up with probability (c mod tile)/tile:
+                               the expected count is c.  The draw for expert e
+                               is the top 32 bits h of SplitMix64 (Steele, Lea,
+                               Flood, OOPSLA 2014) at state seed*2^32 + e; the
+                               count rounds up iff h*tile < (c mod tile)*2^32 */
 } moe_round_mode;
 
 typedef struct {
@@ -78,6 +83,7 @@ typedef struct {
   int32_t k;      /* experts per token */
   int32_t tile;   /* token-rounding tile; ignored when round == MOE_ROUND_OFF */
   int32_t round;  /* moe_round_mode */
+  uint32_t seed;  /* MOE_ROUND_STOCHASTIC: seed of the per-expert draws */
 } moe_shape;
 
 /* Number of rows the expert GEMMs can see: T*k without rounding, T*k + E*tile
@@ -176,8 +182,9 @@ int moe_permute_noalloc(const moe_shape* s, const int32_t* topk_idx, const float
                         int32_t* row_token, float* row_w, void* stream);
 
 /* Token rounding ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化", 3. Token Rounding 路由算法),
- * mode s->round (NEAREST or UP), tile s->tile.  Each expert's count c becomes
- * c' = tile-multiple (nearest half-up, or up), capped at tile*floor(T/tile).
+ * mode s->round (NEAREST, UP or STOCHASTIC), tile s->tile.  Each expert's count
+ * c becomes c' = a tile multiple (nearest half-up, up, or stochastic with seed
+ * s->seed), capped at tile*floor(T/tile).
  * If c' > c the c'-c tokens not routed to e with the highest logits[t, e] join
  * (ties: lower t first); if c' < c the c-c' routed tokens with the lowest
  * logits leave (ties: higher t first); each expert is rounded from the original

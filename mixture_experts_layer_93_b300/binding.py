@@ -24,7 +24,7 @@ MOE_ERR_UNSUPPORTED = 4
 MOE_ERR_TIMEOUT = 5
 MOE_ERR_DEVICE_CHECK = 6
 
-ROUND_MODES = {"off": 0, "nearest": 1, "up": 2}
+ROUND_MODES = {"off": 0, "nearest": 1, "up": 2, "stochastic": 3}
 
 # workspace_layout slots
 WS_SLOTS = ["logits", "topk_idx", "topk_w", "counts", "offsets", "src", "dst", "row_token", "row_w",
@@ -43,7 +43,8 @@ class MoEError(RuntimeError):
 
 class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("n", ctypes.c_int32), ("E", ctypes.c_int32),
-                ("k", ctypes.c_int32), ("tile", ctypes.c_int32), ("round", ctypes.c_int32)]
+                ("k", ctypes.c_int32), ("tile", ctypes.c_int32), ("round", ctypes.c_int32),
+                ("seed", ctypes.c_uint32)]
 
 
 _P = ctypes.c_void_p
@@ -98,9 +99,9 @@ def status_string(status: int) -> str:
     return lib().moe_status_string(int(status)).decode()
 
 
-def make_shape(T, d, n, E, k, tile=128, round="off") -> moe_shape:
+def make_shape(T, d, n, E, k, tile=128, round="off", seed=0) -> moe_shape:
     mode = ROUND_MODES[round] if isinstance(round, str) else int(round)
-    return moe_shape(int(T), int(d), int(n), int(E), int(k), int(tile), mode)
+    return moe_shape(int(T), int(d), int(n), int(E), int(k), int(tile), mode, int(seed) & 0xFFFFFFFF)
 
 
 def _ptr(t):
@@ -308,16 +309,16 @@ def moe_selftest_timeout(ws: Workspace, timeout_ns: int):
 class MoELayer:
     """One MoE layer with its weights packed once and a reusable workspace."""
 
-    def __init__(self, Wr, bias, W1, W3, W2, k: int, tile: int = 128, round: str = "off"):
+    def __init__(self, Wr, bias, W1, W3, W2, k: int, tile: int = 128, round: str = "off", seed: int = 0):
         self.E, self.d, self.n = W1.shape
-        self.k, self.tile, self.round = k, tile, round
+        self.k, self.tile, self.round, self.seed = k, tile, round, seed
         self.Wr = Wr.contiguous()
         self.bias = bias.contiguous() if bias is not None else None
         self.W13p, self.W2p = moe_prepare_weights(W1.contiguous(), W3.contiguous(), W2.contiguous())
         self._ws = {}
 
     def shape(self, T: int) -> moe_shape:
-        return make_shape(T, self.d, self.n, self.E, self.k, self.tile, self.round)
+        return make_shape(T, self.d, self.n, self.E, self.k, self.tile, self.round, self.seed)
 
     def workspace(self, T: int, device) -> Workspace:
         key = (T, str(device))

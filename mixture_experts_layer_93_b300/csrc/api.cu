@@ -17,7 +17,7 @@ bool shape_ok(const moe_shape* s) {
   if (s->k < 1 || s->k > s->E || s->k > 32) return false;
   if (s->d < 64 || s->d % 64 != 0 || s->d > 65536) return false;
   if (s->n < 64 || s->n % 64 != 0 || s->n > 65536) return false;
-  if (s->round != MOE_ROUND_OFF && s->round != MOE_ROUND_NEAREST && s->round != MOE_ROUND_UP) return false;
+  if (s->round < MOE_ROUND_OFF || s->round > MOE_ROUND_STOCHASTIC) return false;
   if (s->round != MOE_ROUND_OFF && s->tile != 64 && s->tile != 128 && s->tile != 256) return false;
   // row indices and element offsets stay in range of the int32 / int64 math
   const int64_t A = static_cast<int64_t>(s->T) * s->k;
@@ -192,7 +192,8 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
   if (st != MOE_OK) return st;
   int64_t off[kNumSlots];
   layout(s, off);
-  launch_token_round(logits, topk_idx, s->T, s->E, s->k, s->tile, s->round, counts, offsets, row_token, row_w,
+  launch_token_round(logits, topk_idx, s->T, s->E, s->k, s->tile, s->round, s->seed, counts, offsets, row_token,
+                     row_w,
                      tok_offsets, tok_rows, at<void>(ws, off[kRoundScratch]), status_of(ws), as_stream(stream));
   return last_launch();
 }

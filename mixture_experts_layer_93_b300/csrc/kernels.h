@@ -28,7 +28,7 @@ void launch_permute_list(const int32_t* expert_of, const float* w, const int32_t
 // round.cu
 size_t round_scratch_bytes(int T, int E, int k, int tile);
 void launch_token_round(const float* logits, const int32_t* idx, int T, int E, int k, int tile, int mode,
-                        int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
+                        uint32_t seed, int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
                         int32_t* tok_rows, void* scratch, int32_t* status, cudaStream_t stream);
 
 // gemm.cu

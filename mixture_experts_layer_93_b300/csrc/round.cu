@@ -4,8 +4,9 @@
 //
 // Reading of the page (its three statements cannot all hold for "always
 // round up"): the count c of expert e becomes c' = the nearest multiple of
-// the tile, half up (mode NEAREST; or the next multiple up, mode UP), capped at
-// tile*floor(T/tile).  If c' > c the c'-c tokens not routed to e with the
+// the tile, half up (mode NEAREST; the next multiple up, mode UP; or, mode
+// STOCHASTIC, up with probability (c mod tile)/tile so that the expected
+// count is exactly c), capped at tile*floor(T/tile).  If c' > c the c'-c tokens not routed to e with the
 // highest logit L[t,e] join e (ties: lower t first); if c' < c the c-c' routed
 // tokens with the lowest logits leave (ties: higher t leaves first).  Each
 // expert is rounded from the original top-k sets.  A token's final set is
@@ -82,6 +83,16 @@ int64_t scratch_size(int T, int E, int64_t cap) {
          (T > kSmemKeyLimit ? align256(int64_t(E) * T * 4) : 0);
 }
 
+// SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom number
+// generators", OOPSLA 2014): add the golden-ratio increment to the state, then
+// two xor-shift-multiply rounds and a final xor-shift.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t state) {
+  uint64_t z = state + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 // Total order key of a logit: larger float -> larger key; -0.0 and +0.0 equal.
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f == 0.0f) return 0x80000000u;
@@ -129,7 +140,7 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
 // non-candidates are 0 (every real key is > 0).  Writes the final membership
 // row and the rounded count.
 __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const float* __restrict__ L, int T, int E,
-                                                                      int64_t W, int tile, int mode,
+                                                                      int64_t W, int tile, int mode, uint32_t seed,
                                                                       const uint32_t* __restrict__ member,
                                                                       uint32_t* __restrict__ final_set,
                                                                       int32_t* __restrict__ new_counts,
@@ -148,10 +159,17 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
   for (int64_t w = threadIdx.x; w < W; w += kSelectThreads) c += __popc(mrow[w]);
   c = block_sum(c, red);
   int c2;
-  if (mode == MOE_ROUND_NEAREST)
+  if (mode == MOE_ROUND_NEAREST) {
     c2 = tile * ((c + tile / 2) / tile);
-  else
+  } else if (mode == MOE_ROUND_STOCHASTIC) {
+    // up with probability (c mod tile) / tile: exact integer comparison of the
+    // draw's top 32 bits against (c mod tile) * 2^32 / tile
+    const uint64_t h = splitmix64((static_cast<uint64_t>(seed) << 32) | static_cast<uint32_t>(e)) >> 32;
+    const bool up = h * static_cast<uint64_t>(tile) < (static_cast<uint64_t>(c % tile) << 32);
+    c2 = tile * (c / tile) + (up ? tile : 0);
+  } else {
     c2 = tile * ((c + tile - 1) / tile);
+  }
   c2 = min(c2, tile * (T / tile));
 
   // adding: choose m = c2 - c among non-members; dropping: keep m = c2 members
@@ -456,7 +474,7 @@ size_t round_scratch_bytes(int T, int E, int k, int tile) {
 }
 
 void launch_token_round(const float* logits, const int32_t* idx, int T, int E, int k, int tile, int mode,
-                        int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
+                        uint32_t seed, int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
                         int32_t* tok_rows, void* scratch, int32_t* status, cudaStream_t stream) {
   const int64_t cap = static_cast<int64_t>(T) * k + static_cast<int64_t>(E) * tile;
   const int64_t W = words_per_row(T);
@@ -468,7 +486,8 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
   const size_t key_smem = in_smem ? static_cast<size_t>(T) * 4 : 0;
   cudaFuncSetAttribute(round_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(kSmemKeyLimit) * 4);
-  round_select_kernel<<<E, kSelectThreads, key_smem, stream>>>(logits, T, E, W, tile, mode, s.member, s.final_set,
+  round_select_kernel<<<E, kSelectThreads, key_smem, stream>>>(logits, T, E, W, tile, mode, seed, s.member,
+                                                              s.final_set,
                                                               s.new_counts, s.keys, in_smem);
   const int EW = (E + 31) / 32;
   const int64_t tblocks = static_cast<int64_t>(EW) * W;  // warps

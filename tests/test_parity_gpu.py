@@ -282,8 +282,8 @@ def test_forward_full_size_sampled(cuda_device, name):
 
 
 # ----------------------------------------------------------- token rounding
-def _expected_rounding(L, idx, tile, mode):
-    r = O.token_round(L, idx, tile, mode)
+def _expected_rounding(L, idx, tile, mode, seed=0):
+    r = O.token_round(L, idx, tile, mode, seed=seed)
     T, E = L.shape
     counts = r["counts"]
     offsets = np.concatenate([[0], np.cumsum(counts)])
@@ -310,18 +310,22 @@ def _expected_rounding(L, idx, tile, mode):
 @pytest.mark.parametrize("T,E,k,tile,mode,zipf", [(1000, 16, 2, 64, "nearest", 0.0), (777, 8, 2, 128, "nearest", 0.0),
                                                  (4099, 64, 4, 128, "nearest", 1.1), (100, 4, 1, 128, "nearest", 0.0),
                                                  (300, 32, 8, 64, "up", 0.0), (2000, 128, 8, 128, "up", 1.1),
-                                                 (513, 5, 5, 256, "nearest", 0.0)])
+                                                 (513, 5, 5, 256, "nearest", 0.0), (3000, 64, 4, 128, "stochastic", 1.1),
+                                                 (900, 16, 2, 64, "stochastic", 0.0)])
 def test_token_round_bit_exact(cuda_device, T, E, k, tile, mode, zipf):
+    seed = 1234 + T
     L = I.make_logits(T, E, seed=T + E + tile, ties=True)
     if zipf:
         L = L - zipf * torch.log(torch.arange(1, E + 1, dtype=torch.float32))[None, :]
         L = (torch.round(L * 4) / 4).contiguous()
     Lnp = L.numpy()
     idx = torch.from_numpy(O.topk(Lnp, k))
-    s, ws = ws_for(T, 64, 64, E, k, cuda_device, tile=tile, round=mode)
+    s = B.make_shape(T, 64, 64, E, k, tile, mode, seed)
+    ws = B.Workspace(s, cuda_device)
     out = B.moe_token_round(s, L.to(cuda_device), idx.to(cuda_device), ws)
     assert B.moe_check_device_status(ws) == B.MOE_OK
-    counts, offsets, row_token, tok_offsets, tok_rows, row_w = _expected_rounding(Lnp, idx.numpy(), tile, mode)
+    counts, offsets, row_token, tok_offsets, tok_rows, row_w = _expected_rounding(Lnp, idx.numpy(), tile, mode,
+                                                                                  seed)
     R = int(offsets[-1])
     assert np.array_equal(out["counts"].cpu().numpy(), counts)
     assert np.all(counts % tile == 0)
@@ -345,26 +349,56 @@ def _gpu_sets(ws, shape, T):
 
 
 @pytest.mark.parametrize("T,d,n,E,k,tile,mode", [(256, 128, 64, 8, 2, 64, "nearest"), (1500, 256, 128, 16, 4, 128, "nearest"),
-                                                 (700, 128, 192, 12, 3, 64, "up")])
+                                                 (700, 128, 192, 12, 3, 64, "up"),
+                                                 (1200, 256, 128, 16, 4, 64, "stochastic")])
 def test_forward_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="zipf", bias_scale=1.1)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T)
-    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile, round=mode)
+    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile, round=mode, seed=77)
     y = layer.forward(inp["x"])
     ws = layer.workspace(T, cuda_device)
     assert B.moe_check_device_status(ws) == B.MOE_OK
     gsets = _gpu_sets(ws, layer.shape(T), T)
     counts = ws.view("counts", torch.int32, E).cpu().numpy()
     assert np.all(counts % tile == 0)
-    toks, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], k, tile=tile, mode=mode)
+    toks, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], k, tile=tile, mode=mode, seed=77)
     same = np.array([np.array_equal(a, b) for a, b in zip(gsets, osets)])
     # fp32 logits on the GPU vs fp64 ones in the oracle can flip a selection
     # only at a near-tie between two tokens' logits
     assert same.mean() > 0.97, same.mean()
     keep = np.flatnonzero(same)
     y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile,
-                          mode=mode, tokens=keep)
+                          mode=mode, tokens=keep, seed=77)
     assert_moe_close(y[torch.from_numpy(keep).to(cuda_device)], y_ref)
     empty = [t for t in keep if len(osets[t]) == 0]
     if empty:
         assert torch.all(y[torch.tensor(empty, device=cuda_device)] == 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["nearest", "stochastic"])
+def test_forward_full_size_skew_rounding(cuda_device, mode):
+    """The skewed-load layer at full size with tile-128 token rounding: every
+    rounded count is a tile multiple, the GPU's final expert sets match the
+    oracle's on sampled tokens (except near-ties of fp32 vs fp64 logits), and
+    those tokens' outputs meet the tolerance."""
+    cfg = I.get_config("skew")
+    inp = I.make_inputs(cfg, device=cuda_device, seed=0)
+    layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k, tile=128, round=mode,
+                       seed=5)
+    y = layer.forward(inp["x"])
+    ws = layer.workspace(cfg.T, cuda_device)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    counts = ws.view("counts", torch.int32, cfg.E).cpu().numpy()
+    assert np.all(counts % 128 == 0)
+    toks = _sample_tokens(cfg.T, 32, 3)
+    gsets = _gpu_sets(ws, layer.shape(cfg.T), cfg.T)
+    _, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], cfg.k, tile=128, mode=mode, tokens=toks, seed=5)
+    same = np.array([np.array_equal(gsets[t], s) for t, s in zip(toks, osets)])
+    assert same.mean() >= 0.9, same.mean()
+    keep = toks[same]
+    y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k, tile=128,
+                          mode=mode, tokens=keep, seed=5)
+    assert_moe_close(y[torch.from_numpy(keep).to(cuda_device)], y_ref)
+    del layer, inp
+    torch.cuda.empty_cache()
