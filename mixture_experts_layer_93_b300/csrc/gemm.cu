@@ -67,9 +67,12 @@ struct GemmParams {
 
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = 4;
-constexpr int kEpiWarp0 = 5;
+constexpr int kEpiWarp0 = 5;   // epilogue warps 5..8 (and 10..13 with eight)
 constexpr int kRelayWarp = 9;  // gather 2: publishes landed rows to the MMA warp
-constexpr int kGemmThreads = 10 * 32;
+// Epilogue width: four warps (one per TMEM lane quadrant), or eight (two per
+// quadrant, each taking half the columns) for short-K tiles whose epilogue is
+// on the critical path; eight cost one operand stage of shared memory.
+__host__ __device__ constexpr int gemm_threads(int epi_warps) { return (epi_warps == 8 ? 14 : 10) * 32; }
 
 __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (n <= 64 ? 64 : (n <= 128 ? 128 : (n <= 256 ? 256 : 512))); }
 
@@ -79,20 +82,23 @@ __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (
 // operands; D rows 128r.. land in CTA r's TMEM.  Each SM thus stores and feeds
 // half of B: per k-block 32 KB of shared-memory writes and reads instead of
 // 48 KB, which is what keeps a 1-CTA M=128 x N=256 MMA from full rate.
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int EPI>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows held per CTA
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE_BYTES) > 8 ? 8 : (196608 / STAGE_BYTES);
+  // operand ring: what is left of 227 KB after the staging boxes, barriers,
+  // prefix table and token table (at most 8 stages)
+  static constexpr int RING_BUDGET = 232448 - 1024 - EPI * 2 * 32 * 64 - (3 * 8 + 4) * 8 - 16 - 1025 * 4 - BM * 4;
+  static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : (RING_BUDGET / STAGE_BYTES);
   static constexpr int TMEM_COLS = tmem_cols_for(2 * BN);
   static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
   static constexpr int PREFIX_BYTES = 1025 * 4;
   static constexpr int TOK_BYTES = BM * 4;
   // epilogue staging for TMA stores: per epilogue warp two 32 x 64-byte boxes
-  static constexpr int STAGE_OUT_BYTES = 4 * 2 * 32 * 64;
+  static constexpr int STAGE_OUT_BYTES = EPI * 2 * 32 * 64;
   static constexpr int SMEM_BYTES =
       1024 + STAGES * STAGE_BYTES + STAGE_OUT_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES;
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
@@ -143,11 +149,11 @@ __device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_
   }
 }
 
-template <int BN, int MODE, bool PAIR>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <int BN, int MODE, bool PAIR, int EPI>
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using C = GemmCfg<BN, PAIR>;
+  using C = GemmCfg<BN, PAIR, EPI>;
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull_bar[a]), 1);
-      mbar_init(smem_u32(&tempty_bar[a]), 4 * kPer);
+      mbar_init(smem_u32(&tempty_bar[a]), EPI * kPer);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -205,7 +211,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     tc_fence_before();
   } else if (warp == kEpiWarp0) {
-    // prefix[e] = number of tile units of groups < e
+    // prefix[e] = number of tile units of groups < e (this warp is free before the pipeline starts)
     if (p.single_rows > 0) {
       if (lane == 0) {
         prefix[0] = 0;
@@ -403,12 +409,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp & 3;  // TMEM lanes 32*ew .. 32*ew+31
+    const int epi = warp < kRelayWarp ? warp - kEpiWarp0 : warp - kEpiWarp0 - 1;  // 0..EPI-1
+    constexpr int NCH = EPI / 4;  // column slices per TMEM lane quadrant
+    const int ch = epi / 4;       // this warp's slice
     const int r_in_tile = ew * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     // 32 rows x 32 columns of 16-bit outputs per chunk go through one of this
     // warp's two staging boxes (64-byte rows, 64-byte swizzle) to a TMA store
-    uint8_t* stage_out = sOut + ew * (2 * 32 * 64);
+    uint8_t* stage_out = sOut + epi * (2 * 32 * 64);
     int out_buf = 0;
     auto store_chunk = [&](const uint32_t (&o)[16], int col, int64_t row_w0, int warp_rows, int64_t row,
                            auto* dst_row) {
@@ -454,10 +463,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int warp_rows = max(0, min(32, rows_valid - ew * 32));
       const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
       if constexpr (MODE == kModeUp) {
+        // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile
         constexpr int H = BN / 2;
         __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
 #pragma unroll 1
-        for (int c = 0; c < H; c += 32) {
+        for (int c = ch * (H / NCH); c < (ch + 1) * (H / NCH); c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(taddr + c, g);
           tmem_ld32(taddr + H + c, u);
@@ -476,29 +486,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else if constexpr (MODE == kModeDown) {
         // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
         // same traffic); values past the fp16 range saturate and are reported
+        // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait
         const float wr = valid ? p.row_w[row] : 0.f;
         __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
         bool overflow = false;
+        constexpr int STEP = (BN / NCH) >= 64 ? 64 : 32;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(taddr + c, v);
+        for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
+          uint32_t v[2][32];
+          tmem_ld32(taddr + c0, v[0]);
+          if (STEP == 64) tmem_ld32(taddr + c0 + 32, v[1]);
           tc_wait_ld();
-          uint32_t o[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float a = wr * __uint_as_float(v[2 * q]), b = wr * __uint_as_float(v[2 * q + 1]);
-            overflow |= !(fabsf(a) <= kHalfMax) || !(fabsf(b) <= kHalfMax);
-            a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
-            b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
-            o[q] = pack_half2(a, b);
+          for (int half = 0; half < STEP / 32; ++half) {
+            uint32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              float a = wr * __uint_as_float(v[half][2 * q]), b = wr * __uint_as_float(v[half][2 * q + 1]);
+              overflow |= !(fabsf(a) <= kHalfMax) || !(fabsf(b) <= kHalfMax);
+              a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
+              b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
+              o[q] = pack_half2(a, b);
+            }
+            const int c = c0 + 32 * half;
+            if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
           }
-          if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
         }
         if (overflow && valid) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
-      } else {
-        // router: the three column groups hold x*hi, x*mid, x*lo of the same
-        // EB experts; their fp32 sum plus the bias is the logit
+      } else if (ch == 0) {
+        // router (first four epilogue warps only): the three column groups
+        // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum plus
+        // the bias is the logit
         constexpr int EB = BN / 3;
         const int e0 = nb * EB;
         float* dst = p.out_f32 + row * p.out_ld;
@@ -559,6 +577,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ----------------------------------------------------------------- host
+template <int BN, int MODE, bool PAIR, int EPI>
+static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const GemmParams& p, cudaStream_t stream);
+
+// Eight epilogue warps when the K loop is short enough for the epilogue to be
+// on the critical path (measured: 7B-style layer +9 %, long-K layers -2..-3 %
+// with eight).
+template <int BN, int MODE, bool PAIR>
+static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
+                       cudaStream_t stream) {
+  const bool wide = (MODE == kModeUp && p.num_kb <= 24) || (MODE == kModeDown && p.num_kb <= 8);
+  if (MODE != kModeRouter && wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+  return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -607,11 +640,12 @@ int num_sms() {
   return sms > 0 ? sms : 1;
 }
 
-template <int BN, int MODE, bool PAIR>
-static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
-                       cudaStream_t stream) {
-  using C = GemmCfg<BN, PAIR>;
-  auto kern = moe_gemm_kernel<BN, MODE, PAIR>;
+template <int BN, int MODE, bool PAIR, int EPI>
+static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                           const GemmParams& p, cudaStream_t stream) {
+  using C = GemmCfg<BN, PAIR, EPI>;
+  auto kern = moe_gemm_kernel<BN, MODE, PAIR, EPI>;
+  constexpr int kGemmThreads = gemm_threads(EPI);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!PAIR) {
