@@ -288,8 +288,8 @@ def run_ours(args, world, rank, local):
             c_off, c_rows = tok_offsets, tok_rows
         if ev:
             ev[2].record(stream)
-        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(h), args.gather, ws.ptr,
-                              ws.nbytes, st), "up")
+        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(c_off), P(c_rows), P(h),
+                              args.gather, ws.ptr, ws.nbytes, st), "up")
         if ev:
             ev[3].record(stream)
         check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,

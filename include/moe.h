@@ -205,13 +205,18 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
  *   x [T, d] bf16; W13p from moe_prepare_weights; h [moe_row_capacity, n] bf16.
  * gather selects how token rows reach shared memory:
  *   0 = a gather kernel copies the rows into the workspace (ys region), then
- *       tiled TMA loads them;
+ *       tiled TMA loads them.  With tok_rows (token -> its rows, same
+ *       convention as moe_combine: tok_rows[tok_offsets[t] ..), or
+ *       tok_rows[t*k .. t*k+k) when tok_offsets is NULL, i.e. moe_permute's
+ *       dst) the copy runs in token order and reads each x row once; with
+ *       tok_rows NULL it runs in row order from row_token;
  *   1 = TMA tile::gather4 (four token rows per copy) straight from x;
  *   2 = per-lane 16-byte cp.async straight from x into the swizzled tile.
  * Any other value returns MOE_ERR_INVALID. */
 int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int32_t* counts,
-                  const int32_t* offsets, const int32_t* row_token, void* h, int gather,
-                  void* ws, size_t ws_bytes, void* stream);
+                  const int32_t* offsets, const int32_t* row_token, const int32_t* tok_offsets,
+                  const int32_t* tok_rows, void* h, int gather, void* ws, size_t ws_bytes,
+                  void* stream);
 
 /* Down-projection grouped GEMM with the gate weight in the epilogue:
  *   ys[r, :] = fp16( row_w[r] * (h[r] W2_e) ) for rows of expert e.

@@ -65,7 +65,7 @@ _SIGNATURES = {
     "moe_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
+    "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_SHP, _P, _P, _P, _P, _P]),
     "moe_forward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -263,14 +263,14 @@ def moe_token_round(shape: moe_shape, logits, topk_idx, ws: Workspace) -> dict:
 
 
 def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Workspace, gather: int = 2,
-                  h=None):
-    _need_cuda(x, W13p, counts, offsets, row_token)
+                  h=None, tok_offsets=None, tok_rows=None):
+    _need_cuda(x, W13p, counts, offsets, row_token, tok_offsets, tok_rows)
     cap = moe_row_capacity(shape)
     if h is None:
         h = torch.empty(cap, shape.n, dtype=torch.bfloat16, device=x.device)
     _check(lib().moe_expert_up(ctypes.byref(shape), _ptr(x), _ptr(W13p), _ptr(counts), _ptr(offsets),
-                               _ptr(row_token), _ptr(h), int(gather), ws.ptr, ws.nbytes,
-                               _stream(x.device)), "moe_expert_up")
+                               _ptr(row_token), _ptr(tok_offsets), _ptr(tok_rows), _ptr(h), int(gather), ws.ptr,
+                               ws.nbytes, _stream(x.device)), "moe_expert_up")
     return h
 
 

@@ -199,7 +199,8 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
 }
 
 int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int32_t* counts, const int32_t* offsets,
-                  const int32_t* row_token, void* h, int gather, void* ws, size_t ws_bytes, void* stream) {
+                  const int32_t* row_token, const int32_t* tok_offsets, const int32_t* tok_rows, void* h, int gather,
+                  void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !x || !W13p || !counts || !offsets || !row_token || !h) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(W13p) || !aligned16(h)) return MOE_ERR_INVALID;
   if (gather < 0 || gather > 2) return MOE_ERR_INVALID;
@@ -210,9 +211,9 @@ int moe_expert_up(const moe_shape* s, const void* x, const void* W13p, const int
   // the non-gather variant stages the gathered rows in the ys region, which
   // the forward only writes after the up-projection
   return launch_expert_up(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(W13p), counts,
-                          offsets, row_token, static_cast<__nv_bfloat16*>(h), s->T, s->d, s->n, s->E, row_cap(s),
-                          gather, at<__nv_bfloat16>(ws, off[kYs]), status_of(ws), kDefaultTimeoutNs,
-                          as_stream(stream));
+                          offsets, row_token, tok_rows, tok_offsets, static_cast<__nv_bfloat16*>(h), s->T, s->d, s->n,
+                          s->E, s->k, row_cap(s), gather, at<__nv_bfloat16>(ws, off[kYs]), status_of(ws),
+                          kDefaultTimeoutNs, as_stream(stream));
 }
 
 int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const int32_t* counts,
@@ -270,7 +271,8 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
     combine_offsets = tok_offsets;
     combine_rows = tok_rows;
   }
-  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, h, kForwardGather, ws, ws_bytes, stream)) != MOE_OK)
+  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, combine_offsets, combine_rows, h, kForwardGather, ws,
+                          ws_bytes, stream)) != MOE_OK)
     return st;
   if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);

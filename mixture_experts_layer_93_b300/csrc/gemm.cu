@@ -692,6 +692,45 @@ void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const 
   gather_rows_kernel<<<num_sms() * 8, 256, 0, stream>>>(x, row_token, offsets, E, d, out, rows_cap);
 }
 
+// The same copy in token order: one warp per token reads x[t] once, 4 KB at
+// a time into registers, and writes it to each of the token's rows
+// (tok_rows[tok_offsets[t] ..), or tok_rows[t*k ..) without offsets).  Every x
+// row leaves HBM once instead of once per row it feeds.
+__global__ void __launch_bounds__(256) gather_rows_by_token_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                   const int32_t* __restrict__ tok_rows,
+                                                                   const int32_t* __restrict__ tok_offsets, int T,
+                                                                   int k, int d, __nv_bfloat16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  const int r0 = tok_offsets ? tok_offsets[t] : t * k;
+  const int r1 = tok_offsets ? tok_offsets[t + 1] : r0 + k;
+  if (r0 == r1) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t) * d);
+  const int groups = d / 8;  // 16-byte groups per row
+  for (int g0 = 0; g0 < groups; g0 += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = g0 + i * 32 + lane;
+      if (g < groups) v[i] = __ldg(src + g);
+    }
+    for (int j = r0; j < r1; ++j) {
+      uint4* dst = reinterpret_cast<uint4*>(out + static_cast<int64_t>(tok_rows[j]) * d);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = g0 + i * 32 + lane;
+        if (g < groups) dst[g] = v[i];
+      }
+    }
+  }
+}
+
+void launch_gather_rows_by_token(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T,
+                                 int k, int d, __nv_bfloat16* out, cudaStream_t stream) {
+  gather_rows_by_token_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, tok_rows, tok_offsets, T, k, d, out);
+}
+
 // How SM-pair GEMMs treat an expert's odd last 128-row block.  Run as a
 // half-empty pair inside the main kernel, it costs one pair tile of MMA time
 // but reuses the expert's weights from L2; run by a separate single-SM launch,
@@ -709,7 +748,8 @@ static GemmParams base_params(int32_t* status, uint64_t timeout_ns) {
 }
 
 int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
-                     const int32_t* offsets, const int32_t* row_token, __nv_bfloat16* h, int T, int d, int n, int E,
+                     const int32_t* offsets, const int32_t* row_token, const int32_t* tok_rows,
+                     const int32_t* tok_offsets, __nv_bfloat16* h, int T, int d, int n, int E, int k,
                      int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
                      uint64_t timeout_ns, cudaStream_t stream) {
   const int H = up_half_block(n);
@@ -720,7 +760,10 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   } else if (gather == 2) {
     if (!make_map_bf16(&tmA, x, d, T, 128)) return MOE_ERR_CUDA;  // not read by the kernel
   } else {
-    launch_gather_rows(x, row_token, offsets, E, d, xperm_scratch, rows_cap, stream);
+    if (tok_rows)
+      launch_gather_rows_by_token(x, tok_rows, tok_offsets, T, k, d, xperm_scratch, stream);
+    else
+      launch_gather_rows(x, row_token, offsets, E, d, xperm_scratch, rows_cap, stream);
     if (!make_map_bf16(&tmA, xperm_scratch, d, rows_cap, 128)) return MOE_ERR_CUDA;
   }
   const bool pair = (gather == 0 || gather == 2) && BN == 256;

@@ -33,7 +33,8 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
 
 // gemm.cu
 int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
-                     const int32_t* offsets, const int32_t* row_token, __nv_bfloat16* h, int T, int d, int n, int E,
+                     const int32_t* offsets, const int32_t* row_token, const int32_t* tok_rows,
+                     const int32_t* tok_offsets, __nv_bfloat16* h, int T, int d, int n, int E, int k,
                      int64_t rows_cap, int gather, __nv_bfloat16* xperm_scratch, int32_t* status,
                      uint64_t timeout_ns, cudaStream_t stream);
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,

@@ -94,18 +94,27 @@ def _synthetic_routing(T, E, k, seed, skew=0.0):
 
 
 # ------------------------------------------------------------ up-projection
-@pytest.mark.parametrize("gather", [0, 1, 2])
+@pytest.mark.parametrize("gather", [0, 1, 2, "0-token", "0-offsets"])
 @pytest.mark.parametrize("T,d,n,E,k,skew", [(700, 256, 192, 6, 2, 0.0), (600, 384, 256, 5, 3, 1.0),
                                             (300, 128, 64, 8, 2, 0.0), (1100, 512, 128, 3, 1, 0.5)])
 def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
+    """gather "0-token" copies rows in token order from dst; "0-offsets" the
+    same through explicit per-token offsets (k rows each)."""
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T + d + n)
     idx, counts, offsets, src, dst = _synthetic_routing(T, E, k, seed=T + 1, skew=skew)
     s, ws = ws_for(T, d, n, E, k, cuda_device)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     row_token = torch.from_numpy((src // k).astype(np.int32)).to(cuda_device)
+    tok_offsets = tok_rows = None
+    if isinstance(gather, str):
+        tok_rows = torch.from_numpy(dst.astype(np.int32)).to(cuda_device)
+        if gather == "0-offsets":
+            tok_offsets = torch.arange(0, T * k + 1, k, dtype=torch.int32, device=cuda_device)
+        gather = 0
     h = B.moe_expert_up(s, inp["x"], W13p, torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
-                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=gather)
+                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=gather,
+                        tok_offsets=tok_offsets, tok_rows=tok_rows)
     assert B.moe_check_device_status(ws) == B.MOE_OK
     A = T * k
     h_gpu = to64(h[:A])
