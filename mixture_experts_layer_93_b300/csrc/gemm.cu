@@ -91,18 +91,22 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // operand ring: what is left of 227 KB after the staging boxes, barriers,
   // prefix table and token table (at most 8 stages)
-  static constexpr int RING_BUDGET = 232448 - 1024 - EPI * 2 * 32 * 64 - (3 * 8 + 4) * 8 - 16 - 1025 * 4 - BM * 4;
+  static constexpr int RING_BUDGET =
+      232448 - 1024 - EPI * 2 * 32 * 64 - (3 * 8 + 4) * 8 - 16 - 1025 * 4 - BM * 4 - 4 - 1024 * 8;
   static constexpr int STAGES = (RING_BUDGET / STAGE_BYTES) > 8 ? 8 : (RING_BUDGET / STAGE_BYTES);
   static constexpr int TMEM_COLS = tmem_cols_for(2 * BN);
   static constexpr int BAR_BYTES = (3 * STAGES + 4) * 8 + 16;
   static constexpr int PREFIX_BYTES = 1025 * 4;
   static constexpr int TOK_BYTES = BM * 4;
+  static constexpr int GRP_BYTES = 4 + 1024 * 8;  // alignment pad + (first row, rows) of each group
   // epilogue staging for TMA stores: per epilogue warp two 32 x 64-byte boxes
   static constexpr int STAGE_OUT_BYTES = EPI * 2 * 32 * 64;
   static constexpr int SMEM_BYTES =
-      1024 + STAGES * STAGE_BYTES + STAGE_OUT_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES;
+      1024 + STAGES * STAGE_BYTES + STAGE_OUT_BYTES + BAR_BYTES + PREFIX_BYTES + TOK_BYTES + GRP_BYTES;
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(BAR_BYTES % 8 == 0 && STAGE_OUT_BYTES % 8 == 0 && (PREFIX_BYTES + TOK_BYTES + 4) % 8 == 0,
+                "group table alignment");
 };
 
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
@@ -139,13 +143,17 @@ __device__ __forceinline__ int unit_block(int units, int mu, int rank, int gcoun
   return mu;
 }
 
-__device__ __forceinline__ void group_rows(const GemmParams& p, int e, int& row_start, int& count) {
+// First row and row count of group e; grp_s holds (offsets[e], counts[e]),
+// copied to shared memory once per CTA.
+__device__ __forceinline__ void group_rows(const GemmParams& p, const int2* grp_s, int e, int& row_start,
+                                           int& count) {
   if (p.single_rows > 0) {
     row_start = 0;
     count = p.single_rows;
   } else {
-    row_start = p.offsets[e];
-    count = p.counts[e];
+    const int2 g = grp_s[e];
+    row_start = g.x;
+    count = g.y;
   }
 }
 
@@ -170,6 +178,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int32_t* prefix = reinterpret_cast<int32_t*>(sOut + C::STAGE_OUT_BYTES + C::BAR_BYTES);
   int32_t* tok_s = prefix + 1025;  // gather 2: token of each row of the current tile
+  // prefix starts 8-byte aligned; one int of padding after tok_s aligns grp_s
+  int2* grp_s = reinterpret_cast<int2*>(tok_s + C::BM + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_groups = p.single_rows > 0 ? 1 : p.E;
@@ -223,7 +233,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       for (int b = 0; b < p.E; b += 32) {
         const int e = b + lane;
         int m = 0;
-        if (e < p.E) m = tile_units(p.units, (p.counts[e] + C::BM - 1) / C::BM);
+        if (e < p.E) {
+          const int c = p.counts[e];
+          grp_s[e] = make_int2(p.offsets[e], c);
+          m = tile_units(p.units, (c + C::BM - 1) / C::BM);
+        }
         int incl = m;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
         int e, nb, mu, gstart, gcount;
         decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
-        group_rows(p, e, gstart, gcount);
+        group_rows(p, grp_s, e, gstart, gcount);
         const int mb = unit_block(p.units, mu, rank, gcount);
         const int row0 = gstart + mb * C::BM;
         const int rows_valid = min(C::BM, gcount - mb * C::BM);
@@ -444,13 +458,26 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       }
       (void)row;
     };
+    // down: the gate weight of this thread's row is loaded one tile ahead,
+    // so its latency hides behind the previous tile's epilogue
+    auto load_row_w = [&](int t) -> float {
+      int e, nb, mu, gstart, gcount;
+      decode_tile(t, prefix, n_groups, p.n_blocks, e, nb, mu);
+      group_rows(p, grp_s, e, gstart, gcount);
+      const int mb = unit_block(p.units, mu, rank, gcount);
+      return r_in_tile < min(C::BM, gcount - mb * C::BM) ? p.row_w[gstart + mb * C::BM + r_in_tile] : 0.f;
+    };
+    float wr_next = 0.f;
+    if (MODE == kModeDown && unit0 < total_tiles) wr_next = load_row_w(unit0);
     for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
       int e, nb, mu, gstart, gcount;
       decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
-      group_rows(p, e, gstart, gcount);
+      group_rows(p, grp_s, e, gstart, gcount);
       const int mb = unit_block(p.units, mu, rank, gcount);
       const int row0 = gstart + mb * C::BM;
       const int rows_valid = min(C::BM, gcount - mb * C::BM);
+      const float wr = wr_next;
+      if (MODE == kModeDown && tau + unit_stride < total_tiles) wr_next = load_row_w(tau + unit_stride);
       int w = 1;
       if (lane == 0)
         w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
@@ -477,8 +504,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           for (int q = 0; q < 16; ++q) {
             const float g0 = __uint_as_float(g[2 * q]), g1 = __uint_as_float(g[2 * q + 1]);
             const float u0 = __uint_as_float(u[2 * q]), u1 = __uint_as_float(u[2 * q + 1]);
-            const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-            const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             o[q] = pack_bf16x2(h0, h1);
           }
           if (warp_rows > 0) store_chunk(o, nb * H + c, row_w0, warp_rows, row, dst + c);
@@ -486,10 +513,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       } else if constexpr (MODE == kModeDown) {
         // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
         // same traffic); values past the fp16 range saturate and are reported
-        // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait
-        const float wr = valid ? p.row_w[row] : 0.f;
+        // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait.
+        // amax = max |acc| over the row (NaN if any is NaN): since rounding is
+        // monotonic, some |w * acc| exceeds the fp16 range iff |w| * amax does.
         __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
-        bool overflow = false;
+        float amax = 0.f;
         constexpr int STEP = (BN / NCH) >= 64 ? 64 : 32;
 #pragma unroll 1
         for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
@@ -502,17 +530,15 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
             uint32_t o[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              float a = wr * __uint_as_float(v[half][2 * q]), b = wr * __uint_as_float(v[half][2 * q + 1]);
-              overflow |= !(fabsf(a) <= kHalfMax) || !(fabsf(b) <= kHalfMax);
-              a = fminf(fmaxf(a, -kHalfMax), kHalfMax);
-              b = fminf(fmaxf(b, -kHalfMax), kHalfMax);
-              o[q] = pack_half2(a, b);
+              const float a = __uint_as_float(v[half][2 * q]), b = __uint_as_float(v[half][2 * q + 1]);
+              amax = fmax_nan(amax, fmax_nan(fabsf(a), fabsf(b)));
+              o[q] = pack_half2_satfinite(wr * a, wr * b);
             }
             const int c = c0 + 32 * half;
             if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
           }
         }
-        if (overflow && valid) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
+        if (valid && !(fabsf(wr) * amax <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
       } else if (ch == 0) {
         // router (first four epilogue warps only): the three column groups
         // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum plus

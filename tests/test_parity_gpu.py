@@ -161,6 +161,50 @@ def test_expert_down_gate_weight(cuda_device, T, d, n, E, k):
     assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-5 * rms), err_stats(got, ref)
 
 
+def test_expert_down_fp16_saturation(cuda_device):
+    """Rows whose w * (h W2) leaves the fp16 range are stored as +-65504 and
+    reported (MOE_ERR_DEVICE_CHECK, detail 16); the other rows are unaffected."""
+    T, d, n, E, k = 300, 256, 128, 4, 2
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=5)
+    idx, counts, offsets, src, dst = _synthetic_routing(T, E, k, seed=3)
+    A = T * k
+    g = torch.Generator(device="cpu").manual_seed(4)
+    h = torch.randn(A, n, generator=g).to(torch.bfloat16).to(cuda_device)
+    row_w = torch.rand(A, generator=g) * 0.5 + 0.5
+    big = torch.zeros(A, dtype=torch.bool)
+    big[::37] = True                       # these rows overflow: |acc| ~ 1 times 1e6
+    row_w[big] *= 1e6
+    row_w = row_w.to(cuda_device)
+    s, ws = ws_for(T, d, n, E, k, cuda_device)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    cap = B.moe_row_capacity(s)
+    hcap = torch.zeros(cap, n, dtype=torch.bfloat16, device=cuda_device)
+    hcap[:A] = h
+    wcap = torch.zeros(cap, device=cuda_device)
+    wcap[:A] = row_w
+    B.moe_clear_device_status(ws)
+    ys = B.moe_expert_down(s, hcap, W2p, torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
+                           torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap, ws)
+    with pytest.raises(B.MoEError) as info:
+        B.moe_check_device_status(ws)
+    assert info.value.status == B.MOE_ERR_DEVICE_CHECK and info.value.detail == 16
+    ref = np.zeros((A, d))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = to64(row_w[r0:r1])[:, None] * O.expert_out(h[r0:r1], inp["W2"][e])
+    got = to64(ys[:A])
+    over = np.abs(ref) > 65520.0           # rounds past the largest fp16 value
+    assert over.any() and big.numpy()[np.nonzero(over)[0]].all()
+    assert np.array_equal(got[over], np.sign(ref[over]) * 65504.0)
+    inside = np.abs(ref) < 65000.0
+    # fp32 accumulation error scales with the row's gate weight: floor per row
+    row_rms = np.broadcast_to(np.sqrt(np.mean(ref ** 2, axis=1))[:, None], ref.shape)
+    assert np.all(np.abs(got[inside] - ref[inside]) <= 2.0 ** -11 * np.abs(ref[inside]) + 1e-5 * row_rms[inside])
+    B.moe_clear_device_status(ws)
+
+
 # ------------------------------------------------------------------ combine
 @pytest.mark.parametrize("T,d,k", [(256, 128, 2), (1001, 512, 8), (3, 4096, 1)])
 def test_combine_fixed_k(cuda_device, T, d, k):
