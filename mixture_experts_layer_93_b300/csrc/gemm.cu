@@ -109,17 +109,27 @@ struct GemmCfg {
                 "group table alignment");
 };
 
+// e: on entry the group of a tile at or before tau (each warp visits its tiles
+// in increasing order, starting from e = 0); on exit the group of tau.  A few
+// linear probes cover the usual step to the same or a nearby group, then a
+// binary search over the rest.  prefix[E] * n_blocks > tau bounds both.
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
                                             int& mb) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] * n_blocks <= tau)
-      lo = mid;
-    else
-      hi = mid - 1;
+  for (int probe = 0; prefix[e + 1] * n_blocks <= tau; ++probe) {
+    if (probe == 4) {
+      int lo = e + 1, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] * n_blocks <= tau)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      e = lo;
+      break;
+    }
+    ++e;
   }
-  e = lo;
   const int local = tau - prefix[e] * n_blocks;
   const int me = prefix[e + 1] - prefix[e];
   nb = local / me;
@@ -266,8 +276,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      int e = 0;  // group cursor of decode_tile
       for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
-        int e, nb, mu, gstart, gcount;
+        int nb, mu, gstart, gcount;
         decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, grp_s, e, gstart, gcount);
         const int mb = unit_block(p.units, mu, rank, gcount);
@@ -458,26 +469,26 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       }
       (void)row;
     };
-    // down: the gate weight of this thread's row is loaded one tile ahead,
-    // so its latency hides behind the previous tile's epilogue
-    auto load_row_w = [&](int t) -> float {
-      int e, nb, mu, gstart, gcount;
-      decode_tile(t, prefix, n_groups, p.n_blocks, e, nb, mu);
-      group_rows(p, grp_s, e, gstart, gcount);
+    // Tiles are decoded one ahead: the next tile's place (and, down, the
+    // gate weight of this thread's row in it) is fetched before this tile's
+    // accumulator is waited for, so the load latency hides behind this tile.
+    int dec_e = 0;  // group cursor of decode_tile
+    int nx_nb = 0, nx_row0 = 0, nx_rows = 0;
+    float nx_w = 0.f;
+    auto decode_next = [&](int t) {
+      int mu, gstart, gcount;
+      decode_tile(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
+      group_rows(p, grp_s, dec_e, gstart, gcount);
       const int mb = unit_block(p.units, mu, rank, gcount);
-      return r_in_tile < min(C::BM, gcount - mb * C::BM) ? p.row_w[gstart + mb * C::BM + r_in_tile] : 0.f;
+      nx_row0 = gstart + mb * C::BM;
+      nx_rows = min(C::BM, gcount - mb * C::BM);
+      if (MODE == kModeDown) nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] : 0.f;
     };
-    float wr_next = 0.f;
-    if (MODE == kModeDown && unit0 < total_tiles) wr_next = load_row_w(unit0);
+    if (unit0 < total_tiles) decode_next(unit0);
     for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
-      int e, nb, mu, gstart, gcount;
-      decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
-      group_rows(p, grp_s, e, gstart, gcount);
-      const int mb = unit_block(p.units, mu, rank, gcount);
-      const int row0 = gstart + mb * C::BM;
-      const int rows_valid = min(C::BM, gcount - mb * C::BM);
-      const float wr = wr_next;
-      if (MODE == kModeDown && tau + unit_stride < total_tiles) wr_next = load_row_w(tau + unit_stride);
+      const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows;
+      const float wr = nx_w;
+      if (tau + unit_stride < total_tiles) decode_next(tau + unit_stride);
       int w = 1;
       if (lane == 0)
         w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
@@ -569,8 +580,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
+        // the TMEM reads are complete (tcgen05.wait::ld) and nothing written
+        // here is read by the MMA thread: a relaxed arrival suffices
         if (PAIR)
-          mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's MMA waits on it
+          mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's MMA waits on it
         else
           mbar_arrive(smem_u32(&tempty_bar[acc]));
       }
