@@ -891,9 +891,11 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   const int EB = router_expert_block(E);
   const int BN = 3 * EB;
   const int nblk = (E + EB - 1) / EB;
+  // SM pairs: each CTA holds half of the 3*EB split-weight rows, so a k-block
+  // moves 28 KB per SM instead of 40 KB through shared memory
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, x, d, T, 128)) return MOE_ERR_CUDA;
-  if (!make_map_bf16(&tmB, Wr3, d, static_cast<uint64_t>(nblk) * BN, BN)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, Wr3, d, static_cast<uint64_t>(nblk) * BN, BN / 2)) return MOE_ERR_CUDA;
   const CUtensorMap& tmC = tmA;  // the router epilogue stores fp32 logits directly
   GemmParams p = base_params(status, timeout_ns);
   p.single_rows = T;
@@ -906,9 +908,10 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   p.n_blocks = nblk;
   p.b_rows_per_expert = 0;
   p.gather = 0;
-  if (BN == 48) return launch_gemm<48, kModeRouter, false>(tmA, tmB, tmC, p, stream);
-  if (BN == 96) return launch_gemm<96, kModeRouter, false>(tmA, tmB, tmC, p, stream);
-  return launch_gemm<192, kModeRouter, false>(tmA, tmB, tmC, p, stream);
+  p.units = 3;  // pairs of 128-row blocks; an odd last block runs as a half-empty pair
+  if (BN == 48) return launch_gemm<48, kModeRouter, true>(tmA, tmB, tmC, p, stream);
+  if (BN == 96) return launch_gemm<96, kModeRouter, true>(tmA, tmB, tmC, p, stream);
+  return launch_gemm<192, kModeRouter, true>(tmA, tmB, tmC, p, stream);
 }
 
 // Wr [d, E] fp32 -> Wr3 [nblk * 3EB, d] bf16: for expert block b, rows

@@ -73,17 +73,27 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   for (int e = wid; e < E; e += 32) {
     int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
     int32_t run = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int32_t v = (c < nchunks) ? hrow[c] : 0;
-      int32_t incl = v;
+    // 256 chunk counts per pass, all loads issued before the first scan
+    for (int c0 = 0; c0 < nchunks; c0 += 8 * 32) {
+      int32_t v[8];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + 32 * i + lane;
+        v[i] = (c < nchunks) ? hrow[c] : 0;
       }
-      if (c < nchunks) hrow[c] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c0 + 32 * i >= nchunks) break;  // warp-uniform
+        const int c = c0 + 32 * i + lane;
+        int32_t incl = v[i];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (c < nchunks) hrow[c] = run + incl - v[i];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) cnt_s[e] = run;
   }
