@@ -284,6 +284,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         const int mb = unit_block(p.units, mu, rank, gcount);
         const int row0 = gstart + mb * C::BM;
         const int rows_valid = min(C::BM, gcount - mb * C::BM);
+        // units 3: the odd CTA's block of the last pair may lie past the group
+        const bool partner_empty = PAIR && (2 * mu + 1) * C::BM >= gcount;
         // gathered rows past the group repeat a row of the group
         const int last = max(rows_valid, 1) - 1;
         const int tok_base = rows_valid > 0 ? row0 : gstart;
@@ -315,8 +317,13 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
               // both CTAs' TMA copies complete on the even CTA's barrier
               const uint32_t fb0 = map_to_cta(fb, 0);
               if (lane == 0) {
-                if (leader) mbar_arrive_expect_tx(fb, 2 * (p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES));
-                if (p.gather == 0) tma_load_2d_pair(a_dst, &tmA, kb * C::BK, row0, fb0, pol_a);
+                // a half-empty pair tile (the odd CTA's block lies past the
+                // group) skips the odd CTA's A rows: its accumulator rows are
+                // never stored, so stale operand rows there are harmless
+                if (leader)
+                  mbar_arrive_expect_tx(fb, p.gather == 2 ? 2 * C::B_BYTES
+                                                          : 2 * C::STAGE_BYTES - (partner_empty ? C::A_BYTES : 0));
+                if (p.gather == 0 && rows_valid > 0) tma_load_2d_pair(a_dst, &tmA, kb * C::BK, row0, fb0, pol_a);
                 tma_load_2d_pair(b_dst, &tmB, kb * C::BK, brow, fb0, pol_b);
               }
             } else {
