@@ -113,6 +113,11 @@ struct GemmCfg {
 // in increasing order, starting from e = 0); on exit the group of tau.  A few
 // linear probes cover the usual step to the same or a nearby group, then a
 // binary search over the rest.  prefix[E] * n_blocks > tau bounds both.
+// Within a group the m-block runs fastest (N_FAST false): the expert's weight
+// slice of one n-block stays in L2 for all its m-blocks.  N_FAST (the router,
+// whose whole B is a few MB) runs the n-blocks of one m-block together, so
+// each A row block is read from HBM once.
+template <bool N_FAST = false>
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
                                             int& mb) {
   for (int probe = 0; prefix[e + 1] * n_blocks <= tau; ++probe) {
@@ -131,9 +136,14 @@ __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int 
     ++e;
   }
   const int local = tau - prefix[e] * n_blocks;
-  const int me = prefix[e + 1] - prefix[e];
-  nb = local / me;
-  mb = local - nb * me;
+  if (N_FAST) {
+    mb = local / n_blocks;
+    nb = local - mb * n_blocks;
+  } else {
+    const int me = prefix[e + 1] - prefix[e];
+    nb = local / me;
+    mb = local - nb * me;
+  }
 }
 
 // Tile units of a group with mblocks 128-row blocks: 0 every block, 1
@@ -271,15 +281,18 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     // ------------------------------------------------------------ producers
     const bool issuer = (warp == 0);
     if (issuer || p.gather == 2) {
-      const uint64_t pol_a = policy_evict_last();    // A rows are re-read by every n-block
-      const uint64_t pol_b = policy_evict_normal();  // B tiles are re-read by the m-blocks of one group
+      // expert GEMMs: A rows are re-read by every n-block, a B slice only by
+      // the m-blocks of one group; router: the few-MB B is re-read by every
+      // m-block, an A row block only by its n-blocks (run together)
+      const uint64_t pol_a = MODE == kModeRouter ? policy_evict_normal() : policy_evict_last();
+      const uint64_t pol_b = MODE == kModeRouter ? policy_evict_last() : policy_evict_normal();
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       int e = 0;  // group cursor of decode_tile
       for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
         int nb, mu, gstart, gcount;
-        decode_tile(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
+        decode_tile<MODE == kModeRouter>(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, grp_s, e, gstart, gcount);
         const int mb = unit_block(p.units, mu, rank, gcount);
         const int row0 = gstart + mb * C::BM;
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     float nx_w = 0.f;
     auto decode_next = [&](int t) {
       int mu, gstart, gcount;
-      decode_tile(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
+      decode_tile<MODE == kModeRouter>(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
       group_rows(p, grp_s, dec_e, gstart, gcount);
       const int mb = unit_block(p.units, mu, rank, gcount);
       nx_row0 = gstart + mb * C::BM;
