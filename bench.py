@@ -41,11 +41,12 @@ from mixture_experts_layer_93_b300 import inputs as I  # noqa: E402
 METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (read + write) of one up-projection launch from an ncu capture of
-# the current kernel (profiles/moe_gemm_mixtral.md), keyed by workload, A path
-# and kernel revision; a kernel change bumps GEMM_REV and drops stale entries.
-GEMM_REV = "cta-pair-tma-store-v6"
-UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2118082048 + 459504128}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one up-projection
+# launch, from an ncu capture of the current kernel on the full workload, keyed
+# by workload, A path and kernel revision; a kernel change bumps GEMM_REV and
+# drops stale entries.
+GEMM_REV = "cta-pair-skip-empty-a-v7"
+UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2895006890}  # mean of three launches
 
 
 def load_peaks():
