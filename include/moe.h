@@ -110,10 +110,9 @@ int moe_clear_device_status(void* ws, void* stream);
 /* One-time weight repack into the layouts the grouped GEMMs read K-major.
  *   W1, W3   [E, d, n] bf16   (W1 = gated branch, W3 = linear branch)
  *   W2       [E, n, d] bf16
- *   W13p     [E, 2n, d] bf16 out: per block b of H = (n % 128 ? 64 : 128)
- *            columns, rows [2Hb, 2Hb+H) hold W1[e][:, Hb + i]^T and rows
- *            [2Hb+H, 2Hb+2H) hold W3[e][:, Hb + i]^T, so one GEMM tile
- *            carries matching gate and linear columns.
+ *   W13p     [E, 2n, d] bf16 out: row 2j holds W1[e][:, j]^T and row 2j+1
+ *            holds W3[e][:, j]^T, so every GEMM tile carries matching gate
+ *            and linear columns side by side.
  *   W2p      [E, d, n] bf16 out: W2p[e][i][j] = W2[e][j][i]. */
 int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, const void* W2,
                         void* W13p, void* W2p, void* stream);

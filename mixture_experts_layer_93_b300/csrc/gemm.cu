@@ -521,20 +521,22 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const int warp_rows = max(0, min(32, rows_valid - ew * 32));
       const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
       if constexpr (MODE == kModeUp) {
-        // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile
+        // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile; accumulator
+        // columns 2j and 2j+1 hold the gate and linear branch of h column j
         constexpr int H = BN / 2;
         __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
 #pragma unroll 1
         for (int c = ch * (H / NCH); c < (ch + 1) * (H / NCH); c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c, g);
-          tmem_ld32(taddr + H + c, u);
+          uint32_t a[2][32];
+          tmem_ld32(taddr + 2 * c, a[0]);
+          tmem_ld32(taddr + 2 * c + 32, a[1]);
           tc_wait_ld();
           uint32_t o[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
-            const float g0 = __uint_as_float(g[2 * q]), g1 = __uint_as_float(g[2 * q + 1]);
-            const float u0 = __uint_as_float(u[2 * q]), u1 = __uint_as_float(u[2 * q + 1]);
+            const uint32_t* v = a[q >> 3] + 4 * (q & 7);
+            const float g0 = __uint_as_float(v[0]), u0 = __uint_as_float(v[1]);
+            const float g1 = __uint_as_float(v[2]), u1 = __uint_as_float(v[3]);
             const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             o[q] = pack_bf16x2(h0, h1);

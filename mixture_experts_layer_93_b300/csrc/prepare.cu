@@ -1,13 +1,13 @@
 // One-time repack of the expert weights into the K-major layouts the grouped
 // GEMMs stream with TMA (both operands of a tcgen05 MMA are read K-major).
 //
-//   W13p[e][p][i]: p in block b of 2H rows (H = 128, or 64 when n % 128 != 0):
-//                  p = 2Hb + r, r < H  -> W1[e][i][Hb + r]
-//                               r >= H -> W3[e][i][Hb + r - H]
-//   W2p[e][i][j] = W2[e][j][i]
+//   W13p[e][2j][i]     = W1[e][i][j]   (gate branch, column j)
+//   W13p[e][2j + 1][i] = W3[e][i][j]   (linear branch, column j)
+//   W2p[e][i][j]       = W2[e][j][i]
 //
-// Interleaving gate and linear columns per block lets one accumulator tile
-// hold both halves of SwiGLU, so the activation is applied in the epilogue.
+// Interleaving gate and linear rows pairwise puts both halves of SwiGLU for
+// output column j in adjacent accumulator columns of every tile, whatever its
+// width, so the activation runs in the epilogue.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -17,7 +17,7 @@ namespace moe {
 // mode 0: identity row map (W2 -> W2p); mode 1/2: W1/W3 into W13p.
 __global__ void __launch_bounds__(256) transpose_pack_kernel(const __nv_bfloat16* __restrict__ src,
                                                              __nv_bfloat16* __restrict__ dst, int rows, int cols,
-                                                             int mode, int H, int64_t dst_expert_stride) {
+                                                             int mode, int64_t dst_expert_stride) {
   __shared__ __nv_bfloat16 tile[32][33];
   const int e = blockIdx.z;
   const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const __nv_bfloat16
     const int c = c0 + i, r = r0 + tx;
     if (r < rows && c < cols) {
       int64_t p = c;
-      if (mode != 0) p = static_cast<int64_t>(c / H) * 2 * H + (mode == 2 ? H : 0) + (c % H);
+      if (mode != 0) p = 2 * static_cast<int64_t>(c) + (mode == 2 ? 1 : 0);
       dd[p * rows + r] = tile[tx][i];
     }
   }
@@ -41,14 +41,13 @@ __global__ void __launch_bounds__(256) transpose_pack_kernel(const __nv_bfloat16
 
 void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, const __nv_bfloat16* W2,
                             __nv_bfloat16* W13p, __nv_bfloat16* W2p, int E, int d, int n, cudaStream_t stream) {
-  const int H = up_half_block(n);
   // W1/W3: [d, n] per expert -> rows of W13p (row length d)
   dim3 g13((n + 31) / 32, (d + 31) / 32, E);
-  transpose_pack_kernel<<<g13, 256, 0, stream>>>(W1, W13p, d, n, 1, H, static_cast<int64_t>(2) * n * d);
-  transpose_pack_kernel<<<g13, 256, 0, stream>>>(W3, W13p, d, n, 2, H, static_cast<int64_t>(2) * n * d);
+  transpose_pack_kernel<<<g13, 256, 0, stream>>>(W1, W13p, d, n, 1, static_cast<int64_t>(2) * n * d);
+  transpose_pack_kernel<<<g13, 256, 0, stream>>>(W3, W13p, d, n, 2, static_cast<int64_t>(2) * n * d);
   // W2: [n, d] per expert -> W2p [d, n]
   dim3 g2((d + 31) / 32, (n + 31) / 32, E);
-  transpose_pack_kernel<<<g2, 256, 0, stream>>>(W2, W2p, n, d, 0, H, static_cast<int64_t>(d) * n);
+  transpose_pack_kernel<<<g2, 256, 0, stream>>>(W2, W2p, n, d, 0, static_cast<int64_t>(d) * n);
 }
 
 }  // namespace moe

@@ -93,6 +93,22 @@ def _synthetic_routing(T, E, k, seed, skew=0.0):
     return idx, counts, offsets, src, dst
 
 
+# ---------------------------------------------------------- weight repack
+@pytest.mark.parametrize("E,d,n", [(3, 128, 64), (2, 192, 320), (1, 64, 128)])
+def test_prepare_weights_layout(cuda_device, E, d, n):
+    """W13p row 2j = W1[:, j]^T, row 2j+1 = W3[:, j]^T; W2p = W2^T (bit copies)."""
+    g = torch.Generator(device="cpu").manual_seed(E * 1000 + d + n)
+    W1 = torch.randn(E, d, n, generator=g).to(torch.bfloat16)
+    W3 = torch.randn(E, d, n, generator=g).to(torch.bfloat16)
+    W2 = torch.randn(E, n, d, generator=g).to(torch.bfloat16)
+    W13p, W2p = B.moe_prepare_weights(W1.to(cuda_device), W3.to(cuda_device), W2.to(cuda_device))
+    W13p, W2p = W13p.cpu(), W2p.cpu()
+    assert W13p.shape == (E, 2 * n, d) and W2p.shape == (E, d, n)
+    assert torch.equal(W13p[:, 0::2, :], W1.transpose(1, 2))
+    assert torch.equal(W13p[:, 1::2, :], W3.transpose(1, 2))
+    assert torch.equal(W2p, W2.transpose(1, 2))
+
+
 # ------------------------------------------------------------ up-projection
 @pytest.mark.parametrize("gather", [0, 1, 2, "0-token", "0-offsets"])
 @pytest.mark.parametrize("T,d,n,E,k,skew", [(700, 256, 192, 6, 2, 0.0), (600, 384, 256, 5, 3, 1.0),
@@ -128,6 +144,83 @@ def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
     # the exact value, plus fp32 accumulation noise
     rms = float(np.sqrt(np.mean(h_ref ** 2)))
     assert np.all(np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-5 * rms), err_stats(h_gpu, h_ref)
+
+
+# Per-expert counts whose last 128-row block takes sizes across 1..128 rows,
+# with odd and even block counts.  Plus 0 they take the separate odd-block
+# launch; plus 1024 each (same remainders) the host runs odd blocks as
+# half-empty SM pairs.
+ODD_COUNTS = [1, 31, 32, 33, 64, 95, 97, 128, 129, 160, 255, 256, 257, 300, 383, 384, 0, 450]
+
+
+def _routing_with_counts(counts, seed):
+    """k = 1 routing whose expert e gets exactly counts[e] tokens (shuffled)."""
+    g = np.random.default_rng(seed)
+    idx = np.repeat(np.arange(len(counts)), counts)
+    g.shuffle(idx)
+    idx = torch.from_numpy(idx.astype(np.int32)).reshape(-1, 1)
+    c, offsets, src, dst = O.permute(idx.numpy(), len(counts))
+    assert list(c) == list(counts)
+    return idx, c, offsets, src, dst
+
+
+@pytest.mark.parametrize("extra", [0, 1024])
+def test_expert_up_odd_tails(cuda_device, extra):
+    """Up GEMM on SM pairs (n % 128 == 0) with odd last blocks of every size:
+    h within one bf16 rounding."""
+    counts = [c + extra for c in ODD_COUNTS]
+    T, d, n, E, k = sum(counts), 256, 256, len(counts), 1
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=11)
+    idx, c, offsets, src, dst = _routing_with_counts(counts, seed=5)
+    s, ws = ws_for(T, d, n, E, k, cuda_device)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    row_token = torch.from_numpy((src // k).astype(np.int32)).to(cuda_device)
+    h = B.moe_expert_up(s, inp["x"], W13p, torch.from_numpy(c.astype(np.int32)).to(cuda_device),
+                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=0,
+                        tok_rows=torch.from_numpy(dst.astype(np.int32)).to(cuda_device))
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    h_gpu = to64(h[:T])
+    h_ref = np.zeros((T, n))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            h_ref[r0:r1] = O.expert_hidden(inp["x"][torch.from_numpy(src[r0:r1] // k).to(cuda_device)],
+                                           inp["W1"][e], inp["W3"][e])
+    rms = float(np.sqrt(np.mean(h_ref ** 2)))
+    assert np.all(np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-5 * rms), err_stats(h_gpu, h_ref)
+
+
+@pytest.mark.parametrize("extra", [0, 1024])
+def test_expert_down_odd_tails(cuda_device, extra):
+    """Down GEMM on SM pairs (d % 256 == 0) with odd last blocks of every
+    size: ys within one fp16 rounding, gate weight applied per row."""
+    counts = [c + extra for c in ODD_COUNTS]
+    T, d, n, E, k = sum(counts), 512, 128, len(counts), 1
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=12)
+    idx, c, offsets, src, dst = _routing_with_counts(counts, seed=6)
+    g = torch.Generator(device="cpu").manual_seed(13)
+    h = torch.randn(T, n, generator=g).to(torch.bfloat16).to(cuda_device)
+    row_w = torch.rand(T, generator=g).to(cuda_device)
+    s, ws = ws_for(T, d, n, E, k, cuda_device)
+    W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    cap = B.moe_row_capacity(s)
+    hcap = torch.zeros(cap, n, dtype=torch.bfloat16, device=cuda_device)
+    hcap[:T] = h
+    wcap = torch.zeros(cap, device=cuda_device)
+    wcap[:T] = row_w
+    ys = B.moe_expert_down(s, hcap, W2p, torch.from_numpy(c.astype(np.int32)).to(cuda_device),
+                           torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap, ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    ref = np.zeros((T, d))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = to64(row_w[r0:r1])[:, None] * O.expert_out(h[r0:r1], inp["W2"][e])
+    got = to64(ys[:T])
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-5 * rms), err_stats(got, ref)
 
 
 # ---------------------------------------------------------- down-projection
