@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __half* __restrict__
                                                       const int32_t* __restrict__ tok_offsets,
                                                       const int32_t* __restrict__ tok_rows, float* __restrict__ y,
                                                       int T, int d, int k) {
+  pdl_wait();
+  pdl_trigger();
   const int groups = d / 8;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(T) * groups) return;
@@ -52,7 +54,7 @@ void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t*
                     int k, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(T) * (d / 8);
   const int blocks = static_cast<int>((total + 255) / 256);
-  combine_kernel<<<blocks, 256, 0, stream>>>(ys, tok_offsets, tok_rows, y, T, d, k);
+  launch_pdl(combine_kernel, blocks, 256, 0, stream, 1, ys, tok_offsets, tok_rows, y, T, d, k);
 }
 
 }  // namespace moe

@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     tc_fence_before();
   } else if (warp == kEpiWarp0) {
     // prefix[e] = number of tile units of groups < e (this warp is free before the pipeline starts)
+    pdl_wait();  // counts come from the previous kernel
     if (p.single_rows > 0) {
       if (lane == 0) {
         prefix[0] = 0;
@@ -269,6 +270,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       }
     }
   }
+  // barrier init, TMEM allocation and descriptor prefetch above touch no data
+  // of earlier kernels; everything below may
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   // the peer's copies, commits and arrivals target our barriers: both CTAs'
   // barriers are initialised before either starts
@@ -710,7 +715,8 @@ static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (!PAIR) {
-    kern<<<num_sms(), kGemmThreads, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
+    if (launch_pdl(kern, num_sms(), kGemmThreads, C::SMEM_BYTES, stream, 1, tmA, tmB, tmC, p) != cudaSuccess)
+      return MOE_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg = {};
@@ -729,14 +735,17 @@ static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const
   int clusters = 0;
   cfg.gridDim = dim3(num_sms() & ~1);
   if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) clusters = num_sms() / 2;
-  cfg.gridDim = dim3(2 * std::min(clusters, num_sms() / 2));
-  if (cudaLaunchKernelEx(&cfg, kern, tmA, tmB, tmC, p) != cudaSuccess) return MOE_ERR_CUDA;
+  const int grid = 2 * std::min(clusters, num_sms() / 2);
+  if (launch_pdl(kern, grid, kGemmThreads, C::SMEM_BYTES, stream, 2, tmA, tmB, tmC, p) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_token,
                                    const int32_t* __restrict__ offsets, int E, int d,
                                    __nv_bfloat16* __restrict__ out, int64_t rows_cap) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t R = min(static_cast<int64_t>(offsets[E]), rows_cap);
   const int groups = d / 8;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < R * groups;
@@ -750,7 +759,7 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const in
 
 void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const int32_t* offsets, int E, int d,
                         __nv_bfloat16* out, int64_t rows_cap, cudaStream_t stream) {
-  gather_rows_kernel<<<num_sms() * 8, 256, 0, stream>>>(x, row_token, offsets, E, d, out, rows_cap);
+  launch_pdl(gather_rows_kernel, num_sms() * 8, 256, 0, stream, 1, x, row_token, offsets, E, d, out, rows_cap);
 }
 
 // The same copy in token order: one warp per token reads x[t] once, 4 KB at
@@ -761,6 +770,8 @@ __global__ void __launch_bounds__(256) gather_rows_by_token_kernel(const __nv_bf
                                                                    const int32_t* __restrict__ tok_rows,
                                                                    const int32_t* __restrict__ tok_offsets, int T,
                                                                    int k, int d, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -789,7 +800,7 @@ __global__ void __launch_bounds__(256) gather_rows_by_token_kernel(const __nv_bf
 
 void launch_gather_rows_by_token(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T,
                                  int k, int d, __nv_bfloat16* out, cudaStream_t stream) {
-  gather_rows_by_token_kernel<<<(T + 7) / 8, 256, 0, stream>>>(x, tok_rows, tok_offsets, T, k, d, out);
+  launch_pdl(gather_rows_by_token_kernel, (T + 7) / 8, 256, 0, stream, 1, x, tok_rows, tok_offsets, T, k, d, out);
 }
 
 // How SM-pair GEMMs treat an expert's odd last 128-row block.  Run as a
@@ -943,6 +954,8 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
 // past E are zero.
 __global__ void split_router_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ Wr3, int d, int E,
                                     int EB, int nblk) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t total = static_cast<int64_t>(nblk) * EB * d;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -973,7 +986,7 @@ void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cuda
   const int nblk = (E + EB - 1) / EB;
   const int64_t total = static_cast<int64_t>(nblk) * EB * d;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, num_sms() * 16));
-  split_router_kernel<<<blocks, 256, 0, stream>>>(Wr, Wr3, d, E, EB, nblk);
+  launch_pdl(split_router_kernel, blocks, 256, 0, stream, 1, Wr, Wr3, d, E, EB, nblk);
 }
 
 // ------------------------------------------------------------- selftest

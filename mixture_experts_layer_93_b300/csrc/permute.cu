@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_
                                                                   const int32_t* __restrict__ len, int E,
                                                                   int nchunks, int32_t* __restrict__ chunk_hist,
                                                                   int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t hist_s[];
   const int c = blockIdx.x;
   A = list_length(A, len);
@@ -65,6 +67,8 @@ __global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_
 // are scanned and added back as each expert's base.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist, int E, int nchunks,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t cnt_s[1024];
   __shared__ int32_t warp_s[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -145,6 +149,8 @@ __global__ void __launch_bounds__(kPermWarps * 32) perm_scatter_kernel(
     const int32_t* __restrict__ len, int k, int E, int nchunks, const int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ src, int32_t* __restrict__ dst, int32_t* __restrict__ row_token,
     float* __restrict__ row_w) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t wbase[];  // [kPermWarps][E]
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int c = blockIdx.x;
@@ -199,10 +205,10 @@ static void permute_impl(const int32_t* idx, const float* w, const int32_t* toke
                          int k, int E, int32_t* chunk_hist, int32_t* counts, int32_t* offsets, int32_t* src,
                          int32_t* dst, int32_t* row_token, float* row_w, int32_t* status, cudaStream_t stream) {
   const int nchunks = static_cast<int>(perm_num_chunks(A));
-  perm_hist_kernel<<<nchunks, kPermWarps * 32, static_cast<size_t>(E) * sizeof(int32_t), stream>>>(
+  launch_pdl(perm_hist_kernel, nchunks, kPermWarps * 32, static_cast<size_t>(E) * sizeof(int32_t), stream, 1, 
       idx, A, len, E, nchunks, chunk_hist, status);
-  perm_scan_kernel<<<1, 1024, 0, stream>>>(chunk_hist, E, nchunks, counts, offsets);
-  perm_scatter_kernel<<<nchunks, kPermWarps * 32, static_cast<size_t>(kPermWarps) * E * sizeof(int32_t), stream>>>(
+  launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, 1, chunk_hist, E, nchunks, counts, offsets);
+  launch_pdl(perm_scatter_kernel, nchunks, kPermWarps * 32, static_cast<size_t>(kPermWarps) * E * sizeof(int32_t), stream, 1, 
       idx, w, token_of, A, len, k, E, nchunks, chunk_hist, src, dst, row_token, row_w);
 }
 

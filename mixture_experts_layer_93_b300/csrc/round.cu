@@ -102,6 +102,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 __global__ void member_bitmap_kernel(const int32_t* __restrict__ idx, int T, int k, int E, int64_t W,
                                      uint32_t* __restrict__ member, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= static_cast<int64_t>(T) * k) return;
   const int t = static_cast<int>(i / k);
@@ -146,6 +148,8 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
                                                                       int32_t* __restrict__ new_counts,
                                                                       uint32_t* __restrict__ global_keys,
                                                                       int keys_in_smem) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t smem_keys[];
   __shared__ int red[33];
   __shared__ int hist[256];
@@ -310,6 +314,8 @@ __global__ void __launch_bounds__(kSelectThreads) round_select_kernel(const floa
 // 32*eb+i's word, and a ballot over lanes of bit j is token j's 32 experts.
 __global__ void bits_transpose_kernel(const uint32_t* __restrict__ final_set, int T, int E, int64_t W, int EW,
                                       uint32_t* __restrict__ tok_bits) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t wg = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nblk = static_cast<int64_t>(EW) * W;
@@ -335,6 +341,8 @@ __global__ void bits_transpose_kernel(const uint32_t* __restrict__ final_set, in
 __global__ void __launch_bounds__(1024) token_offsets_local_kernel(const uint32_t* __restrict__ tok_bits, int T,
                                                                    int EW, int32_t* __restrict__ tok_offsets,
                                                                    int32_t* __restrict__ block_sums) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t warp_s[32];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int t = blockIdx.x * 1024 + tid;
@@ -366,6 +374,8 @@ __global__ void __launch_bounds__(1024) token_offsets_local_kernel(const uint32_
 
 __global__ void __launch_bounds__(1024) token_offsets_add_kernel(int T, int32_t* __restrict__ tok_offsets,
                                                                  const int32_t* __restrict__ block_sums) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t base_s;
   const int tid = threadIdx.x;
   if (tid < 32) {
@@ -391,6 +401,8 @@ __global__ void __launch_bounds__(256) token_sets_kernel(const float* __restrict
                                                          const int32_t* __restrict__ tok_offsets,
                                                          int32_t* __restrict__ tok_expert, float* __restrict__ tok_w,
                                                          int32_t* __restrict__ tok_token) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -450,7 +462,7 @@ void launch_token_sets(const float* L, const uint32_t* tok_bits, int T, int E, i
                        int32_t* tok_expert, float* tok_w, int32_t* tok_token, cudaStream_t stream) {
   const int blocks = (T + 7) / 8;
 #define MOE_SETS(NV) \
-  token_sets_kernel<NV><<<blocks, 256, 0, stream>>>(L, tok_bits, T, E, EW, tok_offsets, tok_expert, tok_w, tok_token)
+  launch_pdl(token_sets_kernel<NV>, blocks, 256, 0, stream, 1, L, tok_bits, T, E, EW, tok_offsets, tok_expert, tok_w, tok_token)
   if (EW <= 1)
     MOE_SETS(1);
   else if (EW <= 2)
@@ -481,21 +493,21 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
   RoundScratch s = carve(scratch, T, E, cap);
   cudaMemsetAsync(s.member, 0, static_cast<size_t>(E * W * 4), stream);
   const int64_t A = static_cast<int64_t>(T) * k;
-  member_bitmap_kernel<<<static_cast<int>((A + 255) / 256), 256, 0, stream>>>(idx, T, k, E, W, s.member, status);
+  launch_pdl(member_bitmap_kernel, static_cast<int>((A + 255) / 256), 256, 0, stream, 1, idx, T, k, E, W, s.member, status);
   const int in_smem = T <= kSmemKeyLimit ? 1 : 0;
   const size_t key_smem = in_smem ? static_cast<size_t>(T) * 4 : 0;
   cudaFuncSetAttribute(round_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        static_cast<int>(kSmemKeyLimit) * 4);
-  round_select_kernel<<<E, kSelectThreads, key_smem, stream>>>(logits, T, E, W, tile, mode, seed, s.member,
+  launch_pdl(round_select_kernel, E, kSelectThreads, key_smem, stream, 1, logits, T, E, W, tile, mode, seed, s.member,
                                                               s.final_set,
                                                               s.new_counts, s.keys, in_smem);
   const int EW = (E + 31) / 32;
   const int64_t tblocks = static_cast<int64_t>(EW) * W;  // warps
-  bits_transpose_kernel<<<static_cast<int>((tblocks * 32 + 255) / 256), 256, 0, stream>>>(s.final_set, T, E, W, EW,
+  launch_pdl(bits_transpose_kernel, static_cast<int>((tblocks * 32 + 255) / 256), 256, 0, stream, 1, s.final_set, T, E, W, EW,
                                                                                          s.tok_bits);
   const int tb = (T + 1023) / 1024;
-  token_offsets_local_kernel<<<tb, 1024, 0, stream>>>(s.tok_bits, T, EW, tok_offsets, s.block_sums);
-  token_offsets_add_kernel<<<tb, 1024, 0, stream>>>(T, tok_offsets, s.block_sums);
+  launch_pdl(token_offsets_local_kernel, tb, 1024, 0, stream, 1, s.tok_bits, T, EW, tok_offsets, s.block_sums);
+  launch_pdl(token_offsets_add_kernel, tb, 1024, 0, stream, 1, T, tok_offsets, s.block_sums);
   launch_token_sets(logits, s.tok_bits, T, E, EW, tok_offsets, s.tok_expert, s.tok_w, s.tok_token, stream);
   // stable grouping by expert of the token-ordered list: rows of an expert
   // come out in ascending t; tok_rows is the list's row map (moe_permute's dst)

@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(256) topk_gating_kernel(const float* __restric
                                                           int32_t* __restrict__ topk_idx,
                                                           float* __restrict__ topk_w, int T, int E, int k,
                                                           int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -130,6 +132,8 @@ __global__ void __launch_bounds__(256) topk_gating_sorted_kernel(const float* __
                                                                  int32_t* __restrict__ topk_idx,
                                                                  float* __restrict__ topk_w, int T, int E, int k,
                                                                  int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
@@ -180,17 +184,17 @@ void launch_topk_gating(const float* logits, int32_t* idx, float* w, int T, int 
   const int blocks = (T + 7) / 8;
   const int nv = (E + 31) / 32;
   if (nv <= 1)
-    topk_gating_sorted_kernel<1><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_sorted_kernel<1>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
   else if (nv <= 2)
-    topk_gating_sorted_kernel<2><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_sorted_kernel<2>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
   else if (nv <= 4)
-    topk_gating_sorted_kernel<4><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_sorted_kernel<4>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
   else if (nv <= 8)
-    topk_gating_sorted_kernel<8><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_sorted_kernel<8>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
   else if (nv <= 16)
-    topk_gating_kernel<16><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_kernel<16>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
   else
-    topk_gating_kernel<32><<<blocks, 256, 0, stream>>>(logits, idx, w, T, E, k, status);
+    launch_pdl(topk_gating_kernel<32>, blocks, 256, 0, stream, 1, logits, idx, w, T, E, k, status);
 }
 
 }  // namespace moe
