@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # launch, from an ncu capture of the current kernel on the full workload, keyed
 # by workload, A path and kernel revision; a kernel change bumps GEMM_REV and
 # drops stale entries.
-GEMM_REV = "cta-pair-skip-empty-a-v7"
-UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2895006890}  # mean of three launches
+GEMM_REV = "cta-pair-pdl-interleaved-w13-v8"
+UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 2509180074}  # mean of three launches
 
 
 def load_peaks():
@@ -258,48 +258,52 @@ def run_ours(args, world, rank, local):
     P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
-    stages = ["route", "permute", "up", "down", "combine"]
-    # route: Wr split + router GEMM + top-k; permute: 3; rounding: member,
-    # select, transpose, 2 offsets, sets + a 3-launch permutation (9); up: row gather + SM-pair GEMM + odd-block GEMM
-    # (A path 0) or one GEMM (paths 1, 2); down: SM-pair + odd-block GEMMs;
-    # combine: 1
+    # rounding off: route+permute fused (Wr split, router GEMM, fused top-k +
+    # histogram, scan, scatter: 5 launches; 6 when E > 256); rounding: route
+    # (Wr split, router GEMM, top-k: 3) then member, select, transpose, 2
+    # offsets, sets + a 3-launch permutation (9).  up: row gather + SM-pair GEMM
+    # + odd-block GEMM (A path 0) or one GEMM (paths 1, 2); down: SM-pair +
+    # odd-block GEMMs; combine: 1
+    stages = ["route_permute", "up", "down", "combine"] if mode == "off" else \
+        ["route", "round", "up", "down", "combine"]
     # SM-pair GEMMs run an expert's odd last block in the same launch when
     # odd blocks are a small share (128 E <= 0.15 rows), else in a second one
     gemm_launches = 1 if 128.0 * E <= 0.15 * cap else 2
     up_launches = (1 + gemm_launches) if args.gather == 0 else (gemm_launches if d % 1 == 0 and n % 128 == 0 else 1)
-    launches_per_step = 3 + (3 if mode == "off" else 9) + up_launches + gemm_launches + 1
+    route_launches = (5 if E <= 256 else 6) if mode == "off" else 3 + 9
+    launches_per_step = route_launches + up_launches + gemm_launches + 1
 
     def check(rc, what):
         if rc != 0:
             raise B.MoEError(rc, what)
 
     def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        check(L.moe_route(sp, P(x), P(Wr), P(bias), P(logits), P(idx), P(w), ws.ptr, st), "route")
-        if ev:
-            ev[1].record(stream)
+        marks = iter(ev) if ev else None
+
+        def mark():
+            if marks:
+                next(marks).record(stream)
+
+        mark()
         if mode == "off":
-            check(L.moe_permute(sp, P(idx), P(w), P(counts), P(offsets), P(src), P(dst), P(row_token), P(row_w),
-                                ws.ptr, ws.nbytes, st), "permute")
+            check(L.moe_route_permute(sp, P(x), P(Wr), P(bias), P(logits), P(idx), P(w), P(counts), P(offsets),
+                                      P(src), P(dst), P(row_token), P(row_w), ws.ptr, ws.nbytes, st), "route_permute")
             c_off, c_rows = None, dst
         else:
+            check(L.moe_route(sp, P(x), P(Wr), P(bias), P(logits), P(idx), P(w), ws.ptr, st), "route")
+            mark()
             check(L.moe_token_round(sp, P(logits), P(idx), P(counts), P(offsets), P(row_token), P(row_w),
                                     P(tok_offsets), P(tok_rows), ws.ptr, ws.nbytes, st), "round")
             c_off, c_rows = tok_offsets, tok_rows
-        if ev:
-            ev[2].record(stream)
+        mark()
         check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(c_off), P(c_rows), P(h),
                               args.gather, ws.ptr, ws.nbytes, st), "up")
-        if ev:
-            ev[3].record(stream)
+        mark()
         check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,
                                 st), "down")
-        if ev:
-            ev[4].record(stream)
+        mark()
         check(L.moe_combine(sp, P(ys), P(c_off), P(c_rows), P(y), st), "combine")
-        if ev:
-            ev[5].record(stream)
+        mark()
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     for _ in range(args.warmup):
@@ -308,7 +312,7 @@ def run_ours(args, world, rank, local):
     B.moe_check_device_status(ws)
 
     clocks = ClockSampler(local)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
@@ -320,7 +324,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clk = clocks.stop()
     B.moe_check_device_status(ws)
-    step_ms = [events[i][0].elapsed_time(events[i][5]) for i in range(args.steps)]
+    step_ms = [events[i][0].elapsed_time(events[i][-1]) for i in range(args.steps)]
     stage_ms = {s: [events[i][j].elapsed_time(events[i][j + 1]) for i in range(args.steps)]
                 for j, s in enumerate(stages)}
     total_ms = max_over_ranks(sum(step_ms), world, dev)

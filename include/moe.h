@@ -152,6 +152,20 @@ int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w
                 int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst,
                 int32_t* row_token, float* row_w, void* ws, size_t ws_bytes, void* stream);
 
+/* Fused route + permutation (the first three steps of the fused MoE kernel of
+ * "硬件加速的考量", section 自定义核与核融合: gate scores, top-k, and the
+ * grouping that collects each expert's tokens).  Same outputs, bit for bit, as
+ * moe_route followed by moe_permute with topk_w given, in fewer launches: for
+ * E <= 256 one kernel runs the top-k of each token and counts each chunk's
+ * assignments per expert (integer atomics); the scan of the counts and the
+ * scatter follow.  (E > 256 runs the separate top-k and permutation
+ * kernels.)  Arrays as in moe_route and moe_permute; every output pointer is
+ * required.  Uses the workspace (split weights, chunk histograms). */
+int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                      float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts,
+                      int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                      float* row_w, void* ws, size_t ws_bytes, void* stream);
+
 /* moe_permute without a workspace, for callers that cannot allocate device
  * memory: code running inside a host engine that owns every device byte (a
  * serving runtime with a fixed memory arena, or a plugin loaded into another

@@ -63,6 +63,7 @@ _SIGNATURES = {
     "moe_topk_gating": (_I, [_SHP, _P, _P, _P, _P, _P]),
     "moe_route": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_route_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
@@ -240,6 +241,32 @@ def moe_permute(shape: moe_shape, topk_idx, topk_w, ws: Workspace) -> dict:
                              _ptr(out["offsets"]), _ptr(out["src"]), _ptr(out["dst"]), _ptr(out["row_token"]),
                              _ptr(out["row_w"]) if topk_w is not None else None, ws.ptr, ws.nbytes,
                              _stream(dev)), "moe_permute")
+    return out
+
+
+def moe_route_permute(shape: moe_shape, x, Wr, bias, ws: Workspace) -> dict:
+    """Fused route + permutation: logits, top-k indices and weights, and the
+    permutation arrays (as moe_route then moe_permute)."""
+    _need_cuda(x, Wr, bias)
+    dev = x.device
+    T, E, k = shape.T, shape.E, shape.k
+    A = T * k
+    cap = moe_row_capacity(shape)
+    out = {
+        "logits": torch.empty(T, E, dtype=torch.float32, device=dev),
+        "idx": torch.empty(T, k, dtype=torch.int32, device=dev),
+        "w": torch.empty(T, k, dtype=torch.float32, device=dev),
+        "counts": torch.empty(E, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
+        "src": torch.empty(cap, dtype=torch.int32, device=dev),
+        "dst": torch.empty(A, dtype=torch.int32, device=dev),
+        "row_token": torch.empty(cap, dtype=torch.int32, device=dev),
+        "row_w": torch.empty(cap, dtype=torch.float32, device=dev),
+    }
+    _check(lib().moe_route_permute(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(out["logits"]),
+                                   _ptr(out["idx"]), _ptr(out["w"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                   _ptr(out["src"]), _ptr(out["dst"]), _ptr(out["row_token"]), _ptr(out["row_w"]),
+                                   ws.ptr, ws.nbytes, _stream(dev)), "moe_route_permute")
     return out
 
 

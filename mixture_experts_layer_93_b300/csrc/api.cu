@@ -167,6 +167,31 @@ int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* b
   return moe_topk_gating(s, logits, topk_idx, topk_w, ws, stream);
 }
 
+int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
+                      int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets, int32_t* src,
+                      int32_t* dst, int32_t* row_token, float* row_w, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !logits || !topk_idx || !topk_w || !counts || !offsets || !src || !dst ||
+      !row_token || !row_w)
+    return MOE_ERR_INVALID;
+  if (!aligned16(x)) return MOE_ERR_INVALID;
+  const int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
+  int32_t* chunk_hist = at<int32_t>(ws, off[kPermHist]);
+  const bool fused = s->E <= 256;  // the fused top-k + histogram kernel (counts start at zero)
+  launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), fused ? chunk_hist : nullptr,
+                      fused ? static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k) : 0);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const int rst = launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
+                                   status_of(ws), kDefaultTimeoutNs, as_stream(stream));
+  if (rst != MOE_OK) return rst;
+  launch_topk_permute(logits, s->T, s->E, s->k, topk_idx, topk_w, chunk_hist, counts, offsets, src, dst, row_token,
+                      row_w, status_of(ws), as_stream(stream));
+  return last_launch();
+}
+
 int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w, int32_t* counts,
                 int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token, float* row_w, void* ws,
                 size_t ws_bytes, void* stream) {
@@ -258,13 +283,14 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
   void* h = at<void>(ws, off[kH]);
   void* ys = at<void>(ws, off[kYs]);
 
-  if ((st = moe_route(s, x, Wr, bias, logits, idx, w, ws, stream)) != MOE_OK) return st;
   const int32_t* combine_offsets = nullptr;
   const int32_t* combine_rows = dst;
   if (s->round == MOE_ROUND_OFF) {
-    if ((st = moe_permute(s, idx, w, counts, offsets, src, dst, row_token, row_w, ws, ws_bytes, stream)) != MOE_OK)
+    if ((st = moe_route_permute(s, x, Wr, bias, logits, idx, w, counts, offsets, src, dst, row_token, row_w, ws,
+                                ws_bytes, stream)) != MOE_OK)
       return st;
   } else {
+    if ((st = moe_route(s, x, Wr, bias, logits, idx, w, ws, stream)) != MOE_OK) return st;
     if ((st = moe_token_round(s, logits, idx, counts, offsets, row_token, row_w, tok_offsets, tok_rows, ws, ws_bytes,
                               stream)) != MOE_OK)
       return st;

@@ -953,9 +953,13 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
 // are exact in fp32, so hi + mid + lo equals w to within 2^-27 |w|.  Columns
 // past E are zero.
 __global__ void split_router_kernel(const float* __restrict__ Wr, __nv_bfloat16* __restrict__ Wr3, int d, int E,
-                                    int EB, int nblk) {
+                                    int EB, int nblk, int32_t* zero, int64_t zero_count) {
   pdl_wait();
   pdl_trigger();
+  // the counts of the fused top-k + histogram kernel that follows
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_count;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    zero[i] = 0;
   const int64_t total = static_cast<int64_t>(nblk) * EB * d;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -981,12 +985,13 @@ size_t router_split_elems(int d, int E) {
   return static_cast<size_t>(nblk) * 3 * EB * d;
 }
 
-void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream) {
+void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream, int32_t* zero,
+                         int64_t zero_count) {
   const int EB = router_expert_block(E);
   const int nblk = (E + EB - 1) / EB;
   const int64_t total = static_cast<int64_t>(nblk) * EB * d;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, num_sms() * 16));
-  launch_pdl(split_router_kernel, blocks, 256, 0, stream, 1, Wr, Wr3, d, E, EB, nblk);
+  launch_pdl(split_router_kernel, blocks, 256, 0, stream, 1, Wr, Wr3, d, E, EB, nblk, zero, zero_count);
 }
 
 // ------------------------------------------------------------- selftest

@@ -16,6 +16,12 @@ void launch_topk_gating(const float* logits, int32_t* idx, float* w, int T, int 
 // permute.cu
 constexpr int kPermChunk = 2048;  // assignments per warp chunk
 inline int64_t perm_num_chunks(int64_t A) { return (A + kPermChunk - 1) / kPermChunk; }
+// Top-k gating plus the permutation of the assignments; E <= 256 runs the
+// fused top-k + histogram kernel (chunk_hist[E * chunks] zero on entry, see
+// launch_split_router), then the scan and the scatter.
+void launch_topk_permute(const float* logits, int T, int E, int k, int32_t* idx, float* w, int32_t* chunk_hist,
+                         int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                         float* row_w, int32_t* status, cudaStream_t stream);
 void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
                     int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
                     float* row_w, int32_t* status, cudaStream_t stream);
@@ -47,7 +53,10 @@ int num_sms();
 // router on the tensor cores: Wr split into three bf16 terms (see gemm.cu)
 int router_expert_block(int E);
 size_t router_split_elems(int d, int E);
-void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream);
+// zero[0, zero_count) (nullable): zeroed for launch_topk_permute's fused
+// kernel (its chunk counts).
+void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream,
+                         int32_t* zero = nullptr, int64_t zero_count = 0);
 int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
                      int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -11,6 +11,7 @@
 //           rows of an expert come out in ascending a, i.e. ascending t.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 #include <mutex>
 
@@ -62,15 +63,14 @@ __global__ void __launch_bounds__(kPermWarps * 32) perm_hist_kernel(const int32_
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_hist[static_cast<int64_t>(e) * nchunks + c] = hist_s[e];
 }
 
-// One block of 1024 threads: warp w scans the chunk counts of experts
-// w, w+32, ... (32 chunks at a time, warp shuffles), then the expert totals
-// are scanned and added back as each expert's base.
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist, int E, int nchunks,
-                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ int32_t cnt_s[1024];
-  __shared__ int32_t warp_s[32];
+// Run by one block of 1024 threads: warp w scans the chunk counts of experts
+// w, w+32, ... (up to 256 chunks per pass, all loads issued first; warp
+// shuffles), then the expert totals are scanned and added back as each
+// expert's base.  chunk_hist[e][c] becomes the first row of expert e's rows
+// from chunk c; counts and offsets are written.  cnt_s: 1024 ints, warp_s: 32
+// ints of shared memory.
+__device__ void scan_chunk_hist(int32_t* __restrict__ chunk_hist, int E, int nchunks, int32_t* __restrict__ counts,
+                                int32_t* __restrict__ offsets, int32_t* cnt_s, int32_t* warp_s) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   for (int e = tid; e < 1024; e += blockDim.x) cnt_s[e] = 0;
   __syncthreads();
@@ -135,6 +135,45 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
     int32_t* hrow = chunk_hist + static_cast<int64_t>(e) * nchunks;
     const int32_t base = cnt_s[e];
     for (int c = lane; c < nchunks; c += 32) hrow[c] += base;
+  }
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist, int E, int nchunks,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int32_t cnt_s[1024];
+  __shared__ int32_t warp_s[32];
+  scan_chunk_hist(chunk_hist, E, nchunks, counts, offsets, cnt_s, warp_s);
+}
+
+// ---------------------------------------------------------------------------
+// Fused top-k + chunk histogram (E <= 256): a warp per token runs the top-k
+// (topk.cuh: the same code as the top-k kernel, so the same bits), writes the
+// indices and weights, and adds each assignment a = t*k + j to the count of
+// its expert in chunk a / kPermChunk with an integer atomic (counts only: the
+// order of increments does not matter).  The counts are zero on entry: the
+// split-weight kernel that precedes this one zeroes them.
+template <int NV>
+__global__ void __launch_bounds__(256) topk_perm_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                             int32_t* __restrict__ topk_idx,
+                                                             float* __restrict__ topk_w, int nchunks,
+                                                             int32_t* __restrict__ chunk_hist, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (t >= T) return;
+  bool nan_seen;
+  const uint64_t mine = warp_topk_key<NV>(logits + static_cast<size_t>(t) * E, E, k, lane, nan_seen);
+  if (__any_sync(0xffffffffu, nan_seen) && lane == 0) report_error(status, MOE_ERR_DEVICE_CHECK, t);
+  const float w = warp_gate_weight(mine, k, lane);
+  if (lane < k) {
+    const int64_t a = static_cast<int64_t>(t) * k + lane;
+    const int32_t e = topk_key_expert(mine);
+    topk_idx[a] = e;
+    topk_w[a] = w;
+    atomicAdd(&chunk_hist[static_cast<int64_t>(e) * nchunks + a / kPermChunk], 1);
   }
 }
 
@@ -217,6 +256,33 @@ void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E,
                     float* row_w, int32_t* status, cudaStream_t stream) {
   permute_impl(idx, w, nullptr, A, nullptr, k, E, chunk_hist, counts, offsets, src, dst, row_token, row_w, status,
                stream);
+}
+
+// Top-k gating and the permutation of its assignments.  E <= 256: the fused
+// top-k + histogram kernel (chunk_hist zeroed beforehand, see
+// launch_split_router), the scan and the scatter (three launches instead of
+// four); larger E: the top-k kernel and the three permutation launches.
+void launch_topk_permute(const float* logits, int T, int E, int k, int32_t* idx, float* w, int32_t* chunk_hist,
+                         int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                         float* row_w, int32_t* status, cudaStream_t stream) {
+  const int64_t A = static_cast<int64_t>(T) * k;
+  const int nchunks = static_cast<int>(perm_num_chunks(A));
+  const int nv = (E + 31) / 32;
+  if (nv > 8) {
+    launch_topk_gating(logits, idx, w, T, E, k, status, stream);
+    launch_permute(idx, w, A, k, E, chunk_hist, counts, offsets, src, dst, row_token, row_w, status, stream);
+    return;
+  }
+  auto kern = nv <= 1 ? topk_perm_hist_kernel<1>
+            : nv <= 2 ? topk_perm_hist_kernel<2>
+            : nv <= 4 ? topk_perm_hist_kernel<4>
+                      : topk_perm_hist_kernel<8>;
+  launch_pdl(kern, (T + 7) / 8, 256, 0, stream, 1, logits, T, E, k, idx, w, nchunks, chunk_hist, status);
+  launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, 1, chunk_hist, E, nchunks, counts, offsets);
+  launch_pdl(perm_scatter_kernel, nchunks, kPermWarps * 32, static_cast<size_t>(kPermWarps) * E * sizeof(int32_t),
+             stream, 1, static_cast<const int32_t*>(idx), static_cast<const float*>(w),
+             static_cast<const int32_t*>(nullptr), A, static_cast<const int32_t*>(nullptr), k, E, nchunks,
+             static_cast<const int32_t*>(chunk_hist), src, dst, row_token, row_w);
 }
 
 void launch_permute_list(const int32_t* expert_of, const float* w, const int32_t* token_of, const int32_t* len,

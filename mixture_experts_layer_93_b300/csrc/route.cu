@@ -6,6 +6,7 @@
 // the fused MoE kernel ("硬件加速的考量", section 自定义核与核融合).
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -84,49 +85,9 @@ __global__ void __launch_bounds__(256) topk_gating_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------------------
-// The same selection with each lane's candidates pre-sorted (E <= 256).
-//
-// Logit L of expert e becomes the 64-bit key (ord(L) << 32) | (2^32-1 - e),
-// where ord maps float order onto unsigned order (-0 taken as +0, NaN as
-// -inf): a larger key is a larger logit, or an equal logit of a lower expert,
-// which is exactly the order the k rounds above pick in.  Lane l sorts its NV
-// keys once (Batcher's odd-even merge network); a round is then one warp
-// max over the lanes' heads, and the winning lane shifts its list.
-__device__ __forceinline__ uint64_t topk_key(float v, int e) {
-  if (v != v) v = -INFINITY;
-  if (v == 0.f) v = 0.f;  // -0 ranks with +0
-  const uint32_t b = __float_as_uint(v);
-  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-  return (static_cast<uint64_t>(ord) << 32) | (0xffffffffu - static_cast<uint32_t>(e));
-}
-
-__device__ __forceinline__ float topk_key_value(uint64_t key) {
-  const uint32_t ord = static_cast<uint32_t>(key >> 32);
-  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
-}
-
-template <int NV>
-__device__ __forceinline__ void sort_desc(uint64_t (&a)[NV]) {
-  // Batcher's odd-even merge sort network for NV a power of two
-#pragma unroll
-  for (int p = 1; p < NV; p <<= 1) {
-#pragma unroll
-    for (int q = p; q >= 1; q >>= 1) {
-#pragma unroll
-      for (int j = q % p; j + q < NV; j += 2 * q) {
-#pragma unroll
-        for (int i = 0; i < q; ++i) {
-          if (i + j + q < NV && (i + j) / (2 * p) == (i + j + q) / (2 * p)) {
-            const uint64_t x = a[i + j], y = a[i + j + q];
-            a[i + j] = x > y ? x : y;
-            a[i + j + q] = x > y ? y : x;
-          }
-        }
-      }
-    }
-  }
-}
-
+// The same selection with each lane's candidates pre-sorted (E <= 256), over
+// the 64-bit keys of topk.cuh: a round is one warp max over the lanes' heads,
+// and the winning lane shifts its list.
 template <int NV>
 __global__ void __launch_bounds__(256) topk_gating_sorted_kernel(const float* __restrict__ logits,
                                                                  int32_t* __restrict__ topk_idx,
@@ -137,45 +98,13 @@ __global__ void __launch_bounds__(256) topk_gating_sorted_kernel(const float* __
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
-  const float* row = logits + static_cast<size_t>(t) * E;
-  uint64_t key[NV];
-  bool nan_seen = false;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      const float val = row[e];
-      nan_seen |= (val != val);
-      key[i] = topk_key(val, e);
-    } else {
-      key[i] = 0;  // below every real key: never selected (k <= E)
-    }
-  }
+  bool nan_seen;
+  const uint64_t mine = warp_topk_key<NV>(logits + static_cast<size_t>(t) * E, E, k, lane, nan_seen);
   if (__any_sync(0xffffffffu, nan_seen) && lane == 0) report_error(status, MOE_ERR_DEVICE_CHECK, t);
-  sort_desc<NV>(key);
-  uint64_t mine = 0;
-  for (int j = 0; j < k; ++j) {
-    uint64_t best = key[0];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    if (((0xffffffffu - static_cast<uint32_t>(best)) & 31u) == static_cast<uint32_t>(lane)) {
-#pragma unroll
-      for (int i = 0; i + 1 < NV; ++i) key[i] = key[i + 1];
-      key[NV - 1] = 0;
-    }
-    if (lane == j) mine = best;
-  }
-  const float my_v = topk_key_value(mine);
-  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = (lane < k) ? expf(my_v - vmax) : 0.f;
-  float s = 0.f;
-  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+  const float w = warp_gate_weight(mine, k, lane);
   if (lane < k) {
-    topk_idx[static_cast<size_t>(t) * k + lane] = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(mine));
-    topk_w[static_cast<size_t>(t) * k + lane] = ex / s;
+    topk_idx[static_cast<size_t>(t) * k + lane] = topk_key_expert(mine);
+    topk_w[static_cast<size_t>(t) * k + lane] = w;
   }
 }
 

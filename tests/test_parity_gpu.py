@@ -87,6 +87,60 @@ def test_permute_bit_exact(cuda_device, T, E, k, skew):
     assert torch.equal(out["row_w"][:A].cpu(), w.reshape(-1)[torch.from_numpy(src)])
 
 
+# ------------------------------------------------------- fused route+permute
+@pytest.mark.parametrize("T,d,E,k,bias", [(1, 128, 1, 1, False), (777, 256, 8, 2, True), (1500, 128, 40, 3, False),
+                                          (5000, 256, 128, 8, False), (3001, 128, 256, 5, True),
+                                          (700, 128, 256, 6, False), (333, 128, 300, 7, True),
+                                          (4096, 128, 64, 1, False)])
+def test_route_permute_fused_matches_separate(cuda_device, T, d, E, k, bias):
+    """moe_route_permute equals moe_route then moe_permute bit for bit (every
+    output), matches the oracle's top-k and permutation on the same fp32
+    logits, and gives the same bits when called again.  k = 3, 5, 6, 7 put
+    tokens across the 2048-assignment chunk boundaries; E = 300 takes the
+    unfused path."""
+    cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=k, bias="normal" if bias else None, bias_scale=0.3)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=T + E + k, weights=False)
+    s, ws = ws_for(T, d, 64, E, k, cuda_device)
+    fused = B.moe_route_permute(s, inp["x"], inp["Wr"], inp["bias"], ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    again = B.moe_route_permute(s, inp["x"], inp["Wr"], inp["bias"], ws)
+    logits, idx, w = B.moe_route(inp["x"], inp["Wr"], inp["bias"], k, ws)
+    sep = B.moe_permute(s, idx, w, ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    A = T * k
+    pairs = [("logits", logits), ("idx", idx), ("w", w)] + [(n, sep[n]) for n in
+                                                             ("counts", "offsets", "dst")]
+    pairs += [(n, sep[n][:A]) for n in ("src", "row_token", "row_w")]
+    for name, ref in pairs:
+        got = fused[name] if name in ("logits", "idx", "w", "counts", "offsets", "dst") else fused[name][:A]
+        got2 = again[name] if name in ("logits", "idx", "w", "counts", "offsets", "dst") else again[name][:A]
+        assert torch.equal(got, ref), name
+        assert torch.equal(got2, ref), name
+    L = fused["logits"].cpu().numpy()
+    ref_idx = O.topk(L, k)
+    assert np.array_equal(fused["idx"].cpu().numpy(), ref_idx)
+    assert np.abs(to64(fused["w"]) - O.gate_weights(L, ref_idx)).max() <= 2e-6
+    counts, offsets, src, dst = O.permute(ref_idx, E)
+    assert np.array_equal(fused["counts"].cpu().numpy(), counts)
+    assert np.array_equal(fused["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(fused["src"][:A].cpu().numpy(), src)
+    assert np.array_equal(fused["dst"].cpu().numpy(), dst)
+
+
+def test_route_permute_fused_reports_nan(cuda_device):
+    T, d, E, k = 300, 128, 16, 2
+    cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=3, weights=False)
+    x = inp["x"].clone()
+    x[5, 7] = float("nan")
+    s, ws = ws_for(T, d, 64, E, k, cuda_device)
+    B.moe_clear_device_status(ws)
+    out = B.moe_route_permute(s, x, inp["Wr"], inp["bias"], ws)
+    assert B.moe_check_device_status(ws, raise_on_error=False) == B.MOE_ERR_DEVICE_CHECK
+    assert int(out["offsets"][E]) == T * k
+    B.moe_clear_device_status(ws)
+
+
 def _synthetic_routing(T, E, k, seed, skew=0.0):
     idx = I.make_topk_idx(T, E, k, seed=seed, skew=skew)
     counts, offsets, src, dst = O.permute(idx.numpy(), E)
