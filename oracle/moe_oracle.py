@@ -48,12 +48,22 @@ Readings of the pages (where they are silent or at odds):
     ordered by (L desc, id asc) and weighted by softmax over that set; an empty
     set gives y_t = 0.
 
+  * FP8 up-projection (the FP8 quantisation the pages name for MoE compute
+    and communication, "硬件加速的考量", section 量化; they fix no recipe):
+    e4m3 codes with one fp32 scale per activation row (token) and one per
+    weight output channel (a row of the packed W1/W3), scale =
+    fp32(amax / 448) (1 for an all-zero row) and code = e4m3(fp32(x / scale)),
+    rounded to nearest with ties to even and saturated to +-448.  The
+    up-projection then runs on the dequantised values code * scale; routing
+    and the down-projection stay as above.
+
 Pins (tests/test_oracle.py): brute-force k-subset top-k; the closed form
 w0 = sigmoid(L0 - L1) at k=2; numpy's stable argsort for the permutation;
 index-arithmetic SwiGLU on one-nonzero-per-column weights (catches a
 transposed operand); E=1,k=1 == dense FFN; identical experts == dense FFN;
 relabelling invariance; W2=0 -> 0; token-rounding invariants checked by
-brute force on tiny inputs.  No function here is unpinned.
+brute force on tiny inputs; e4m3 rounding against a brute-force nearest
+search over all values of the format.  No function here is unpinned.
 """
 from __future__ import annotations
 
@@ -323,3 +333,91 @@ def moe_forward(x, Wr, bias, W1, W3, W2, k: int, tile: int = 128, mode: str = RO
 def dense_swiglu_ffn(x, W1e, W3e, W2e) -> np.ndarray:
     """A dense (one-expert) SwiGLU FFN, the E=1/k=1 special case."""
     return expert_out(expert_hidden(x, W1e, W3e), W2e)
+
+
+# --------------------------------------------------------------------------
+# 7. FP8 (e4m3) up-projection
+# --------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_values() -> np.ndarray:
+    """Every finite non-negative e4m3 value, from the format's definition:
+    1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities; an
+    exponent field of 0 is subnormal (m/8 * 2^-6) and the pattern with
+    exponent field 15 and mantissa 7 is NaN."""
+    vals = []
+    for ef in range(16):
+        for m in range(8):
+            if ef == 15 and m == 7:
+                continue
+            vals.append(m / 8.0 * 2.0 ** -6 if ef == 0 else (1.0 + m / 8.0) * 2.0 ** (ef - 7))
+    return np.array(vals, dtype=F64)
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest e4m3 value, ties to the even mantissa, saturated to +-448
+    (NaN stays NaN).  In the binade [2^e, 2^(e+1)), e >= -6, values are
+    multiples of 2^(e-3); below 2^-6 of 2^-9.  Division by that power of two is
+    exact, and numpy's round() breaks ties to even."""
+    v = np.asarray(v, dtype=F64)
+    a = np.abs(v)
+    _, ex = np.frexp(a)                         # a = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, -6)
+    q = np.ldexp(1.0, e - 3)
+    r = np.minimum(np.round(a / q) * q, E4M3_MAX)
+    return np.where(np.isnan(v), np.nan, np.copysign(r, v))
+
+
+def quantize_rows_e4m3(X):
+    """(codes, scales) of each row of X: scale = fp32(amax / 448) (1 for an
+    all-zero row), code = e4m3(fp32(x / scale)); both divisions are fp32 with
+    round-to-nearest.  Codes are returned as their exact fp64 values."""
+    X32 = np.asarray(_f64(X), dtype=np.float32)
+    amax = np.max(np.abs(X32), axis=1)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    s = np.where(amax > 0, s, np.float32(1.0)).astype(np.float32)
+    v = (X32 / s[:, None]).astype(np.float32)
+    return e4m3_round(v.astype(F64)), s.astype(F64)
+
+
+def dequantized_rows_e4m3(X) -> np.ndarray:
+    """code * scale for each row of X (exact in fp64)."""
+    q, s = quantize_rows_e4m3(X)
+    return q * s[:, None]
+
+
+def quantized_expert_weights(W1e, W3e):
+    """W1e, W3e [d, n] as the FP8 path uses them: each output column
+    quantised over d (a row of the packed weights), dequantised."""
+    W1h = dequantized_rows_e4m3(_f64(W1e).T).T
+    W3h = dequantized_rows_e4m3(_f64(W3e).T).T
+    return W1h, W3h
+
+
+def moe_forward_fp8(x, Wr, bias, W1, W3, W2, k: int, tokens=None):
+    """The layer with the FP8 up-projection: routing on x as in moe_forward,
+    the up-projection on the dequantised token rows and weight columns, the
+    down-projection and combine as in moe_forward.  fp64 result."""
+    tokens, sets, weights = route(x, Wr, bias, k, tokens=tokens)
+    x64 = _f64(x)
+    xq = dequantized_rows_e4m3(x64[tokens])
+    d = x64.shape[1]
+    y = np.zeros((len(tokens), d), dtype=F64)
+    E = W1.shape[0]
+    pos_of = {e: [] for e in range(E)}
+    w_of = {e: [] for e in range(E)}
+    for p, (st, w) in enumerate(zip(sets, weights)):
+        for e, we in zip(st, w):
+            pos_of[int(e)].append(p)
+            w_of[int(e)].append(we)
+    for e in range(E):
+        if not pos_of[e]:
+            continue
+        pos = np.array(pos_of[e], dtype=np.int64)
+        W1h, W3h = quantized_expert_weights(W1[e], W3[e])
+        h = expert_hidden(xq[pos], W1h, W3h)
+        o = expert_out(h, W2[e])
+        np.add.at(y, pos, np.array(w_of[e])[:, None] * o)
+    return y
+

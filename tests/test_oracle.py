@@ -360,3 +360,83 @@ def test_stochastic_token_rounding_brute_force(T, E, k, tile, seed):
     c0 = member0.sum(0)
     for e in range(E):
         assert abs(int(r["counts"][e]) - int(c0[e])) < tile
+
+
+# ------------------------------------------------------------------ FP8 e4m3
+def _e4m3_brute(v):
+    """Nearest value of the format by exhaustive search over all values;
+    ties to the even mantissa (even index in the ascending value list, since
+    each binade holds 8 mantissas), beyond 448 saturated."""
+    vals = O.e4m3_values()
+    out = np.empty_like(v)
+    for i, x in enumerate(v):
+        a = min(abs(x), 448.0)
+        d = np.abs(vals - a)
+        best = np.flatnonzero(d == d.min())
+        j = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        out[i] = np.copysign(vals[j], x)
+    return out
+
+
+def test_e4m3_value_set():
+    vals = O.e4m3_values()
+    assert len(vals) == 127 and vals[0] == 0.0 and vals[-1] == 448.0
+    assert np.all(np.diff(vals) > 0)
+    assert vals[1] == 2.0 ** -9 and vals[8] == 2.0 ** -6 and 1.0 in vals
+
+
+def test_e4m3_round_fixed_points_and_saturation():
+    vals = O.e4m3_values()
+    assert np.array_equal(O.e4m3_round(vals), vals)
+    assert np.array_equal(O.e4m3_round(-vals), -vals)
+    assert np.all(O.e4m3_round(np.array([448.5, 470.0, 1e6, -500.0])) == np.array([448, 448, 448, -448]))
+    assert np.isnan(O.e4m3_round(np.array([np.nan])))[0]
+
+
+def test_e4m3_round_matches_brute_force():
+    rng = np.random.default_rng(7)
+    vals = O.e4m3_values()
+    mids = (vals[1:] + vals[:-1]) / 2
+    v = np.concatenate([rng.standard_normal(2000) * 10 ** rng.uniform(-4, 2.8, 2000), mids, -mids,
+                        mids * (1 + 1e-12), mids * (1 - 1e-12)])
+    assert np.array_equal(O.e4m3_round(v), _e4m3_brute(v))
+
+
+def test_quantize_rows_scale_and_range():
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((50, 96)).astype(np.float32)
+    X[4] = 0.0
+    q, s = O.quantize_rows_e4m3(X)
+    assert np.all(np.abs(q) <= 448) and s[4] == 1.0 and np.all(q[4] == 0)
+    amax = np.abs(X).max(axis=1)
+    assert np.array_equal(s[amax > 0], (amax[amax > 0] / np.float32(448)).astype(np.float32).astype(np.float64))
+    assert np.all(np.abs(q[amax > 0]).max(axis=1) == 448.0)
+    # the dequantised rows are within half an e4m3 step (2^-4 relative) of x
+    Xh = q * s[:, None]
+    assert np.all(np.abs(Xh - X) <= 2.0 ** -4 * np.abs(X) + 2.0 ** -10 * s[:, None] + 1e-12)
+
+
+def test_fp8_forward_on_representable_inputs_equals_plain_forward():
+    """Token rows with entries in {0, +-1/2, +-1} and weight columns with
+    entries in {0, +-c_j/2, +-c_j} are representable up to the fp32 scale
+    (x/s lands on 224 or 448): the FP8 layer equals the plain one to fp32
+    rounding of the scales.  Quantising weight rows instead of output columns
+    does not (the column maxima c_j in {0.7, 1, 1.1, 1.3} put w/amax off the
+    e4m3 grid)."""
+    rng = np.random.default_rng(11)
+    T, d, n, E, k = 40, 32, 24, 4, 2
+    x = rng.choice([0.0, 0.5, -0.5, 1.0, -1.0], size=(T, d))
+    x[:, 0] = 1.0
+    c = rng.choice([0.7, 1.0, 1.1, 1.3], size=(E, 1, n))
+    W1 = rng.choice([0.0, 0.5, -0.5, 1.0, -1.0], size=(E, d, n)) * c
+    W3 = rng.choice([0.0, 0.5, -0.5, 1.0, -1.0], size=(E, d, n)) * c[:, :, ::-1]
+    W1[:, 0, :] = c[:, 0, :]
+    W3[:, 0, :] = c[:, 0, ::-1]
+    W2 = rng.standard_normal((E, n, d)) / np.sqrt(n)
+    Wr = rng.standard_normal((d, E))
+    y = O.moe_forward(x, Wr, None, W1, W3, W2, k)
+    y8 = O.moe_forward_fp8(x, Wr, None, W1, W3, W2, k)
+    assert np.allclose(y8, y, rtol=1e-5, atol=1e-6 * np.abs(y).max())
+    # quantising W rows (over n) instead of columns gives a different layer
+    bad = [O.dequantized_rows_e4m3(W1[e]) for e in range(E)]
+    assert not all(np.allclose(b, O.quantized_expert_weights(W1[e], W3[e])[0]) for e, b in enumerate(bad))
