@@ -265,6 +265,36 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
  * [10] tok_rows i32[cap] [11] h bf16[cap*n]   [12] ys fp16[cap*d] */
 int moe_workspace_layout(const moe_shape* s, int64_t* offsets_out, int32_t n_out);
 
+/* ---------------------------------------------------------------- FP8 ---
+ * e4m3 up-projection.  The pages name FP8 among the precisions MoE compute
+ * runs in ("硬件加速的考量", section 量化) without a recipe; reading: one fp32
+ * scale per row (a token, or one output channel of the packed gate / linear
+ * weights), scale = fp32(amax / 448), code = e4m3(fp32(x * fp32(448 / amax)))
+ * rounded to nearest-even and saturated to +-448; an all-zero row has scale 1
+ * and codes 0.  Routing and the down-projection stay as in moe_forward. */
+
+/* codes[rows, K] (e4m3 bytes) and scales[rows] fp32 of src[rows, K] bf16.
+ * K % 16 == 0; src and codes 16-byte aligned.  For the weights, src is W13p
+ * from moe_prepare_weights viewed as [E * 2n, d]. */
+int moe_quantize_rows_fp8(const void* src, int64_t rows, int32_t K, void* codes, float* scales,
+                          void* stream);
+
+/* Up-projection with e4m3 operands: h[row] = silu(g) * u with
+ * g, u = (code_x . code_w) * scale_x * scale_w, fp32 accumulation (kind::f8f6f4
+ * on SM pairs), h bf16 as moe_expert_up.  x is quantised per token inside
+ * (into the workspace) while it is gathered: tok_rows / tok_offsets as in
+ * moe_expert_up's token-order gather (tok_offsets may be NULL: k rows per
+ * token).  W13q / sW13 from moe_quantize_rows_fp8 of W13p.  Requires
+ * n % 128 == 0 and d % 128 == 0 (else MOE_ERR_UNSUPPORTED). */
+int moe_expert_up_fp8(const moe_shape* s, const void* x, const void* W13q, const float* sW13,
+                      const int32_t* counts, const int32_t* offsets, const int32_t* tok_offsets,
+                      const int32_t* tok_rows, void* h, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward with the e4m3 up-projection (moe_expert_up_fp8); W2p bf16. */
+int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                    const void* W13q, const float* sW13, const void* W2p, void* y, void* ws,
+                    size_t ws_bytes, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on a
  * device flag nobody sets, giving up after `timeout_ns` nanoseconds; the
  * kernel then records MOE_ERR_TIMEOUT in the status word of `ws` and returns. */

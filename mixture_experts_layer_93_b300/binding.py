@@ -64,6 +64,9 @@ _SIGNATURES = {
     "moe_route": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_route_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_rows_fp8": (_I, [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
+    "moe_expert_up_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
@@ -268,6 +271,40 @@ def moe_route_permute(shape: moe_shape, x, Wr, bias, ws: Workspace) -> dict:
                                    _ptr(out["src"]), _ptr(out["dst"]), _ptr(out["row_token"]), _ptr(out["row_w"]),
                                    ws.ptr, ws.nbytes, _stream(dev)), "moe_route_permute")
     return out
+
+
+def moe_quantize_rows_fp8(src):
+    """(codes uint8 [rows, K], scales fp32 [rows]) of a bf16 [rows, K] tensor
+    (any leading shape is flattened into rows)."""
+    _need_cuda(src)
+    src = src.contiguous()
+    K = src.shape[-1]
+    rows = src.numel() // K
+    codes = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scales = torch.empty(src.shape[:-1], dtype=torch.float32, device=src.device)
+    _check(lib().moe_quantize_rows_fp8(_ptr(src), rows, K, _ptr(codes), _ptr(scales), _stream(src.device)),
+           "moe_quantize_rows_fp8")
+    return codes, scales
+
+
+def moe_expert_up_fp8(shape: moe_shape, x, W13q, sW13, counts, offsets, tok_rows, ws: Workspace,
+                      tok_offsets=None, h=None):
+    _need_cuda(x, W13q, sW13, counts, offsets, tok_rows, tok_offsets)
+    if h is None:
+        h = torch.empty(moe_row_capacity(shape), shape.n, dtype=torch.bfloat16, device=x.device)
+    _check(lib().moe_expert_up_fp8(ctypes.byref(shape), _ptr(x), _ptr(W13q), _ptr(sW13), _ptr(counts),
+                                   _ptr(offsets), _ptr(tok_offsets), _ptr(tok_rows), _ptr(h), ws.ptr, ws.nbytes,
+                                   _stream(x.device)), "moe_expert_up_fp8")
+    return h
+
+
+def moe_forward_fp8(shape: moe_shape, x, Wr, bias, W13q, sW13, W2p, ws: Workspace, y=None):
+    _need_cuda(x, Wr, bias, W13q, sW13, W2p)
+    if y is None:
+        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=x.device)
+    _check(lib().moe_forward_fp8(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13q), _ptr(sW13),
+                                 _ptr(W2p), _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward_fp8")
+    return y
 
 
 def moe_token_round(shape: moe_shape, logits, topk_idx, ws: Workspace) -> dict:

@@ -304,6 +304,78 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
 }
 
+int moe_quantize_rows_fp8(const void* src, int64_t rows, int32_t K, void* codes, float* scales, void* stream) {
+  if (!src || !codes || !scales || rows < 0 || K <= 0 || K % 16 != 0) return MOE_ERR_INVALID;
+  if (!aligned16(src) || !aligned16(codes)) return MOE_ERR_INVALID;
+  if (rows == 0) return MOE_OK;
+  launch_quant_rows(static_cast<const __nv_bfloat16*>(src), rows, K, static_cast<uint8_t*>(codes), scales,
+                    as_stream(stream));
+  return last_launch();
+}
+
+int moe_expert_up_fp8(const moe_shape* s, const void* x, const void* W13q, const float* sW13, const int32_t* counts,
+                      const int32_t* offsets, const int32_t* tok_offsets, const int32_t* tok_rows, void* h,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !W13q || !sW13 || !counts || !offsets || !tok_rows || !h) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13q) || !aligned16(h)) return MOE_ERR_INVALID;
+  if (s->n % 128 != 0 || s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  const int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  // the codes (cap x d bytes) and row scales (cap floats) fit in the ys
+  // region (cap x d x 2 bytes), which the forward writes only afterwards
+  const int64_t cap = row_cap(s);
+  uint8_t* xq = at<uint8_t>(ws, off[kYs]);
+  float* row_scale = reinterpret_cast<float*>(xq + cap * s->d);
+  return launch_expert_up_f8(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(W13q), sW13, counts,
+                             offsets, tok_rows, tok_offsets, static_cast<__nv_bfloat16*>(h), s->T, s->d, s->n, s->E,
+                             s->k, cap, xq, row_scale, status_of(ws), kDefaultTimeoutNs, as_stream(stream));
+}
+
+int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13q,
+                    const float* sW13, const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !W13q || !sW13 || !W2p || !y) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13q) || !aligned16(W2p) || !aligned16(y)) return MOE_ERR_INVALID;
+  if (s->n % 128 != 0 || s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  int st = check_ws(s, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off);
+  float* logits = at<float>(ws, off[kLogits]);
+  int32_t* idx = at<int32_t>(ws, off[kTopkIdx]);
+  float* w = at<float>(ws, off[kTopkW]);
+  int32_t* counts = at<int32_t>(ws, off[kCounts]);
+  int32_t* offsets = at<int32_t>(ws, off[kOffsets]);
+  int32_t* src = at<int32_t>(ws, off[kSrc]);
+  int32_t* dst = at<int32_t>(ws, off[kDst]);
+  int32_t* row_token = at<int32_t>(ws, off[kRowToken]);
+  float* row_w = at<float>(ws, off[kRowW]);
+  int32_t* tok_offsets = at<int32_t>(ws, off[kTokOffsets]);
+  int32_t* tok_rows = at<int32_t>(ws, off[kTokRows]);
+  void* h = at<void>(ws, off[kH]);
+  void* ys = at<void>(ws, off[kYs]);
+  const int32_t* combine_offsets = nullptr;
+  const int32_t* combine_rows = dst;
+  if (s->round == MOE_ROUND_OFF) {
+    if ((st = moe_route_permute(s, x, Wr, bias, logits, idx, w, counts, offsets, src, dst, row_token, row_w, ws,
+                                ws_bytes, stream)) != MOE_OK)
+      return st;
+  } else {
+    if ((st = moe_route(s, x, Wr, bias, logits, idx, w, ws, stream)) != MOE_OK) return st;
+    if ((st = moe_token_round(s, logits, idx, counts, offsets, row_token, row_w, tok_offsets, tok_rows, ws, ws_bytes,
+                              stream)) != MOE_OK)
+      return st;
+    combine_offsets = tok_offsets;
+    combine_rows = tok_rows;
+  }
+  if ((st = moe_expert_up_fp8(s, x, W13q, sW13, counts, offsets, combine_offsets, combine_rows, h, ws, ws_bytes,
+                              stream)) != MOE_OK)
+    return st;
+  if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
+  return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
+}
+
 int moe_selftest_timeout(void* ws, uint64_t timeout_ns, void* stream) {
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
   if (cudaMemsetAsync(ws, 0, kStatusBytes, as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;

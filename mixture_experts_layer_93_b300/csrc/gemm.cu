@@ -37,7 +37,7 @@
 
 namespace moe {
 
-enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2 };
+enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3 };  // F8: e4m3 operands
 
 struct GemmParams {
   const int32_t* counts;     // [E] rows per group (ignored when single_rows > 0)
@@ -63,6 +63,8 @@ struct GemmParams {
   int64_t lda;
   int32_t* status;
   uint64_t timeout_ns;
+  const float* row_scale;    // F8 up: scale of each A row [cap]
+  const float* col_scale;    // F8 up: scale of each B row (output channel) [E * b_rows_per_expert]
 };
 
 constexpr int kProducerWarps = 4;
@@ -183,6 +185,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN, PAIR, EPI>;
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
+  constexpr bool kF8 = MODE == kModeUpF8;
+  static_assert(!kF8 || PAIR, "the e4m3 up-projection runs on SM pairs");
+  // K elements per operand stage: a stage row is 128 bytes (64 bf16 or 128 e4m3)
+  constexpr int KB_ELEMS = kF8 ? 128 : C::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -341,8 +347,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                 if (leader)
                   mbar_arrive_expect_tx(fb, p.gather == 2 ? 2 * C::B_BYTES
                                                           : 2 * C::STAGE_BYTES - (partner_empty ? C::A_BYTES : 0));
-                if (p.gather == 0 && rows_valid > 0) tma_load_2d_pair(a_dst, &tmA, kb * C::BK, row0, fb0, pol_a);
-                tma_load_2d_pair(b_dst, &tmB, kb * C::BK, brow, fb0, pol_b);
+                if (p.gather == 0 && rows_valid > 0) tma_load_2d_pair(a_dst, &tmA, kb * KB_ELEMS, row0, fb0, pol_a);
+                tma_load_2d_pair(b_dst, &tmB, kb * KB_ELEMS, brow, fb0, pol_b);
               }
             } else {
               if (lane == 0) mbar_arrive_expect_tx(fb, p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES);
@@ -378,7 +384,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kPer * C::BM, BN);
+      constexpr uint32_t idesc = kF8 ? idesc_e4m3_f32(kPer * C::BM, BN) : idesc_bf16_f32(kPer * C::BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -403,7 +409,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           for (int kk = 0; kk < C::BK / 16; ++kk) {
             const uint64_t ad = smem_desc_k128(a0 + kk * 32), bd = smem_desc_k128(b0 + kk * 32);
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-            if (PAIR)
+            if constexpr (kF8)  // 32 e4m3 of K per instruction: the same 32 bytes per row as 16 bf16
+              tc_mma_f8_pair(d_tmem, ad, bd, idesc, accum);
+            else if (PAIR)
               tc_mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
             else
               tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
@@ -498,8 +506,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     // gate weight of this thread's row in it) is fetched before this tile's
     // accumulator is waited for, so the load latency hides behind this tile.
     int dec_e = 0;  // group cursor of decode_tile
-    int nx_nb = 0, nx_row0 = 0, nx_rows = 0;
-    float nx_w = 0.f;
+    int nx_nb = 0, nx_row0 = 0, nx_rows = 0, nx_e = 0;
+    float nx_w = 0.f;  // down: gate weight; F8 up: row scale
     auto decode_next = [&](int t) {
       int mu, gstart, gcount;
       decode_tile<MODE == kModeRouter>(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
@@ -507,11 +515,13 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const int mb = unit_block(p.units, mu, rank, gcount);
       nx_row0 = gstart + mb * C::BM;
       nx_rows = min(C::BM, gcount - mb * C::BM);
+      nx_e = dec_e;
       if (MODE == kModeDown) nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] : 0.f;
+      if (kF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
     };
     if (unit0 < total_tiles) decode_next(unit0);
     for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
-      const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows;
+      const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows, e_tile = nx_e;
       const float wr = nx_w;
       if (tau + unit_stride < total_tiles) decode_next(tau + unit_stride);
       int w = 1;
@@ -525,23 +535,35 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
       const int warp_rows = max(0, min(32, rows_valid - ew * 32));
       const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
-      if constexpr (MODE == kModeUp) {
+      if constexpr (MODE == kModeUp || MODE == kModeUpF8) {
         // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile; accumulator
-        // columns 2j and 2j+1 hold the gate and linear branch of h column j
+        // columns 2j and 2j+1 hold the gate and linear branch of h column j.
+        // F8: the accumulator is a sum of code products; times the row's and
+        // the output channel's scale it is the product of the dequantised
+        // operands.  Lane l holds the two channel scales of h column c + l.
         constexpr int H = BN / 2;
         __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
+        const float* cs = kF8 ? p.col_scale + static_cast<int64_t>(e_tile) * p.b_rows_per_expert + nb * BN : nullptr;
 #pragma unroll 1
         for (int c = ch * (H / NCH); c < (ch + 1) * (H / NCH); c += 32) {
           uint32_t a[2][32];
           tmem_ld32(taddr + 2 * c, a[0]);
           tmem_ld32(taddr + 2 * c + 32, a[1]);
+          float2 sc = make_float2(1.f, 1.f);
+          if constexpr (kF8) sc = *reinterpret_cast<const float2*>(cs + 2 * (c + lane));
           tc_wait_ld();
           uint32_t o[16];
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const uint32_t* v = a[q >> 3] + 4 * (q & 7);
-            const float g0 = __uint_as_float(v[0]), u0 = __uint_as_float(v[1]);
-            const float g1 = __uint_as_float(v[2]), u1 = __uint_as_float(v[3]);
+            float g0 = __uint_as_float(v[0]), u0 = __uint_as_float(v[1]);
+            float g1 = __uint_as_float(v[2]), u1 = __uint_as_float(v[3]);
+            if constexpr (kF8) {
+              g0 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q);
+              u0 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q);
+              g1 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q + 1);
+              u1 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q + 1);
+            }
             const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
             const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
             o[q] = pack_bf16x2(h0, h1);
@@ -653,7 +675,7 @@ static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 template <int BN, int MODE, bool PAIR>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                        cudaStream_t stream) {
-  const bool wide = (MODE == kModeUp && p.num_kb <= 24) || (MODE == kModeDown && p.num_kb <= 8);
+  const bool wide = ((MODE == kModeUp || MODE == kModeUpF8) && p.num_kb <= 24) || (MODE == kModeDown && p.num_kb <= 8);
   if (MODE != kModeRouter && wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
   return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
 }
@@ -692,6 +714,19 @@ static bool make_map_16(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr,
 static bool make_map_bf16(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
   return make_map_16(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, inner, outer, 64, box_outer,
                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Operand tile of e4m3 codes: uint8 box [box_outer rows, 128], 128-byte swizzle.
+static bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Output tile for the epilogue's TMA stores: box [32 rows, 32], 64-byte swizzle.
@@ -876,6 +911,38 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   p.units = 0;
   if (BN == 256) return launch_gemm<256, kModeUp, false>(tmA, tmB, tmC, p, stream);
   return launch_gemm<128, kModeUp, false>(tmA, tmB, tmC, p, stream);
+}
+
+// e4m3 up-projection: the token-order gather quantises each x row once
+// (codes and a scale per row into the workspace), then the SM-pair GEMM runs
+// on the codes with kind::f8f6f4 and applies the row and channel scales in
+// the SwiGLU epilogue.  n % 128 == 0 and d % 128 == 0; odd last blocks run as
+// half-empty pairs.
+int launch_expert_up_f8(const __nv_bfloat16* x, const uint8_t* W13q, const float* sW13, const int32_t* counts,
+                        const int32_t* offsets, const int32_t* tok_rows, const int32_t* tok_offsets,
+                        __nv_bfloat16* h, int T, int d, int n, int E, int k, int64_t rows_cap, uint8_t* xq_scratch,
+                        float* row_scale, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  if (n % 128 != 0 || d % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  constexpr int BN = 256;
+  launch_gather_quant(x, tok_rows, tok_offsets, T, k, d, xq_scratch, row_scale, stream);
+  CUtensorMap tmA, tmB, tmC;
+  if (!make_map_u8(&tmA, xq_scratch, d, rows_cap, 128)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&tmB, W13q, d, static_cast<uint64_t>(E) * 2 * n, BN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_out(&tmC, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, n, rows_cap)) return MOE_ERR_CUDA;
+  GemmParams p = base_params(status, timeout_ns);
+  p.counts = counts;
+  p.offsets = offsets;
+  p.out_bf16 = h;
+  p.out_ld = n;
+  p.E = E;
+  p.num_kb = d / 128;
+  p.n_blocks = n / (BN / 2);
+  p.b_rows_per_expert = 2 * n;
+  p.gather = 0;
+  p.units = 3;
+  p.row_scale = row_scale;
+  p.col_scale = sW13;
+  return launch_gemm<BN, kModeUpF8, true>(tmA, tmB, tmC, p, stream);
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,

@@ -37,7 +37,17 @@ void launch_token_round(const float* logits, const int32_t* idx, int T, int E, i
                         uint32_t seed, int32_t* counts, int32_t* offsets, int32_t* row_token, float* row_w, int32_t* tok_offsets,
                         int32_t* tok_rows, void* scratch, int32_t* status, cudaStream_t stream);
 
+// fp8.cu
+void launch_quant_rows(const __nv_bfloat16* src, int64_t rows, int K, uint8_t* codes, float* scales,
+                       cudaStream_t stream);
+void launch_gather_quant(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T, int k,
+                         int d, uint8_t* xq, float* row_scale, cudaStream_t stream);
+
 // gemm.cu
+int launch_expert_up_f8(const __nv_bfloat16* x, const uint8_t* W13q, const float* sW13, const int32_t* counts,
+                        const int32_t* offsets, const int32_t* tok_rows, const int32_t* tok_offsets,
+                        __nv_bfloat16* h, int T, int d, int n, int E, int k, int64_t rows_cap, uint8_t* xq_scratch,
+                        float* row_scale, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const int32_t* counts,
                      const int32_t* offsets, const int32_t* row_token, const int32_t* tok_rows,
                      const int32_t* tok_offsets, __nv_bfloat16* h, int T, int d, int n, int E, int k,

@@ -51,9 +51,10 @@ Readings of the pages (where they are silent or at odds):
   * FP8 up-projection (the FP8 quantisation the pages name for MoE compute
     and communication, "硬件加速的考量", section 量化; they fix no recipe):
     e4m3 codes with one fp32 scale per activation row (token) and one per
-    weight output channel (a row of the packed W1/W3), scale =
-    fp32(amax / 448) (1 for an all-zero row) and code = e4m3(fp32(x / scale)),
-    rounded to nearest with ties to even and saturated to +-448.  The
+    weight output channel (a row of the packed W1/W3): scale =
+    fp32(amax / 448) and code = e4m3(fp32(x * fp32(448 / amax))), rounded to
+    nearest with ties to even and saturated to +-448 (an all-zero row has
+    scale 1 and codes 0).  The
     up-projection then runs on the dequantised values code * scale; routing
     and the down-projection stay as above.
 
@@ -370,15 +371,19 @@ def e4m3_round(v) -> np.ndarray:
 
 
 def quantize_rows_e4m3(X):
-    """(codes, scales) of each row of X: scale = fp32(amax / 448) (1 for an
-    all-zero row), code = e4m3(fp32(x / scale)); both divisions are fp32 with
-    round-to-nearest.  Codes are returned as their exact fp64 values."""
+    """(codes, scales) of each row of X: scale = fp32(amax / 448) and
+    code = e4m3(fp32(x * fp32(448 / amax))), every fp32 operation rounded to
+    nearest; an all-zero row has scale 1 and codes 0.  Codes are returned as
+    their exact fp64 values."""
     X32 = np.asarray(_f64(X), dtype=np.float32)
     amax = np.max(np.abs(X32), axis=1)
-    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
-    s = np.where(amax > 0, s, np.float32(1.0)).astype(np.float32)
-    v = (X32 / s[:, None]).astype(np.float32)
-    return e4m3_round(v.astype(F64)), s.astype(F64)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1.0)).astype(np.float32)
+    s = np.where(nz, (safe / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    inv = (np.float32(E4M3_MAX) / safe).astype(np.float32)
+    v = (X32 * inv[:, None]).astype(np.float32)
+    q = np.where(nz[:, None], e4m3_round(v.astype(F64)), 0.0)
+    return q, s.astype(F64)
 
 
 def dequantized_rows_e4m3(X) -> np.ndarray:
