@@ -221,6 +221,12 @@ def run_ours(args, world, rank, local):
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
     inp = I.make_inputs(cfg, device=dev, seed=rank)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    W13q = sW13 = None
+    if args.fp8:
+        # e4m3 up-projection: codes and one scale per packed weight row
+        W13q, sW13 = B.moe_quantize_rows_fp8(W13p)
+        del W13p
+        W13p = None
     inp_host = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -270,6 +276,8 @@ def run_ours(args, world, rank, local):
     # odd blocks are a small share (128 E <= 0.15 rows), else in a second one
     gemm_launches = 1 if 128.0 * E <= 0.15 * cap else 2
     up_launches = (1 + gemm_launches) if args.gather == 0 else (gemm_launches if d % 1 == 0 and n % 128 == 0 else 1)
+    if args.fp8:
+        up_launches = 2  # quantising gather + one SM-pair e4m3 GEMM
     route_launches = (5 if E <= 256 else 6) if mode == "off" else 3 + 9
     launches_per_step = route_launches + up_launches + gemm_launches + 1
 
@@ -296,8 +304,12 @@ def run_ours(args, world, rank, local):
                                     P(tok_offsets), P(tok_rows), ws.ptr, ws.nbytes, st), "round")
             c_off, c_rows = tok_offsets, tok_rows
         mark()
-        check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(c_off), P(c_rows), P(h),
-                              args.gather, ws.ptr, ws.nbytes, st), "up")
+        if args.fp8:
+            check(L.moe_expert_up_fp8(sp, P(x), P(W13q), P(sW13), P(counts), P(offsets), P(c_off), P(c_rows), P(h),
+                                      ws.ptr, ws.nbytes, st), "up_fp8")
+        else:
+            check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(c_off), P(c_rows),
+                                  P(h), args.gather, ws.ptr, ws.nbytes, st), "up")
         mark()
         check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,
                                 st), "down")
@@ -353,8 +365,12 @@ def run_ours(args, world, rank, local):
         st_b = streams[b]
         with torch.cuda.stream(st_b):
             x_dev[b].copy_(x_host[b], non_blocking=True)
-            check(L.moe_forward(sp, P(x_dev[b]), P(Wr), P(bias), P(W13p), P(W2p), P(y_dev[b]), wss[b].ptr,
-                                wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward")
+            if args.fp8:
+                check(L.moe_forward_fp8(sp, P(x_dev[b]), P(Wr), P(bias), P(W13q), P(sW13), P(W2p), P(y_dev[b]),
+                                        wss[b].ptr, wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward_fp8")
+            else:
+                check(L.moe_forward(sp, P(x_dev[b]), P(Wr), P(bias), P(W13p), P(W2p), P(y_dev[b]), wss[b].ptr,
+                                    wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward")
             y_host[b].copy_(y_dev[b], non_blocking=True)
 
     for i in range(max(2, args.warmup)):
@@ -389,12 +405,18 @@ def run_ours(args, world, rank, local):
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_t = burst
     peak_kind = "bf16_tflops (burst)"
-    roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up, SwiGLU>", "achieved": up_tflops,
-                "peak": peak_t, "unit": "TFLOP/s", "frac": up_tflops / peak_t,
+    up_peak, up_peak_kind = peak_t, peak_kind
+    if args.fp8:
+        # e4m3 contraction: the measured bf16 burst peak times the nominal
+        # dense e4m3 : bf16 ratio (4.5 : 2.25 PFLOP/s)
+        up_peak, up_peak_kind = 2.0 * burst, "bf16_tflops (burst) x 2 (nominal e4m3:bf16)"
+    roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up%s, SwiGLU>" % (" e4m3" if args.fp8 else ""),
+                "achieved": up_tflops, "peak": up_peak, "unit": "TFLOP/s", "frac": up_tflops / up_peak,
                 "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV))
-                if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) else None,
+                if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) and not args.fp8 else None,
                 "traffic_unit": "bytes per launch (ncu dram read+write)",
-                "peak_source": f"{peak_src} {peak_kind}", "frac_of_sustained": up_tflops / sustained,
+                "peak_source": f"{peak_src} {up_peak_kind}",
+                "frac_of_sustained": up_tflops / (sustained * up_peak / peak_t),
                 "algorithmic_flops_per_launch": up_flops}
     # HBM-bound stages: algorithmic bytes / time
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -411,9 +433,11 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 up / bf16" if args.fp8 else "bf16",
+        "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
                    "up_gather": ["gather_kernel+tma", "tma_gather4", "cp_async"][args.gather],
+                   "up_operands": "e4m3 (row and channel scales)" if args.fp8 else "bf16",
                    "tile": cfg.tile if mode != "off" else None,
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},
@@ -452,6 +476,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="e4m3 up-projection (moe_forward_fp8); the default measures the bf16 layer")
     ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
                     help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
                          "rows, 2 = per-lane cp.async of token rows")
