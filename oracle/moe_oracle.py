@@ -48,15 +48,16 @@ Readings of the pages (where they are silent or at odds):
     ordered by (L desc, id asc) and weighted by softmax over that set; an empty
     set gives y_t = 0.
 
-  * FP8 up-projection (the FP8 quantisation the pages name for MoE compute
+  * FP8 expert GEMMs (the FP8 quantisation the pages name for MoE compute
     and communication, "硬件加速的考量", section 量化; they fix no recipe):
-    e4m3 codes with one fp32 scale per activation row (token) and one per
-    weight output channel (a row of the packed W1/W3): scale =
+    e4m3 codes with one fp32 scale per quantised row, scale =
     fp32(amax / 448) and code = e4m3(fp32(x * fp32(448 / amax))), rounded to
     nearest with ties to even and saturated to +-448 (an all-zero row has
-    scale 1 and codes 0).  The
-    up-projection then runs on the dequantised values code * scale; routing
-    and the down-projection stay as above.
+    scale 1 and codes 0).  Up-projection: rows are tokens (activations) and
+    output channels (a row of the packed W1/W3).  Down-projection (the
+    "fp8" layer): rows of the bf16 hidden h (as the up-projection stores it)
+    and one row per expert for all of W2.  The GEMMs run on the dequantised
+    values code * scale; routing and the combine stay as above.
 
 Pins (tests/test_oracle.py): brute-force k-subset top-k; the closed form
 w0 = sigmoid(L0 - L1) at k=2; numpy's stable argsort for the permutation;
@@ -423,6 +424,49 @@ def moe_forward_fp8(x, Wr, bias, W1, W3, W2, k: int, tokens=None):
         W1h, W3h = quantized_expert_weights(W1[e], W3[e])
         h = expert_hidden(xq[pos], W1h, W3h)
         o = expert_out(h, W2[e])
+        np.add.at(y, pos, np.array(w_of[e])[:, None] * o)
+    return y
+
+
+def bf16_round(a) -> np.ndarray:
+    """Round fp64 values to bf16 (nearest, ties to even) and back: the
+    precision the hidden activations are stored in between the GEMMs."""
+    a = np.asarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(F64)
+
+
+def quantized_expert_down_weight(W2e) -> np.ndarray:
+    """W2e [n, d] as the FP8 down-projection uses it: one scale for the
+    whole expert, dequantised."""
+    W = _f64(W2e)
+    return dequantized_rows_e4m3(W.reshape(1, -1)).reshape(W.shape)
+
+
+def moe_forward_fp8_full(x, Wr, bias, W1, W3, W2, k: int, tokens=None):
+    """The layer with both expert GEMMs in e4m3: the up-projection as in
+    moe_forward_fp8; h rounded to bf16 (as stored), quantised per row, and
+    multiplied by the per-expert quantised W2.  fp64 result."""
+    tokens, sets, weights = route(x, Wr, bias, k, tokens=tokens)
+    x64 = _f64(x)
+    xq = dequantized_rows_e4m3(x64[tokens])
+    d = x64.shape[1]
+    y = np.zeros((len(tokens), d), dtype=F64)
+    E = W1.shape[0]
+    pos_of = {e: [] for e in range(E)}
+    w_of = {e: [] for e in range(E)}
+    for p, (st, w) in enumerate(zip(sets, weights)):
+        for e, we in zip(st, w):
+            pos_of[int(e)].append(p)
+            w_of[int(e)].append(we)
+    for e in range(E):
+        if not pos_of[e]:
+            continue
+        pos = np.array(pos_of[e], dtype=np.int64)
+        W1h, W3h = quantized_expert_weights(W1[e], W3[e])
+        h = dequantized_rows_e4m3(bf16_round(expert_hidden(xq[pos], W1h, W3h)))
+        o = expert_out(h, quantized_expert_down_weight(W2[e]))
         np.add.at(y, pos, np.array(w_of[e])[:, None] * o)
     return y
 

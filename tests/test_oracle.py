@@ -440,3 +440,46 @@ def test_fp8_forward_on_representable_inputs_equals_plain_forward():
     # quantising W rows (over n) instead of columns gives a different layer
     bad = [O.dequantized_rows_e4m3(W1[e]) for e in range(E)]
     assert not all(np.allclose(b, O.quantized_expert_weights(W1[e], W3[e])[0]) for e, b in enumerate(bad))
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(5)
+    a = np.concatenate([rng.standard_normal(20000) * 10 ** rng.uniform(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0]])
+    ref = torch.from_numpy(a).to(torch.float32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(O.bf16_round(a), ref)
+
+
+def test_fp8_down_weight_one_scale_per_expert():
+    rng = np.random.default_rng(8)
+    W = rng.standard_normal((24, 40)) / 5
+    Wh = O.quantized_expert_down_weight(W)
+    s = np.float32(np.abs(W).max()) / np.float32(448)
+    codes = Wh / np.float64(np.float32(s))
+    assert np.abs(np.abs(codes).max() - 448) < 1e-3
+    assert np.all(np.abs(Wh - W) <= 2.0 ** -4 * np.abs(W) + 2.0 ** -9 * float(s) + 1e-12)
+
+
+def test_fp8_full_layer_within_quantisation_bound_of_fp8_up_layer():
+    """Quantising h per row and W2 per expert moves each output by at most the
+    e4m3 half-step of both factors: |dy| <= sum_e w_e (|h_e| |W2_e|) * 2^-3 (+ tiny)."""
+    rng = np.random.default_rng(4)
+    T, d, n, E, k = 30, 48, 40, 5, 2
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((d, E)) / np.sqrt(d)
+    W1 = rng.standard_normal((E, d, n)) / np.sqrt(d)
+    W3 = rng.standard_normal((E, d, n)) / np.sqrt(d)
+    W2 = rng.standard_normal((E, n, d)) / np.sqrt(n)
+    y8 = O.moe_forward_fp8(x, Wr, None, W1, W3, W2, k)
+    y8f = O.moe_forward_fp8_full(x, Wr, None, W1, W3, W2, k)
+    _, sets, weights = O.route(x, Wr, None, k)
+    xq = O.dequantized_rows_e4m3(x)
+    bound = np.zeros((T, d))
+    for t in range(T):
+        for e, w in zip(sets[t], weights[t]):
+            W1h, W3h = O.quantized_expert_weights(W1[e], W3[e])
+            h = O.expert_hidden(xq[t:t + 1], W1h, W3h)
+            bound[t] += w * (np.abs(h) @ np.abs(W2[e]))[0]
+    diff = np.abs(y8f - y8)
+    assert np.all(diff <= 2.0 ** -3 * bound + 1e-9)
+    assert diff.max() > 0  # the down-projection really is quantised
