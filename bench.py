@@ -221,19 +221,20 @@ def run_ours(args, world, rank, local):
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
     inp = I.make_inputs(cfg, device=dev, seed=rank)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
-    W13q = sW13 = None
+    W13q = sW13 = W2q = sW2 = None
     if args.fp8:
-        # e4m3 up-projection: codes and one scale per packed weight row
+        # e4m3 GEMMs: codes with one scale per packed W1/W3 row and one per expert of W2
         W13q, sW13 = B.moe_quantize_rows_fp8(W13p)
-        del W13p
-        W13p = None
+        W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+        del W13p, W2p
+        W13p = W2p = None
     inp_host = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp_host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     del inp["W1"], inp["W3"], inp["W2"]
     torch.cuda.empty_cache()
     x, Wr, bias = inp["x"], inp["Wr"], inp["bias"]
-    ws = B.Workspace(shape, dev)
+    ws = B.Workspace(shape, dev, fp8=args.fp8)
     lay = B.moe_workspace_layout(shape)
     cap = B.moe_row_capacity(shape)
     T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
@@ -278,6 +279,7 @@ def run_ours(args, world, rank, local):
     up_launches = (1 + gemm_launches) if args.gather == 0 else (gemm_launches if d % 1 == 0 and n % 128 == 0 else 1)
     if args.fp8:
         up_launches = 2  # quantising gather + one SM-pair e4m3 GEMM
+        gemm_launches = 2  # down: h quantisation + one SM-pair e4m3 GEMM
     route_launches = (5 if E <= 256 else 6) if mode == "off" else 3 + 9
     launches_per_step = route_launches + up_launches + gemm_launches + 1
 
@@ -311,8 +313,12 @@ def run_ours(args, world, rank, local):
             check(L.moe_expert_up(sp, P(x), P(W13p), P(counts), P(offsets), P(row_token), P(c_off), P(c_rows),
                                   P(h), args.gather, ws.ptr, ws.nbytes, st), "up")
         mark()
-        check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,
-                                st), "down")
+        if args.fp8:
+            check(L.moe_expert_down_fp8(sp, P(h), P(W2q), P(sW2), P(counts), P(offsets), P(row_w), P(ys), ws.ptr,
+                                        ws.nbytes, st), "down_fp8")
+        else:
+            check(L.moe_expert_down(sp, P(h), P(W2p), P(counts), P(offsets), P(row_w), P(ys), ws.ptr, ws.nbytes,
+                                    st), "down")
         mark()
         check(L.moe_combine(sp, P(ys), P(c_off), P(c_rows), P(y), st), "combine")
         mark()
@@ -352,7 +358,7 @@ def run_ours(args, world, rank, local):
     # compute, as a serving loop would run them.
     x_cpu = x.cpu()
     streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    wss = [ws, B.Workspace(shape, dev)]
+    wss = [ws, B.Workspace(shape, dev, fp8=args.fp8)]
     x_host = [torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     y_host = [torch.empty(T, d, dtype=torch.float32, pin_memory=True) for _ in range(2)]
     for xh in x_host:
@@ -366,8 +372,9 @@ def run_ours(args, world, rank, local):
         with torch.cuda.stream(st_b):
             x_dev[b].copy_(x_host[b], non_blocking=True)
             if args.fp8:
-                check(L.moe_forward_fp8(sp, P(x_dev[b]), P(Wr), P(bias), P(W13q), P(sW13), P(W2p), P(y_dev[b]),
-                                        wss[b].ptr, wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward_fp8")
+                check(L.moe_forward_fp8(sp, P(x_dev[b]), P(Wr), P(bias), P(W13q), P(sW13), P(W2q), P(sW2),
+                                        P(y_dev[b]), wss[b].ptr, wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)),
+                      "forward_fp8")
             else:
                 check(L.moe_forward(sp, P(x_dev[b]), P(Wr), P(bias), P(W13p), P(W2p), P(y_dev[b]), wss[b].ptr,
                                     wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward")
@@ -433,11 +440,12 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 up / bf16" if args.fp8 else "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 expert GEMMs" if args.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
                    "up_gather": ["gather_kernel+tma", "tma_gather4", "cp_async"][args.gather],
-                   "up_operands": "e4m3 (row and channel scales)" if args.fp8 else "bf16",
+                   "expert_gemm_operands": "e4m3 (x per token, W1/W3 per channel, h per row, W2 per expert)"
+                   if args.fp8 else "bf16",
                    "tile": cfg.tile if mode != "off" else None,
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},
@@ -477,7 +485,7 @@ def main():
     ap.add_argument("--reference-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
-                    help="e4m3 up-projection (moe_forward_fp8); the default measures the bf16 layer")
+                    help="e4m3 expert GEMMs (moe_forward_fp8); the default measures the bf16 layer")
     ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
                     help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
                          "rows, 2 = per-lane cp.async of token rows")

@@ -266,12 +266,19 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
 int moe_workspace_layout(const moe_shape* s, int64_t* offsets_out, int32_t n_out);
 
 /* ---------------------------------------------------------------- FP8 ---
- * e4m3 up-projection.  The pages name FP8 among the precisions MoE compute
+ * e4m3 expert GEMMs.  The pages name FP8 among the precisions MoE compute
  * runs in ("硬件加速的考量", section 量化) without a recipe; reading: one fp32
- * scale per row (a token, or one output channel of the packed gate / linear
- * weights), scale = fp32(amax / 448), code = e4m3(fp32(x * fp32(448 / amax)))
- * rounded to nearest-even and saturated to +-448; an all-zero row has scale 1
- * and codes 0.  Routing and the down-projection stay as in moe_forward. */
+ * scale per quantised row, scale = fp32(amax / 448), code =
+ * e4m3(fp32(x * fp32(448 / amax))) rounded to nearest-even and saturated to
+ * +-448; an all-zero row has scale 1 and codes 0.  Rows: tokens and the
+ * output channels of the packed gate / linear weights (up-projection), rows
+ * of the bf16 hidden h and one row per expert for all of W2
+ * (down-projection).  Routing and the combine stay as in moe_forward. */
+
+/* Workspace bytes of the FP8 entry points that quantise h
+ * (moe_expert_down_fp8, moe_forward_fp8): moe_workspace_bytes plus the e4m3
+ * codes of h and one scale per row. */
+size_t moe_workspace_bytes_fp8(const moe_shape* s);
 
 /* codes[rows, K] (e4m3 bytes) and scales[rows] fp32 of src[rows, K] bf16.
  * K % 16 == 0; src and codes 16-byte aligned.  For the weights, src is W13p
@@ -290,10 +297,28 @@ int moe_expert_up_fp8(const moe_shape* s, const void* x, const void* W13q, const
                       const int32_t* counts, const int32_t* offsets, const int32_t* tok_offsets,
                       const int32_t* tok_rows, void* h, void* ws, size_t ws_bytes, void* stream);
 
-/* moe_forward with the e4m3 up-projection (moe_expert_up_fp8); W2p bf16. */
+/* codes[E, m] and scales[E] with one scale per row of m elements (a whole
+ * expert: W2p from moe_prepare_weights viewed as [E, d * n]).  m % 16 == 0. */
+int moe_quantize_experts_fp8(const void* src, int32_t E, int64_t m, void* codes, float* scales,
+                             void* stream);
+
+/* Down-projection with e4m3 operands: h [moe_row_capacity, n] bf16 (as
+ * moe_expert_up writes it) is quantised per row into the workspace
+ * (moe_workspace_bytes_fp8), then ys[row] = w[row] * (code_h . code_W2) *
+ * scale_h[row] * scale_W2[e] in fp32 (kind::f8f6f4 on SM pairs), stored fp16
+ * as moe_expert_down (saturation reported alike).  W2q / sW2 from
+ * moe_quantize_experts_fp8 of W2p.  Requires n % 128 == 0 and d % 256 == 0
+ * (else MOE_ERR_UNSUPPORTED). */
+int moe_expert_down_fp8(const moe_shape* s, const void* h, const void* W2q, const float* sW2,
+                        const int32_t* counts, const int32_t* offsets, const float* row_w, void* ys,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward with both expert GEMMs in e4m3 (moe_expert_up_fp8,
+ * moe_expert_down_fp8).  ws_bytes >= moe_workspace_bytes_fp8(s); n % 128 ==
+ * 0 and d % 256 == 0. */
 int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const float* bias,
-                    const void* W13q, const float* sW13, const void* W2p, void* y, void* ws,
-                    size_t ws_bytes, void* stream);
+                    const void* W13q, const float* sW13, const void* W2q, const float* sW2,
+                    void* y, void* ws, size_t ws_bytes, void* stream);
 
 /* Self-test of the bounded-wait machinery: launches one block that waits on a
  * device flag nobody sets, giving up after `timeout_ns` nanoseconds; the

@@ -66,7 +66,10 @@ _SIGNATURES = {
     "moe_route_permute": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_quantize_rows_fp8": (_I, [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P]),
     "moe_expert_up_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_forward_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_experts_fp8": (_I, [_P, ctypes.c_int32, ctypes.c_int64, _P, _P, _P]),
+    "moe_expert_down_fp8": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_workspace_bytes_fp8": (_SZ, [_SHP]),
     "moe_permute_noalloc": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_token_round": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
@@ -149,8 +152,8 @@ def moe_workspace_layout(shape: moe_shape) -> dict:
 class Workspace:
     """Device workspace for one shape (status block zeroed at creation)."""
 
-    def __init__(self, shape: moe_shape, device="cuda"):
-        nbytes = moe_workspace_bytes(shape)
+    def __init__(self, shape: moe_shape, device="cuda", fp8: bool = False):
+        nbytes = moe_workspace_bytes_fp8(shape) if fp8 else moe_workspace_bytes(shape)
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID, "moe_workspace_bytes")
         self.shape = shape
@@ -298,12 +301,41 @@ def moe_expert_up_fp8(shape: moe_shape, x, W13q, sW13, counts, offsets, tok_rows
     return h
 
 
-def moe_forward_fp8(shape: moe_shape, x, Wr, bias, W13q, sW13, W2p, ws: Workspace, y=None):
-    _need_cuda(x, Wr, bias, W13q, sW13, W2p)
+def moe_quantize_experts_fp8(src):
+    """(codes uint8, scales fp32 [E]) of a bf16 [E, ...] tensor with one scale
+    per expert (leading dimension)."""
+    _need_cuda(src)
+    src = src.contiguous()
+    E = src.shape[0]
+    m = src.numel() // E
+    codes = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scales = torch.empty(E, dtype=torch.float32, device=src.device)
+    _check(lib().moe_quantize_experts_fp8(_ptr(src), E, m, _ptr(codes), _ptr(scales), _stream(src.device)),
+           "moe_quantize_experts_fp8")
+    return codes, scales
+
+
+def moe_workspace_bytes_fp8(shape: moe_shape) -> int:
+    return int(lib().moe_workspace_bytes_fp8(ctypes.byref(shape)))
+
+
+def moe_expert_down_fp8(shape: moe_shape, h, W2q, sW2, counts, offsets, row_w, ws: Workspace, ys=None):
+    _need_cuda(h, W2q, sW2, counts, offsets, row_w)
+    if ys is None:
+        ys = torch.empty(moe_row_capacity(shape), shape.d, dtype=torch.float16, device=h.device)
+    _check(lib().moe_expert_down_fp8(ctypes.byref(shape), _ptr(h), _ptr(W2q), _ptr(sW2), _ptr(counts), _ptr(offsets),
+                                     _ptr(row_w), _ptr(ys), ws.ptr, ws.nbytes, _stream(h.device)),
+           "moe_expert_down_fp8")
+    return ys
+
+
+def moe_forward_fp8(shape: moe_shape, x, Wr, bias, W13q, sW13, W2q, sW2, ws: Workspace, y=None):
+    _need_cuda(x, Wr, bias, W13q, sW13, W2q, sW2)
     if y is None:
         y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=x.device)
     _check(lib().moe_forward_fp8(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13q), _ptr(sW13),
-                                 _ptr(W2p), _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward_fp8")
+                                 _ptr(W2q), _ptr(sW2), _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)),
+           "moe_forward_fp8")
     return y
 
 

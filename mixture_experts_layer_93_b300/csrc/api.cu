@@ -35,18 +35,20 @@ inline int64_t align256(int64_t v) { return (v + 255) & ~int64_t(255); }
 
 enum Slot {
   kLogits, kTopkIdx, kTopkW, kCounts, kOffsets, kSrc, kDst, kRowToken, kRowW, kTokOffsets, kTokRows, kH, kYs,
-  kPermHist, kRoundScratch, kRouterW, kNumSlots
+  kPermHist, kRoundScratch, kRouterW, kHq, kNumSlots
 };
 
-// Byte offsets of each array in the workspace; returns the total size.
-int64_t layout(const moe_shape* s, int64_t* off) {
+// Byte offsets of each array in the workspace; returns the total size.  The
+// last slot (e4m3 codes of h and their row scales) only counts with fp8.
+int64_t layout(const moe_shape* s, int64_t* off, bool fp8 = false) {
   const int64_t T = s->T, E = s->E, A = T * s->k, cap = row_cap(s);
   const int64_t sizes[kNumSlots] = {
       T * E * 4,          A * 4,     A * 4,     E * 4,   (E + 1) * 4,       cap * 4,
       A * 4,              cap * 4,   cap * 4,   (T + 1) * 4, cap * 4,       cap * s->n * 2,
       cap * s->d * 2,     E * perm_num_chunks(cap) * 4,
       s->round != MOE_ROUND_OFF ? static_cast<int64_t>(round_scratch_bytes(s->T, s->E, s->k, s->tile)) : 0,
-      static_cast<int64_t>(router_split_elems(s->d, s->E)) * 2};
+      static_cast<int64_t>(router_split_elems(s->d, s->E)) * 2,
+      fp8 ? align256(cap * s->n) + cap * 4 : 0};
   int64_t pos = static_cast<int64_t>(kStatusBytes);
   for (int i = 0; i < kNumSlots; ++i) {
     off[i] = pos;
@@ -69,10 +71,10 @@ inline int32_t* status_of(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 // A-operand path moe_forward uses for the up-projection (see moe_expert_up).
 constexpr int kForwardGather = 0;
 
-int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
+int check_ws(const moe_shape* s, void* ws, size_t ws_bytes, bool fp8 = false) {
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
   int64_t off[kNumSlots];
-  if (static_cast<int64_t>(ws_bytes) < layout(s, off)) return MOE_ERR_WORKSPACE;
+  if (static_cast<int64_t>(ws_bytes) < layout(s, off, fp8)) return MOE_ERR_WORKSPACE;
   return MOE_OK;
 }
 
@@ -86,6 +88,12 @@ size_t moe_workspace_bytes(const moe_shape* s) {
   if (!shape_ok(s)) return 0;
   int64_t off[kNumSlots];
   return static_cast<size_t>(layout(s, off));
+}
+
+size_t moe_workspace_bytes_fp8(const moe_shape* s) {
+  if (!shape_ok(s)) return 0;
+  int64_t off[kNumSlots];
+  return static_cast<size_t>(layout(s, off, true));
 }
 
 int moe_workspace_layout(const moe_shape* s, int64_t* out, int32_t n_out) {
@@ -333,12 +341,41 @@ int moe_expert_up_fp8(const moe_shape* s, const void* x, const void* W13q, const
                              s->k, cap, xq, row_scale, status_of(ws), kDefaultTimeoutNs, as_stream(stream));
 }
 
+int moe_quantize_experts_fp8(const void* src, int32_t E, int64_t m, void* codes, float* scales, void* stream) {
+  if (!src || !codes || !scales || E <= 0 || m <= 0 || m % 16 != 0) return MOE_ERR_INVALID;
+  if (!aligned16(src) || !aligned16(codes)) return MOE_ERR_INVALID;
+  launch_quant_experts(static_cast<const __nv_bfloat16*>(src), E, m, static_cast<uint8_t*>(codes), scales,
+                       as_stream(stream));
+  return last_launch();
+}
+
+int moe_expert_down_fp8(const moe_shape* s, const void* h, const void* W2q, const float* sW2, const int32_t* counts,
+                        const int32_t* offsets, const float* row_w, void* ys, void* ws, size_t ws_bytes,
+                        void* stream) {
+  if (!shape_ok(s) || !h || !W2q || !sW2 || !counts || !offsets || !row_w || !ys) return MOE_ERR_INVALID;
+  if (!aligned16(h) || !aligned16(W2q) || !aligned16(ys)) return MOE_ERR_INVALID;
+  if (s->n % 128 != 0 || s->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  const int st = check_ws(s, ws, ws_bytes, true);
+  if (st != MOE_OK) return st;
+  int64_t off[kNumSlots];
+  layout(s, off, true);
+  const int64_t cap = row_cap(s);
+  uint8_t* hq = at<uint8_t>(ws, off[kHq]);
+  float* h_scale = reinterpret_cast<float*>(hq + align256(cap * s->n));
+  launch_quant_rows(static_cast<const __nv_bfloat16*>(h), cap, s->n, hq, h_scale, as_stream(stream));
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_expert_down_f8(hq, h_scale, static_cast<const uint8_t*>(W2q), sW2, counts, offsets, row_w,
+                               static_cast<__half*>(ys), s->d, s->n, s->E, cap, status_of(ws), kDefaultTimeoutNs,
+                               as_stream(stream));
+}
+
 int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13q,
-                    const float* sW13, const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
-  if (!shape_ok(s) || !x || !Wr || !W13q || !sW13 || !W2p || !y) return MOE_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(W13q) || !aligned16(W2p) || !aligned16(y)) return MOE_ERR_INVALID;
-  if (s->n % 128 != 0 || s->d % 128 != 0) return MOE_ERR_UNSUPPORTED;
-  int st = check_ws(s, ws, ws_bytes);
+                    const float* sW13, const void* W2q, const float* sW2, void* y, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !W13q || !sW13 || !W2q || !sW2 || !y) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13q) || !aligned16(W2q) || !aligned16(y)) return MOE_ERR_INVALID;
+  if (s->n % 128 != 0 || s->d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  int st = check_ws(s, ws, ws_bytes, true);
   if (st != MOE_OK) return st;
   int64_t off[kNumSlots];
   layout(s, off);
@@ -372,7 +409,8 @@ int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const fl
   if ((st = moe_expert_up_fp8(s, x, W13q, sW13, counts, offsets, combine_offsets, combine_rows, h, ws, ws_bytes,
                               stream)) != MOE_OK)
     return st;
-  if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
+  if ((st = moe_expert_down_fp8(s, h, W2q, sW2, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK)
+    return st;
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
 }
 

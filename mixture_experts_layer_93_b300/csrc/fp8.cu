@@ -7,6 +7,8 @@
 // amax))) with round-to-nearest-even and saturation to +-448; an all-zero row
 // has scale 1 and codes 0.  Every fp32 operation is IEEE round-to-nearest
 // (explicit _rn intrinsics, so no contraction changes a bit).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -104,6 +106,71 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16* 
 void launch_gather_quant(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T, int k,
                          int d, uint8_t* xq, float* row_scale, cudaStream_t stream) {
   launch_pdl(gather_quant_kernel, (T + 7) / 8, 256, 0, stream, 1, x, tok_rows, tok_offsets, T, k, d, xq, row_scale);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// One scale for each of E rows of m elements (a whole expert's W2): the
+// maximum |x| over many blocks by atomicMax on the bits of non-negative
+// floats (their order is the unsigned order of the bits; the result does not
+// depend on the order of the updates), then the codes, then the scales.
+__global__ void __launch_bounds__(256) quant_expert_amax_kernel(const __nv_bfloat16* __restrict__ src, int64_t m,
+                                                                uint32_t* __restrict__ amax_bits) {
+  pdl_wait();
+  pdl_trigger();
+  const int e = blockIdx.y;
+  const uint4* r4 = reinterpret_cast<const uint4*>(src + static_cast<int64_t>(e) * m);
+  float a = 0.f;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < m / 8;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = __ldg(r4 + g);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a = fmaxf(a, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(&amax_bits[e], __float_as_uint(a));
+}
+
+__global__ void __launch_bounds__(256) quant_expert_codes_kernel(const __nv_bfloat16* __restrict__ src, int64_t m,
+                                                                 const uint32_t* __restrict__ amax_bits,
+                                                                 uint8_t* __restrict__ codes) {
+  pdl_wait();
+  pdl_trigger();
+  const int e = blockIdx.y;
+  float scale, inv;
+  row_scales(__uint_as_float(amax_bits[e]), scale, inv);
+  const __nv_bfloat16* row = src + static_cast<int64_t>(e) * m;
+  uint2* out = reinterpret_cast<uint2*>(codes + static_cast<int64_t>(e) * m);
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < m / 8;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[g] = codes8(row, static_cast<int>(g), inv);
+}
+
+__global__ void quant_expert_scale_kernel(int E, uint32_t* __restrict__ amax_bits_in_scales) {
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float scale, inv;
+    row_scales(__uint_as_float(amax_bits_in_scales[e]), scale, inv);
+    amax_bits_in_scales[e] = __float_as_uint(scale);
+  }
+}
+
+// scales doubles as the amax buffer until the last kernel turns it into scales.
+void launch_quant_experts(const __nv_bfloat16* src, int E, int64_t m, uint8_t* codes, float* scales,
+                          cudaStream_t stream) {
+  uint32_t* bits = reinterpret_cast<uint32_t*>(scales);
+  cudaMemsetAsync(bits, 0, static_cast<size_t>(E) * sizeof(uint32_t), stream);
+  const int64_t groups = m / 8;
+  const unsigned bx = static_cast<unsigned>(std::min<int64_t>((groups + 255) / 256, 1024));
+  launch_pdl(quant_expert_amax_kernel, dim3(bx, E), 256, 0, stream, 1, src, m, bits);
+  launch_pdl(quant_expert_codes_kernel, dim3(bx, E), 256, 0, stream, 1, src, m,
+             static_cast<const uint32_t*>(bits), codes);
+  launch_pdl(quant_expert_scale_kernel, 1, 256, 0, stream, 1, E, bits);
 }
 
 }  // namespace moe

@@ -37,7 +37,7 @@
 
 namespace moe {
 
-enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3 };  // F8: e4m3 operands
+enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3, kModeDownF8 = 4 };  // F8: e4m3
 
 struct GemmParams {
   const int32_t* counts;     // [E] rows per group (ignored when single_rows > 0)
@@ -63,8 +63,9 @@ struct GemmParams {
   int64_t lda;
   int32_t* status;
   uint64_t timeout_ns;
-  const float* row_scale;    // F8 up: scale of each A row [cap]
-  const float* col_scale;    // F8 up: scale of each B row (output channel) [E * b_rows_per_expert]
+  const float* row_scale;    // F8: scale of each A row [cap]
+  const float* col_scale;    // F8 up: scale of each B row (output channel) [E * b_rows_per_expert];
+                             // F8 down: one scale per expert [E]
 };
 
 constexpr int kProducerWarps = 4;
@@ -185,8 +186,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN, PAIR, EPI>;
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
-  constexpr bool kF8 = MODE == kModeUpF8;
-  static_assert(!kF8 || PAIR, "the e4m3 up-projection runs on SM pairs");
+  constexpr bool kF8 = MODE == kModeUpF8 || MODE == kModeDownF8;
+  constexpr bool kDown = MODE == kModeDown || MODE == kModeDownF8;
+  static_assert(!kF8 || PAIR, "the e4m3 GEMMs run on SM pairs");
   // K elements per operand stage: a stage row is 128 bytes (64 bf16 or 128 e4m3)
   constexpr int KB_ELEMS = kF8 ? 128 : C::BK;
   extern __shared__ uint8_t smem_raw[];
@@ -517,7 +519,12 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       nx_rows = min(C::BM, gcount - mb * C::BM);
       nx_e = dec_e;
       if (MODE == kModeDown) nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] : 0.f;
-      if (kF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
+      if (MODE == kModeUpF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
+      // F8 down: the gate weight times the row's and the expert's scales
+      if (MODE == kModeDownF8)
+        nx_w = r_in_tile < nx_rows
+                   ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] * p.col_scale[dec_e]
+                   : 0.f;
     };
     if (unit0 < total_tiles) decode_next(unit0);
     for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
@@ -570,7 +577,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           }
           if (warp_rows > 0) store_chunk(o, nb * H + c, row_w0, warp_rows, row, dst + c);
         }
-      } else if constexpr (MODE == kModeDown) {
+      } else if constexpr (kDown) {
         // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
         // same traffic); values past the fp16 range saturate and are reported
         // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait.
@@ -675,7 +682,8 @@ static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 template <int BN, int MODE, bool PAIR>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                        cudaStream_t stream) {
-  const bool wide = ((MODE == kModeUp || MODE == kModeUpF8) && p.num_kb <= 24) || (MODE == kModeDown && p.num_kb <= 8);
+  const bool wide = ((MODE == kModeUp || MODE == kModeUpF8) && p.num_kb <= 24) ||
+                    ((MODE == kModeDown || MODE == kModeDownF8) && p.num_kb <= 8);
   if (MODE != kModeRouter && wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
   return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
 }
@@ -943,6 +951,37 @@ int launch_expert_up_f8(const __nv_bfloat16* x, const uint8_t* W13q, const float
   p.row_scale = row_scale;
   p.col_scale = sW13;
   return launch_gemm<BN, kModeUpF8, true>(tmA, tmB, tmC, p, stream);
+}
+
+// e4m3 down-projection: hq [cap, n] codes with one scale per row, W2q
+// [E * d, n] codes with one scale per expert; the epilogue multiplies by the
+// gate weight times both scales and stores fp16 ys as the bf16 path.  n % 128
+// == 0 and d % 256 == 0; odd last blocks run as half-empty pairs.
+int launch_expert_down_f8(const uint8_t* hq, const float* h_scale, const uint8_t* W2q, const float* sW2,
+                          const int32_t* counts, const int32_t* offsets, const float* row_w, __half* ys, int d,
+                          int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns,
+                          cudaStream_t stream) {
+  if (n % 128 != 0 || d % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  constexpr int BN = 256;
+  CUtensorMap tmA, tmB, tmC;
+  if (!make_map_u8(&tmA, hq, n, rows_cap, 128)) return MOE_ERR_CUDA;
+  if (!make_map_u8(&tmB, W2q, n, static_cast<uint64_t>(E) * d, BN / 2)) return MOE_ERR_CUDA;
+  if (!make_map_out(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ys, d, rows_cap)) return MOE_ERR_CUDA;
+  GemmParams p = base_params(status, timeout_ns);
+  p.counts = counts;
+  p.offsets = offsets;
+  p.row_w = row_w;
+  p.out_f16 = ys;
+  p.out_ld = d;
+  p.E = E;
+  p.num_kb = n / 128;
+  p.n_blocks = d / BN;
+  p.b_rows_per_expert = d;
+  p.gather = 0;
+  p.units = 3;
+  p.row_scale = h_scale;
+  p.col_scale = sW2;
+  return launch_gemm<BN, kModeDownF8, true>(tmA, tmB, tmC, p, stream);
 }
 
 int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,

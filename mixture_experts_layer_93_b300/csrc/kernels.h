@@ -42,6 +42,11 @@ void launch_quant_rows(const __nv_bfloat16* src, int64_t rows, int K, uint8_t* c
                        cudaStream_t stream);
 void launch_gather_quant(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T, int k,
                          int d, uint8_t* xq, float* row_scale, cudaStream_t stream);
+void launch_quant_experts(const __nv_bfloat16* src, int E, int64_t m, uint8_t* codes, float* scales,
+                          cudaStream_t stream);
+int launch_expert_down_f8(const uint8_t* hq, const float* h_scale, const uint8_t* W2q, const float* sW2,
+                          const int32_t* counts, const int32_t* offsets, const float* row_w, __half* ys, int d,
+                          int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 
 // gemm.cu
 int launch_expert_up_f8(const __nv_bfloat16* x, const uint8_t* W13q, const float* sW13, const int32_t* counts,

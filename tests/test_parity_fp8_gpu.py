@@ -94,14 +94,61 @@ def test_expert_up_fp8_rejects_unsupported(cuda_device):
     del cfg
 
 
+@pytest.mark.parametrize("E,d,n", [(3, 256, 128), (8, 512, 256), (1, 128, 128)])
+def test_quantize_experts_bit_exact(cuda_device, E, d, n):
+    g = torch.Generator().manual_seed(E + d + n)
+    W = (torch.randn(E, d, n, generator=g) * torch.pow(10.0, torch.empty(E, 1, 1).uniform_(-2, 2, generator=g)))
+    W = W.to(torch.bfloat16)
+    codes, scales = B.moe_quantize_experts_fp8(W.to(cuda_device))
+    for e in range(E):
+        q_ref, s_ref = O.quantize_rows_e4m3(W[e].float().reshape(1, -1).numpy())
+        assert np.array_equal(decode_e4m3(codes[e].cpu().numpy().reshape(1, -1)), q_ref)
+        assert float(scales[e]) == float(s_ref[0])
+
+
+@pytest.mark.parametrize("T,d,n,E,k", [(700, 256, 128, 6, 2), (600, 512, 256, 5, 3), (2000, 256, 384, 3, 2)])
+def test_expert_down_fp8(cuda_device, T, d, n, E, k):
+    """ys = w * (dequantised h row) @ (dequantised W2) within one fp16 rounding:
+    the GPU quantises the same bf16 h, so the codes are the oracle's."""
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=d + n)
+    counts, offsets, src, dst = _routing(T, E, k, seed=T + 2)
+    A = T * k
+    g = torch.Generator(device="cpu").manual_seed(9)
+    s = B.make_shape(T, d, n, E, k)
+    ws = B.Workspace(s, cuda_device, fp8=True)
+    cap = B.moe_row_capacity(s)
+    hcap = torch.zeros(cap, n, dtype=torch.bfloat16)
+    hcap[:A] = torch.randn(A, n, generator=g).to(torch.bfloat16)
+    wcap = torch.zeros(cap)
+    wcap[:A] = torch.rand(A, generator=g)
+    _, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+    ys = B.moe_expert_down_fp8(s, hcap.to(cuda_device), W2q, sW2,
+                               torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
+                               torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap.to(cuda_device), ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    hh = O.dequantized_rows_e4m3(hcap[:A].float().numpy())
+    ref = np.zeros((A, d))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            ref[r0:r1] = wcap[r0:r1].double().numpy()[:, None] * (hh[r0:r1] @ O.quantized_expert_down_weight(
+                inp["W2"][e]))
+    got = to64(ys[:A])
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-5 * rms), err_stats(got, ref)
+
+
 def _forward_fp8_and_check(cfg, dev, seed=0, tokens=None):
     inp = I.make_inputs(cfg, device=dev, seed=seed)
     s = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k)
-    ws = B.Workspace(s, dev)
+    ws = B.Workspace(s, dev, fp8=True)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     W13q, sW13 = B.moe_quantize_rows_fp8(W13p)
-    del W13p
-    y = B.moe_forward_fp8(s, inp["x"], inp["Wr"], inp["bias"], W13q, sW13, W2p, ws)
+    W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+    del W13p, W2p
+    y = B.moe_forward_fp8(s, inp["x"], inp["Wr"], inp["bias"], W13q, sW13, W2q, sW2, ws)
     assert B.moe_check_device_status(ws) == B.MOE_OK
     T = cfg.T
     toks = np.arange(T) if tokens is None else np.asarray(tokens)
@@ -113,8 +160,8 @@ def _forward_fp8_and_check(cfg, dev, seed=0, tokens=None):
     for i in np.flatnonzero(~robust):
         assert valid_topk(L64[i], gpu_idx[i], LOGIT_MARGIN), i
     keep = toks[robust]
-    y_ref = O.moe_forward_fp8(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k,
-                              tokens=keep)
+    y_ref = O.moe_forward_fp8_full(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k,
+                                   tokens=keep)
     y_gpu = y[torch.from_numpy(keep).to(dev)]
     stats = assert_moe_close(y_gpu, y_ref)
     # and how far the FP8 layer lies from the bf16 one (reported, not a bound)
@@ -122,7 +169,7 @@ def _forward_fp8_and_check(cfg, dev, seed=0, tokens=None):
     return stats, err_stats(y_gpu, y_bf), float(robust.mean())
 
 
-@pytest.mark.parametrize("T,d,n,E,k", [(256, 128, 128, 8, 2), (1000, 256, 256, 16, 4), (777, 384, 128, 5, 5)])
+@pytest.mark.parametrize("T,d,n,E,k", [(256, 256, 128, 8, 2), (1000, 256, 256, 16, 4), (777, 512, 128, 5, 5)])
 def test_forward_fp8(cuda_device, T, d, n, E, k):
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
     stats, vs_bf16, frac = _forward_fp8_and_check(cfg, cuda_device, seed=T + E)
