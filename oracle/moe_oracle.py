@@ -24,6 +24,8 @@ primitives used):
   5. gate-score-weighted combine (自定义核与核融合 step 5)
   6. optional token rounding of each expert's token count to a tile multiple
      (SonicMoE page, section "3. Token Rounding 路由算法")
+  7. the backward pass of the same layer by recomputation (SonicMoE page,
+     "SonicMoE 的三大核心优化" item 1 and section 反向传播优化)
 
 Readings of the pages (where they are silent or at odds):
   * Selection precision: a top-k choice is taken on fp32 logits (the kernel's
@@ -58,6 +60,12 @@ Readings of the pages (where they are silent or at odds):
     "fp8" layer): rows of the bf16 hidden h (as the up-projection stores it)
     and one row per expert for all of W2.  The GEMMs run on the dequantised
     values code * scale; routing and the combine stay as above.
+  * Backward: the pages give no formulas, only that the gradients stay
+    those of the MoE formula while intermediates are recomputed.  The
+    reading is the exact gradient of the forward above for a given dy = dL/dy,
+    with the selected sets (and any rounding) held fixed: the selection is
+    piecewise constant, so it passes no gradient.  The router gradient goes
+    through the renormalised softmax of the selected logits only.
 
 Pins (tests/test_oracle.py): brute-force k-subset top-k; the closed form
 w0 = sigmoid(L0 - L1) at k=2; numpy's stable argsort for the permutation;
@@ -65,7 +73,10 @@ index-arithmetic SwiGLU on one-nonzero-per-column weights (catches a
 transposed operand); E=1,k=1 == dense FFN; identical experts == dense FFN;
 relabelling invariance; W2=0 -> 0; token-rounding invariants checked by
 brute force on tiny inputs; e4m3 rounding against a brute-force nearest
-search over all values of the format.  No function here is unpinned.
+search over all values of the format; the backward pass against central
+finite differences of moe_forward on tiny layers, the zero router gradient
+at k=1, the dense-FFN case and the zero sum of each token's logit gradient.
+No function here is unpinned.
 """
 from __future__ import annotations
 
@@ -470,3 +481,83 @@ def moe_forward_fp8_full(x, Wr, bias, W1, W3, W2, k: int, tokens=None):
         np.add.at(y, pos, np.array(w_of[e])[:, None] * o)
     return y
 
+
+
+# --------------------------------------------------------------------------
+# 8. backward pass
+# --------------------------------------------------------------------------
+def sigmoid(z) -> np.ndarray:
+    z = np.asarray(z, dtype=F64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def moe_backward(x, Wr, bias, W1, W3, W2, dy, k: int, tile: int = 128, mode: str = ROUND_OFF,
+                 seed: int = 0) -> dict:
+    """Gradients of the scalar sum_t <dy[t], y[t]> with respect to every input
+    of moe_forward, fp64.
+
+    The SonicMoE page ("SonicMoE 的三大核心优化", item 1, and "反向传播优化")
+    recomputes the forward's intermediates instead of caching them and keeps
+    the gradients mathematically those of the MoE formula; the router
+    gradient dS is formed without the expert outputs (the "dS 计算优化" row of
+    the 关键 Kernel 对比 table).  Written out by the chain rule:
+
+      per routed pair (t, e) with gate weight w, g = x W1e, u = x W3e,
+      s = sigmoid(g), a = g s = silu(g), h = a u, o = h W2e:
+        dW2e += h^T (w dy)            dh = w dy W2e^T
+        du = dh a                     dg = dh u s (1 + g (1 - s))
+        dW1e += x^T dg                dW3e += x^T du
+        dx   += dg W1e^T + du W3e^T
+        dw   = <dy, o> = <dy W2e^T, h>
+      per token, over its selected set S (w = softmax of the logits on S):
+        dL[t, i] = w_i (dw_i - sum_{j in S} w_j dw_j) for i in S, 0 elsewhere
+      and through the gate network L = x Wr + b:
+        dWr = x^T dL,  db = sum_t dL[t],  dx += dL Wr^T.
+
+    The selection itself is piecewise constant in the logits, so no gradient
+    flows through it (nor through token rounding's choice of sets).  Returns
+    a dict with dx [T, d], dWr [d, E], db [E], dW1, dW3 [E, d, n], dW2 [E, n, d]
+    and dL [T, E], dw (per token, the list of its set's dw)."""
+    x64 = _f64(x)
+    dy64 = _f64(dy)
+    T, d = x64.shape
+    E, _, n = np.shape(W1)
+    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, seed=seed)
+    dx = np.zeros((T, d), dtype=F64)
+    dW1 = np.zeros((E, d, n), dtype=F64)
+    dW3 = np.zeros((E, d, n), dtype=F64)
+    dW2 = np.zeros((E, n, d), dtype=F64)
+    dw = [np.zeros(len(s), dtype=F64) for s in sets]
+    for e in range(E):
+        pairs = [(t, j) for t, s in enumerate(sets) for j, se in enumerate(s) if int(se) == e]
+        if not pairs:
+            continue
+        ts = np.array([t for t, _ in pairs], dtype=np.int64)
+        w = np.array([weights[t][j] for t, j in pairs], dtype=F64)
+        W1e, W3e, W2e = _f64(W1[e]), _f64(W3[e]), _f64(W2[e])
+        X = x64[ts]
+        g, u = X @ W1e, X @ W3e
+        s = sigmoid(g)
+        a = g * s
+        h = a * u
+        dh_unweighted = dy64[ts] @ W2e.T          # dy W2e^T
+        dW2[e] = h.T @ (w[:, None] * dy64[ts])
+        dh = w[:, None] * dh_unweighted
+        du = dh * a
+        dg = dh * u * (s * (1.0 + g * (1.0 - s)))
+        dW1[e] = X.T @ dg
+        dW3[e] = X.T @ du
+        np.add.at(dx, ts, dg @ W1e.T + du @ W3e.T)
+        dwe = np.sum(dh_unweighted * h, axis=1)   # <dy, h W2e>
+        for (t, j), v in zip(pairs, dwe):
+            dw[t][j] = v
+    dL = np.zeros((T, E), dtype=F64)
+    for t, (s, w) in enumerate(zip(sets, weights)):
+        if len(s):
+            dL[t, np.asarray(s, dtype=np.int64)] = w * (dw[t] - np.dot(w, dw[t]))
+    dWr = x64.T @ dL
+    db = dL.sum(axis=0)
+    dx = dx + dL @ _f64(Wr).T
+    return {"dx": dx, "dWr": dWr, "db": db, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dL": dL, "dw": dw,
+            "sets": sets, "weights": weights}
