@@ -18,6 +18,11 @@ collective on the data path); timing is the max over ranks.
 
 --impl reference times the fp64 CPU oracle (the checker the parity tests use)
 on a bounded token sample on the host cores.
+
+--backward measures the layer's backward pass instead (moe_backward through
+the C ABI: routing, gathers and pre-activations recomputed, then the four
+backward GEMMs and the router gradient); `value` counts 12*T*k*d*n FLOPs per
+step (twice the forward's, recomputation not counted).
 """
 from __future__ import annotations
 
@@ -39,6 +44,7 @@ import torch  # noqa: E402
 from mixture_experts_layer_93_b300 import inputs as I  # noqa: E402
 
 METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
+METRIC_BWD = "MoE bwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one up-projection
@@ -178,13 +184,18 @@ def run_reference(args, world, rank):
         return
     cfg = I.get_config(args.config)
     inp = I.make_inputs(cfg, device="cpu", seed=0)
-    active_per_token = 6.0 * cfg.k * cfg.d * cfg.n
+    if args.backward:
+        inp["dy"] = torch.randn(cfg.T, cfg.d, generator=torch.Generator().manual_seed(1000)).to(torch.bfloat16)
+        sample = lambda budget_s, seed: oracle_backward_time(cfg, inp, budget_s, seed)  # noqa: E731
+    else:
+        sample = lambda budget_s, seed: oracle_sample_time(cfg, inp, args.round, budget_s, seed)  # noqa: E731
+    active_per_token = (12.0 if args.backward else 6.0) * cfg.k * cfg.d * cfg.n
     for _ in range(args.warmup):
-        oracle_sample_time(cfg, inp, args.round, budget_s=0.0)   # one small call each
+        sample(0.0, 0)   # one small call each
     times, toks, threads = [], 0, 1
     budget = max(1.0, args.reference_seconds / max(args.steps, 1))
     for i in range(args.steps):
-        nt, dt, desc, th = oracle_sample_time(cfg, inp, args.round, budget_s=budget, seed=100 + i)
+        nt, dt, desc, th = sample(budget, 100 + i)
         times.append(dt)
         toks += nt
         threads = max(threads, th)
@@ -192,7 +203,7 @@ def run_reference(args, world, rank):
     tps = toks / total
     value = tps * active_per_token / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.description, "round": args.round, "tokens_per_step": toks // args.steps},
@@ -201,6 +212,168 @@ def run_reference(args, world, rank):
                          "sample": desc, "host_cpus": os.cpu_count()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------- backward
+def oracle_backward_time(cfg, inp_host, budget_s: float, seed: int = 0):
+    """Times the oracle's backward pass (as it stands) on token subsets of the
+    workload until ~budget_s; returns (tokens, seconds, description, threads)."""
+    from oracle import moe_oracle as O
+    rng = np.random.default_rng(seed)
+    n = 16
+    total_tok, total_s, total_cpu = 0, 0.0, 0.0
+    while True:
+        toks = np.sort(rng.choice(cfg.T, size=min(n, cfg.T), replace=False))
+        x = inp_host["x"][toks]
+        dy = inp_host["dy"][toks]
+        t0, c0 = time.perf_counter(), time.process_time()
+        O.moe_backward(x, inp_host["Wr"], inp_host["bias"], inp_host["W1"], inp_host["W3"], inp_host["W2"], dy,
+                       k=cfg.k)
+        dt = time.perf_counter() - t0
+        total_cpu += time.process_time() - c0
+        total_tok += len(toks)
+        total_s += dt
+        if total_s >= budget_s:
+            break
+        if dt < budget_s / 4:
+            n = min(cfg.T, n * 2)
+    desc = (f"backward of {total_tok} sampled tokens of the {cfg.name} workload as token subsets (fp64), "
+            f"{total_s:.1f} s")
+    threads = max(1, int(round(total_cpu / total_s))) if total_s > 0 else 1
+    return total_tok, total_s, desc, threads
+
+
+def run_backward(args, world, rank, local):
+    from mixture_experts_layer_93_b300 import binding as B
+    import ctypes
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    cfg = I.get_config(args.config)
+    if args.tokens:
+        cfg = cfg.with_tokens(args.tokens)
+    T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
+    shape = B.make_shape(T, d, n, E, k)
+    inp = I.make_inputs(cfg, device=dev, seed=rank)
+    g = torch.Generator(device=dev).manual_seed(1000 + rank)
+    dy = torch.randn(T, d, generator=g, device=dev).to(torch.bfloat16)
+    W13p, _ = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    W13i = B.moe_prepare_weights_bwd(inp["W1"], inp["W3"])
+    W2 = inp["W2"]
+    inp_host = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inp_host = {kk: (v.cpu() if isinstance(v, torch.Tensor) else v) for kk, v in inp.items()}
+        inp_host["dy"] = dy.cpu()
+    del inp["W1"], inp["W3"]
+    torch.cuda.empty_cache()
+    x, Wr, bias = inp["x"], inp["Wr"], inp["bias"]
+    ws = B.Workspace(shape, dev, backward=True)
+    out = {"dx": torch.empty(T, d, dtype=torch.float32, device=dev),
+           "dWr": torch.empty(d, E, dtype=torch.float32, device=dev),
+           "dbias": torch.empty(E, dtype=torch.float32, device=dev) if bias is not None else None,
+           "dW1": torch.empty(E, d, n, dtype=torch.float32, device=dev),
+           "dW3": torch.empty(E, d, n, dtype=torch.float32, device=dev),
+           "dW2": torch.empty(E, n, d, dtype=torch.float32, device=dev)}
+    L = B.lib()
+    sp = ctypes.byref(shape)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    stream = torch.cuda.current_stream(dev)
+
+    def bwd(x_, dy_, dx_, ws_, st_):
+        rc = L.moe_backward(sp, P(x_), P(Wr), P(bias), P(W13p), P(W13i), P(W2), P(dy_), P(dx_), P(out["dWr"]),
+                            P(out["dbias"]), P(out["dW1"]), P(out["dW3"]), P(out["dW2"]), ws_.ptr, ws_.nbytes,
+                            ctypes.c_void_p(st_.cuda_stream))
+        if rc != 0:
+            raise B.MoEError(rc, "moe_backward")
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        bwd(x, dy, out["dx"], ws, stream)
+    torch.cuda.synchronize()
+    B.moe_check_device_status(ws)
+    clocks = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(float(i))          # L2 flush between steps (not timed)
+        ev[i][0].record(stream)
+        bwd(x, dy, out["dx"], ws, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    B.moe_check_device_status(ws)
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), world, dev)
+    flops = 2.0 * cfg.active_flops()
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # e2e: x and dy in from pinned memory, dx back, every step; the weight
+    # gradients stay on the device (an optimizer step would consume them there)
+    x_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    dy_host = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    dx_host = torch.empty(T, d, dtype=torch.float32, pin_memory=True)
+    x_host.copy_(x.cpu())
+    dy_host.copy_(dy.cpu())
+    x_dev, dy_dev, dx_dev = torch.empty_like(x), torch.empty_like(dy), torch.empty_like(out["dx"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        dy_dev.copy_(dy_host, non_blocking=True)
+        bwd(x_dev, dy_dev, dx_dev, ws, stream)
+        dx_host.copy_(dx_dev, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    B.moe_check_device_status(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    if rank != 0:
+        return
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # launches per moe_backward: route + permute (5, or 6 when E > 256), padded
+    # rows (2), zero padding, two gathers, pre-activations, SwiGLU backward,
+    # router backward, dW2, dW1/dW3, dx rows (1, or 2 with separate odd
+    # blocks), router transpose, dx, dWr partial and final
+    dx_launches = 1 if 128.0 * E <= 0.15 * (T * k + 63 * E) else 2
+    launches = (5 if E <= 256 else 6) + 2 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.description + ", backward pass", "T": T, "d": d, "n": n, "E": E, "k": k,
+                   "flops_per_step": flops, "outputs": "dx, dWr, dbias, dW1, dW3, dW2 in fp32",
+                   "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": world * T * args.steps / (total_ms * 1e-3),
+        "frac_of_bf16_peak": value / world / burst,
+        "frac_of_bf16_sustained_peak": value / world / sustained,
+        "peak_source": f"{peak_src} bf16_tflops (burst)",
+        "e2e": {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": T * d * 4,
+                "how": "moe_backward per step with x and dy H2D from pinned memory and dx D2H; weight "
+                       "gradients stay on the device"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+    if inp_host is not None:
+        ntok, secs, desc, threads = oracle_backward_time(cfg, inp_host, budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": ntok * 12.0 * k * d * n / secs / 1e12, "unit": "TFLOP/s",
+                                "tokens_per_s": ntok / secs, "cores": threads, "host_cpus": os.cpu_count(),
+                                "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
 
 
@@ -489,6 +662,8 @@ def main():
     ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
                     help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
                          "rows, 2 = per-lane cp.async of token rows")
+    ap.add_argument("--backward", action="store_true",
+                    help="measure the backward pass (moe_backward) instead of the forward")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
@@ -498,7 +673,7 @@ def main():
         return
     world, rank, local = dist_init(args)
     try:
-        run_ours(args, world, rank, local)
+        (run_backward if args.backward else run_ours)(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist

@@ -320,6 +320,47 @@ int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const fl
                     const void* W13q, const float* sW13, const void* W2q, const float* sW2,
                     void* y, void* ws, size_t ws_bytes, void* stream);
 
+/* ----------------------------------------------------------- backward ---
+ * Gradients of sum_t <dy[t], y[t]> for y = moe_forward(x, ...), by
+ * recomputation instead of cached activations ("SonicMoE: 加速 MoE 模型的 IO
+ * 与 Tile 感知优化", "SonicMoE 的三大核心优化" item 1 and section 反向传播优化):
+ * routing, the gathered x rows and the up-projection's pre-activations are
+ * recomputed, and the gate weights' gradient is sum_j dh'[j] h[j] per row
+ * (dh' = dy W2^T), so no expert output is formed (the 关键 Kernel 对比
+ * table's "dS 计算优化").  The selected sets are held fixed (selection passes
+ * no gradient); the logits' gradient is that of the softmax over the k
+ * selected logits.  bf16 operands, fp32 accumulation; the pre-activations
+ * are held in fp32, their gradients and w h in bf16 (the weight-gradient
+ * GEMMs' operands), each row's input gradient from the experts in fp16
+ * (saturation is reported as for ys);
+ * every sum runs in a fixed order, so results are bitwise reproducible.
+ * Requires round == MOE_ROUND_OFF, d % 128 == 0 (n % 64 == 0 as always),
+ * else MOE_ERR_UNSUPPORTED. */
+
+/* Workspace bytes of moe_backward (0 for an invalid or unsupported shape). */
+size_t moe_backward_workspace_bytes(const moe_shape* s);
+
+/* W13i [E, d, 2n] bf16 with W13i[e][i][2j] = W1[e][i][j] and
+ * W13i[e][i][2j+1] = W3[e][i][j]: the packed up weight transposed, for the
+ * input gradient.  One-time, like moe_prepare_weights. */
+int moe_prepare_weights_bwd(const moe_shape* s, const void* W1, const void* W3, void* W13i,
+                            void* stream);
+
+/* Backward pass of the layer.
+ *   in:  x [T, d] bf16, Wr [d, E] fp32, bias [E] fp32 or NULL, W13p from
+ *        moe_prepare_weights, W13i from moe_prepare_weights_bwd, W2 [E, n, d]
+ *        bf16 (as given to moe_prepare_weights), dy [T, d] bf16;
+ *   out: dx [T, d], dWr [d, E], dbias [E] (NULL: not written), dW1 and dW3
+ *        [E, d, n], dW2 [E, n, d], all fp32, every element written (an expert
+ *        without tokens gets zero weight gradients).
+ * ws (moe_backward_workspace_bytes) is caller-owned device memory, 16-byte
+ * aligned; its status word reports device-side errors as for moe_forward.
+ * Asynchronous on `stream`. */
+int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                 const void* W13p, const void* W13i, const void* W2, const void* dy, float* dx,
+                 float* dWr, float* dbias, float* dW1, float* dW3, float* dW2, void* ws,
+                 size_t ws_bytes, void* stream);
+
 /* Self-test of the bounded-wait machinery: launches one block that waits on a
  * device flag nobody sets, giving up after `timeout_ns` nanoseconds; the
  * kernel then records MOE_ERR_TIMEOUT in the status word of `ws` and returns. */

@@ -78,6 +78,9 @@ _SIGNATURES = {
     "moe_forward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_workspace_layout": (_I, [_SHP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
     "moe_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+    "moe_backward_workspace_bytes": (_SZ, [_SHP]),
+    "moe_prepare_weights_bwd": (_I, [_SHP, _P, _P, _P, _P]),
+    "moe_backward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 _lib = None
@@ -152,8 +155,11 @@ def moe_workspace_layout(shape: moe_shape) -> dict:
 class Workspace:
     """Device workspace for one shape (status block zeroed at creation)."""
 
-    def __init__(self, shape: moe_shape, device="cuda", fp8: bool = False):
-        nbytes = moe_workspace_bytes_fp8(shape) if fp8 else moe_workspace_bytes(shape)
+    def __init__(self, shape: moe_shape, device="cuda", fp8: bool = False, backward: bool = False):
+        if backward:
+            nbytes = moe_backward_workspace_bytes(shape)
+        else:
+            nbytes = moe_workspace_bytes_fp8(shape) if fp8 else moe_workspace_bytes(shape)
         if nbytes == 0:
             raise MoEError(MOE_ERR_INVALID, "moe_workspace_bytes")
         self.shape = shape
@@ -396,6 +402,40 @@ def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None)
     _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p), _ptr(y),
                              ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward")
     return y
+
+
+def moe_backward_workspace_bytes(shape: moe_shape) -> int:
+    return int(lib().moe_backward_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_prepare_weights_bwd(W1, W3):
+    """W13i [E, d, 2n]: W1 and W3 interleaved along their last dimension."""
+    _need_cuda(W1, W3)
+    E, d, n = W1.shape
+    shape = make_shape(1, d, n, E, 1)
+    W13i = torch.empty(E, d, 2 * n, dtype=torch.bfloat16, device=W1.device)
+    _check(lib().moe_prepare_weights_bwd(ctypes.byref(shape), _ptr(W1), _ptr(W3), _ptr(W13i), _stream(W1.device)),
+           "moe_prepare_weights_bwd")
+    return W13i
+
+
+def moe_backward(shape: moe_shape, x, Wr, bias, W13p, W13i, W2, dy, ws: Workspace, want_dbias: bool = True,
+                 out=None) -> dict:
+    """Gradients {dx, dWr, dbias, dW1, dW3, dW2} (fp32) of sum <dy, y>; dy bf16 [T, d]."""
+    _need_cuda(x, Wr, bias, W13p, W13i, W2, dy)
+    dev = x.device
+    T, d, n, E = shape.T, shape.d, shape.n, shape.E
+    if out is None:
+        out = {"dx": torch.empty(T, d, dtype=torch.float32, device=dev),
+               "dWr": torch.empty(d, E, dtype=torch.float32, device=dev),
+               "dbias": torch.empty(E, dtype=torch.float32, device=dev) if want_dbias else None,
+               "dW1": torch.empty(E, d, n, dtype=torch.float32, device=dev),
+               "dW3": torch.empty(E, d, n, dtype=torch.float32, device=dev),
+               "dW2": torch.empty(E, n, d, dtype=torch.float32, device=dev)}
+    _check(lib().moe_backward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W13i), _ptr(W2),
+                              _ptr(dy), _ptr(out["dx"]), _ptr(out["dWr"]), _ptr(out.get("dbias")), _ptr(out["dW1"]),
+                              _ptr(out["dW3"]), _ptr(out["dW2"]), ws.ptr, ws.nbytes, _stream(dev)), "moe_backward")
+    return out
 
 
 def moe_selftest_timeout(ws: Workspace, timeout_ns: int):

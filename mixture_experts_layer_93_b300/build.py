@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libmoe.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "round.cu", "gemm.cu", "combine.cu", "prepare.cu", "fp8.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "round.cu", "gemm.cu", "combine.cu", "prepare.cu", "fp8.cu", "bwd.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
               "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-cudart", "static"]
 

@@ -78,6 +78,33 @@ int check_ws(const moe_shape* s, void* ws, size_t ws_bytes, bool fp8 = false) {
   return MOE_OK;
 }
 
+// Backward workspace: the forward's slots, then the backward's arrays over
+// the padded row layout (each expert's rows padded to a multiple of 64).
+enum BwdSlot {
+  kOffP, kRowP, kWp, kXp, kDyp, kGl, kDgl, kHw, kDwPart, kDxr, kDl, kDlp, kWrT, kDwrPart, kDbPart, kNumBwdSlots
+};
+
+inline int64_t padded_cap(const moe_shape* s) { return static_cast<int64_t>(s->T) * s->k + 63 * int64_t(s->E); }
+
+int64_t layout_bwd(const moe_shape* s, int64_t* off_fwd, int64_t* off) {
+  const int64_t base = layout(s, off_fwd);
+  const int64_t T = s->T, E = s->E, A = T * s->k, capp = padded_cap(s), d = s->d, n = s->n;
+  const int64_t S = bwd_dwr_splits(s->E, s->d);
+  const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4,
+                                       capp * d * 2, capp * d * 2, capp * 2 * n * 4,
+                                       capp * 2 * n * 2, capp * n * 2, capp * (n / bwd_act_block(s->n)) * 4, capp * d * 2,
+                                       A * 4,        capp * 4,     E * d * 4,
+                                       S * E * d * 4, S * E * 4};
+  int64_t pos = base;
+  for (int i = 0; i < kNumBwdSlots; ++i) {
+    off[i] = pos;
+    pos = align256(pos + sizes[i]);
+  }
+  return pos;
+}
+
+bool bwd_shape_ok(const moe_shape* s) { return s->round == MOE_ROUND_OFF && s->d % 128 == 0 && s->n % 64 == 0; }
+
 }  // namespace
 
 extern "C" {
@@ -412,6 +439,95 @@ int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const fl
   if ((st = moe_expert_down_fp8(s, h, W2q, sW2, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK)
     return st;
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
+}
+
+size_t moe_backward_workspace_bytes(const moe_shape* s) {
+  if (!shape_ok(s) || !bwd_shape_ok(s)) return 0;
+  int64_t off_f[kNumSlots], off[kNumBwdSlots];
+  return static_cast<size_t>(layout_bwd(s, off_f, off));
+}
+
+int moe_prepare_weights_bwd(const moe_shape* s, const void* W1, const void* W3, void* W13i, void* stream) {
+  if (!shape_ok(s) || !W1 || !W3 || !W13i || !aligned16(W13i)) return MOE_ERR_INVALID;
+  launch_prepare_weights_bwd(static_cast<const __nv_bfloat16*>(W1), static_cast<const __nv_bfloat16*>(W3),
+                             static_cast<__nv_bfloat16*>(W13i), s->E, s->d, s->n, as_stream(stream));
+  return last_launch();
+}
+
+int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                 const void* W13i, const void* W2, const void* dy, float* dx, float* dWr, float* dbias, float* dW1,
+                 float* dW3, float* dW2, void* ws, size_t ws_bytes, void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !W13p || !W13i || !W2 || !dy || !dx || !dWr || !dW1 || !dW3 || !dW2)
+    return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(W13p) || !aligned16(W13i) || !aligned16(W2) || !aligned16(dy) || !aligned16(dx))
+    return MOE_ERR_INVALID;
+  if (!bwd_shape_ok(s)) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
+  int64_t off_f[kNumSlots], off[kNumBwdSlots];
+  if (static_cast<int64_t>(ws_bytes) < layout_bwd(s, off_f, off)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  const int T = s->T, d = s->d, n = s->n, E = s->E, k = s->k;
+  const int64_t A = static_cast<int64_t>(T) * k, capp = padded_cap(s);
+  float* logits = at<float>(ws, off_f[kLogits]);
+  int32_t* idx = at<int32_t>(ws, off_f[kTopkIdx]);
+  float* w = at<float>(ws, off_f[kTopkW]);
+  int32_t* counts = at<int32_t>(ws, off_f[kCounts]);
+  int32_t* offsets = at<int32_t>(ws, off_f[kOffsets]);
+  int32_t* src = at<int32_t>(ws, off_f[kSrc]);
+  int32_t* dst = at<int32_t>(ws, off_f[kDst]);
+  int32_t* row_token = at<int32_t>(ws, off_f[kRowToken]);
+  float* row_w = at<float>(ws, off_f[kRowW]);
+  int32_t* offsets_p = at<int32_t>(ws, off[kOffP]);
+  int32_t* rowp = at<int32_t>(ws, off[kRowP]);
+  float* wp = at<float>(ws, off[kWp]);
+  __nv_bfloat16* xp = at<__nv_bfloat16>(ws, off[kXp]);
+  __nv_bfloat16* dyp = at<__nv_bfloat16>(ws, off[kDyp]);
+  float* gl = at<float>(ws, off[kGl]);
+  __nv_bfloat16* dgl = at<__nv_bfloat16>(ws, off[kDgl]);
+  __nv_bfloat16* hw = at<__nv_bfloat16>(ws, off[kHw]);
+  float* dw_part = at<float>(ws, off[kDwPart]);
+  __half* dxr = at<__half>(ws, off[kDxr]);
+  float* dl = at<float>(ws, off[kDl]);
+  float* dlp = at<float>(ws, off[kDlp]);
+  float* WrT = at<float>(ws, off[kWrT]);
+  int32_t* status = status_of(ws);
+
+  // 1. routing, recomputed: the same kernels and bits as the forward
+  int rc = moe_route_permute(s, x, Wr, bias, logits, idx, w, counts, offsets, src, dst, row_token, row_w, ws,
+                             ws_bytes, stream);
+  if (rc != MOE_OK) return rc;
+  // 2. padded rows, zero padding, gathered x and dy
+  launch_bwd_rows(idx, w, dst, counts, offsets, E, A, offsets_p, rowp, wp, st);
+  launch_bwd_zero_pad(counts, offsets_p, E, d, n, xp, dyp, dgl, hw, st);
+  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(x), rowp, nullptr, T, k, d, xp, st);
+  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(dy), rowp, nullptr, T, k, d, dyp, st);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  // 3. pre-activations, then the SwiGLU backward fused into dh' = dy W2^T
+  if ((rc = launch_expert_up_pre(xp, static_cast<const __nv_bfloat16*>(W13p), counts, offsets_p, gl, d, n, E, capp,
+                                 status, kDefaultTimeoutNs, st)) != MOE_OK)
+    return rc;
+  if ((rc = launch_bwd_act(dyp, static_cast<const __nv_bfloat16*>(W2), counts, offsets_p, wp, gl, dgl, hw, dw_part, d,
+                           n, E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
+    return rc;
+  // 4. gate weights -> logits
+  launch_router_bwd(rowp, w, dw_part, n / bwd_act_block(n), T, k, dl, dlp, st);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  // 5. weight gradients: dW2 = (w h)^T dy, dW1 / dW3 = x^T (dg, du)
+  if ((rc = launch_wgrad(dyp, hw, counts, offsets_p, d, n, E, capp, dW2, nullptr, status, kDefaultTimeoutNs, st)) !=
+      MOE_OK)
+    return rc;
+  if ((rc = launch_wgrad(dgl, xp, counts, offsets_p, 2 * n, d, E, capp, dW1, dW3, status, kDefaultTimeoutNs, st)) !=
+      MOE_OK)
+    return rc;
+  // 6. dx: the expert paths ([dg du] W13i^T per row, fp16) and the gate network
+  if ((rc = launch_expert_down(dgl, static_cast<const __nv_bfloat16*>(W13i), counts, offsets_p, nullptr, dxr, d, 2 * n,
+                               E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
+    return rc;
+  launch_bwd_dx(dxr, rowp, idx, dl, Wr, WrT, T, d, E, k, dx, st);
+  // 7. dWr = x^T dL, db = sum dL
+  launch_bwd_dwr(xp, dlp, counts, offsets_p, E, d, at<float>(ws, off[kDwrPart]), at<float>(ws, off[kDbPart]), dWr,
+                 dbias, st);
+  return last_launch();
 }
 
 int moe_selftest_timeout(void* ws, uint64_t timeout_ns, void* stream) {

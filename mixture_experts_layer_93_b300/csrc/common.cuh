@@ -415,6 +415,22 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
   return desc;
 }
 
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle, as
+// TMA writes a [K rows][64 elements] box: each K index is one 128-byte row of
+// 64 consecutive M (or N) elements, eight rows form a 1024-byte swizzle
+// atom.  Consecutive atoms along K are `sbo` bytes apart, consecutive
+// 64-element blocks along M/N `lbo` bytes apart (the canonical MN-major
+// layout ((T,8,m),(8,k)) : ((1,T,LBO),(8T,SBO)), T = 8 elements of 16 bits).
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);          // start address
+  desc |= static_cast<uint64_t>((lbo & 0x3FFFFu) >> 4) << 16;      // leading byte offset: M/N blocks
+  desc |= static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32;      // stride byte offset: K atoms
+  desc |= static_cast<uint64_t>(1u) << 46;                         // descriptor version
+  desc |= static_cast<uint64_t>(2u) << 61;                         // 128-byte swizzle
+  return desc;
+}
+
 // Instruction descriptor for kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                    // D format: f32
@@ -422,6 +438,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (1u << 10)                                 // B format: bf16
          | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);     // M / 16
+}
+
+// The same with both operands MN-major (the transpose-A and transpose-B bits).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 15) | (1u << 16);
 }
 
 // Instruction descriptor for kind::f8f6f4: e4m3 A and B (format code 0, both

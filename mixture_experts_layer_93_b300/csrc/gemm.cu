@@ -37,7 +37,12 @@
 
 namespace moe {
 
-enum GemmMode : int { kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3, kModeDownF8 = 4 };  // F8: e4m3
+// F8: e4m3.  UpPre stores the up-projection's pre-activations; BwdAct and
+// Wgrad are the backward pass (see their epilogues).
+enum GemmMode : int {
+  kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3, kModeDownF8 = 4,
+  kModeUpPre = 5, kModeBwdAct = 6, kModeWgrad = 7
+};
 
 struct GemmParams {
   const int32_t* counts;     // [E] rows per group (ignored when single_rows > 0)
@@ -66,6 +71,14 @@ struct GemmParams {
   const float* row_scale;    // F8: scale of each A row [cap]
   const float* col_scale;    // F8 up: scale of each B row (output channel) [E * b_rows_per_expert];
                              // F8 down: one scale per expert [E]
+  // backward
+  const float* pre;          // BwdAct: pre-activations (g, u interleaved) [cap, 2 * out_ld]
+  __nv_bfloat16* out2_bf16;  // BwdAct: w * h [cap, out_ld]
+  float* out2_f32;           // BwdAct: partial <dh, h> [cap, parts]; Wgrad: odd M rows when interleaved
+  int parts;                 // BwdAct: partials per row (n_blocks)
+  int m_units;               // Wgrad: M tile units per group
+  int64_t out_group_stride;  // Wgrad: elements between the outputs of consecutive groups
+  int interleave;            // Wgrad: even M rows go to out_f32, odd ones to out2_f32, at row M / 2
 };
 
 constexpr int kProducerWarps = 4;
@@ -180,6 +193,17 @@ __device__ __forceinline__ void group_rows(const GemmParams& p, const int2* grp_
   }
 }
 
+// Weight-gradient tiles: every group has m_units x n_blocks tiles (empty
+// groups too: their gradient is zero), n fastest, so the tiles that run
+// together share the group's A columns and its whole B.
+__device__ __forceinline__ void wgrad_tile(int tau, const GemmParams& p, int& e, int& mu, int& nb) {
+  const int per = p.m_units * p.n_blocks;
+  e = tau / per;
+  const int local = tau - e * per;
+  mu = local / p.n_blocks;
+  nb = local - mu * p.n_blocks;
+}
+
 template <int BN, int MODE, bool PAIR, int EPI>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -188,7 +212,12 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   constexpr bool kF8 = MODE == kModeUpF8 || MODE == kModeDownF8;
   constexpr bool kDown = MODE == kModeDown || MODE == kModeDownF8;
+  constexpr bool kWgrad = MODE == kModeWgrad;
   static_assert(!kF8 || PAIR, "the e4m3 GEMMs run on SM pairs");
+  static_assert(!kWgrad || (C::B_ROWS % 64 == 0 && EPI == 4), "weight-gradient tiles: 64-wide B blocks");
+  // Wgrad operands are MN-major: [64 K rows][64 elements] boxes, 8 KB each,
+  // two for the 128 A columns, B_ROWS / 64 for B
+  constexpr uint32_t kMnBlock = 64 * 128;
   // K elements per operand stage: a stage row is 128 bytes (64 bf16 or 128 e4m3)
   constexpr int KB_ELEMS = kF8 ? 128 : C::BK;
   extern __shared__ uint8_t smem_raw[];
@@ -238,7 +267,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE != kModeRouter) tma_prefetch_desc(&tmC);
+    if (MODE != kModeRouter && MODE != kModeBwdAct && MODE != kModeWgrad) tma_prefetch_desc(&tmC);
   } else if (warp == kMmaWarp) {
     if (PAIR) {
       tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -288,12 +317,66 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   if (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int total_tiles = prefix[n_groups] * p.n_blocks;
+  const int total_tiles = kWgrad ? p.E * p.m_units * p.n_blocks : prefix[n_groups] * p.n_blocks;
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
     const bool issuer = (warp == 0);
-    if (issuer || p.gather == 2) {
+    if constexpr (kWgrad) {
+      // K runs over the group's rows (padded to 64 with zero rows); A holds
+      // this CTA's 128 M columns, B its B_ROWS N columns, both MN-major
+      if (issuer) {
+        const uint64_t pol = policy_evict_normal();
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
+          int e, mu, nb;
+          wgrad_tile(tau, p, e, mu, nb);
+          const int2 g = grp_s[e];
+          const int nkb = (g.y + C::BK - 1) / C::BK;
+          const int m0 = (mu * kPer + rank) * C::BM;
+          const int n0 = nb * BN + rank * C::B_ROWS;
+          for (int kb = 0; kb < nkb; ++kb) {
+            int w = 1;
+            if (lane == 0)
+              w = mbar_wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, p.status,
+                                    kWaitProducerEmpty, p.timeout_ns);
+            if (!__shfl_sync(0xffffffffu, w, 0)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t fb = smem_u32(&full_bar[stage]);
+              const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
+              const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
+              const int krow = g.x + kb * C::BK;
+              if (PAIR) {
+                const uint32_t fb0 = map_to_cta(fb, 0);
+                if (leader) mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+#pragma unroll
+                for (int i = 0; i < C::BM / 64; ++i) tma_load_2d_pair(a_dst + i * kMnBlock, &tmA, m0 + 64 * i, krow, fb0, pol);
+#pragma unroll
+                for (int i = 0; i < C::B_ROWS / 64; ++i)
+                  tma_load_2d_pair(b_dst + i * kMnBlock, &tmB, n0 + 64 * i, krow, fb0, pol);
+              } else {
+                mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+#pragma unroll
+                for (int i = 0; i < C::BM / 64; ++i) tma_load_2d(a_dst + i * kMnBlock, &tmA, m0 + 64 * i, krow, fb, pol);
+#pragma unroll
+                for (int i = 0; i < C::B_ROWS / 64; ++i)
+                  tma_load_2d(b_dst + i * kMnBlock, &tmB, n0 + 64 * i, krow, fb, pol);
+              }
+            }
+            __syncwarp();
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    } else if (issuer || p.gather == 2) {
       // expert GEMMs: A rows are re-read by every n-block, a B slice only by
       // the m-blocks of one group; router: the few-MB B is re-read by every
       // m-block, an A row block only by its n-blocks (run together)
@@ -386,7 +469,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      constexpr uint32_t idesc = kF8 ? idesc_e4m3_f32(kPer * C::BM, BN) : idesc_bf16_f32(kPer * C::BM, BN);
+      constexpr uint32_t idesc = kF8       ? idesc_e4m3_f32(kPer * C::BM, BN)
+                                 : kWgrad ? idesc_bf16_f32_mn(kPer * C::BM, BN)
+                                          : idesc_bf16_f32(kPer * C::BM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -398,7 +483,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        int nkb = p.num_kb;
+        if constexpr (kWgrad) {
+          // a group without rows issues no MMA: its epilogue writes zeros
+          int e, mu, nb;
+          wgrad_tile(tau, p, e, mu, nb);
+          nkb = (grp_s[e].y + C::BK - 1) / C::BK;
+        }
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded<PAIR>(smem_u32(&full_bar[stage]), phase, abort_flag, p.status, kWaitMmaFull,
                                        p.timeout_ns)) {
             ok = false;
@@ -409,7 +501,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BK / 16; ++kk) {
-            const uint64_t ad = smem_desc_k128(a0 + kk * 32), bd = smem_desc_k128(b0 + kk * 32);
+            // K-major: 16 elements = 32 bytes along a row; MN-major: 16 K rows = 2048 bytes
+            const uint64_t ad = kWgrad ? smem_desc_mn128(a0 + kk * 2048, kMnBlock, 1024) : smem_desc_k128(a0 + kk * 32);
+            const uint64_t bd = kWgrad ? smem_desc_mn128(b0 + kk * 2048, kMnBlock, 1024) : smem_desc_k128(b0 + kk * 32);
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if constexpr (kF8)  // 32 e4m3 of K per instruction: the same 32 bytes per row as 16 bf16
               tc_mma_f8_pair(d_tmem, ad, bd, idesc, accum);
@@ -504,147 +598,262 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       }
       (void)row;
     };
-    // Tiles are decoded one ahead: the next tile's place (and, down, the
-    // gate weight of this thread's row in it) is fetched before this tile's
-    // accumulator is waited for, so the load latency hides behind this tile.
-    int dec_e = 0;  // group cursor of decode_tile
-    int nx_nb = 0, nx_row0 = 0, nx_rows = 0, nx_e = 0;
-    float nx_w = 0.f;  // down: gate weight; F8 up: row scale
-    auto decode_next = [&](int t) {
-      int mu, gstart, gcount;
-      decode_tile<MODE == kModeRouter>(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
-      group_rows(p, grp_s, dec_e, gstart, gcount);
-      const int mb = unit_block(p.units, mu, rank, gcount);
-      nx_row0 = gstart + mb * C::BM;
-      nx_rows = min(C::BM, gcount - mb * C::BM);
-      nx_e = dec_e;
-      if (MODE == kModeDown) nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] : 0.f;
-      if (MODE == kModeUpF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
-      // F8 down: the gate weight times the row's and the expert's scales
-      if (MODE == kModeDownF8)
-        nx_w = r_in_tile < nx_rows
-                   ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] * p.col_scale[dec_e]
-                   : 0.f;
-    };
-    if (unit0 < total_tiles) decode_next(unit0);
-    for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
-      const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows, e_tile = nx_e;
-      const float wr = nx_w;
-      if (tau + unit_stride < total_tiles) decode_next(tau + unit_stride);
-      int w = 1;
-      if (lane == 0)
-        w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
-                              p.timeout_ns);
-      if (!__shfl_sync(0xffffffffu, w, 0)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      const bool valid = r_in_tile < rows_valid;
-      const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
-      const int warp_rows = max(0, min(32, rows_valid - ew * 32));
-      const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
-      if constexpr (MODE == kModeUp || MODE == kModeUpF8) {
-        // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile; accumulator
-        // columns 2j and 2j+1 hold the gate and linear branch of h column j.
-        // F8: the accumulator is a sum of code products; times the row's and
-        // the output channel's scale it is the product of the dequantised
-        // operands.  Lane l holds the two channel scales of h column c + l.
-        constexpr int H = BN / 2;
-        __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
-        const float* cs = kF8 ? p.col_scale + static_cast<int64_t>(e_tile) * p.b_rows_per_expert + nb * BN : nullptr;
+    if constexpr (kWgrad) {
+      // Lane r_in_tile holds M index m of the tile; TMEM column c is N index
+      // nb*BN + c.  Stores run along M (consecutive lanes, consecutive
+      // addresses): out[group][N][M], or with interleave the even and odd M
+      // rows of out / out2 at M / 2.
+      for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
+        int e, mu, nb;
+        wgrad_tile(tau, p, e, mu, nb);
+        const bool empty = grp_s[e].y == 0;
+        const int m = (mu * kPer + rank) * C::BM + r_in_tile;
+        float* dst = (p.interleave && (m & 1)) ? p.out2_f32 : p.out_f32;
+        dst += static_cast<int64_t>(e) * p.out_group_stride + (p.interleave ? (m >> 1) : m);
+        int w = 1;
+        if (lane == 0)
+          w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
+                                p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, w, 0)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
-        for (int c = ch * (H / NCH); c < (ch + 1) * (H / NCH); c += 32) {
-          uint32_t a[2][32];
-          tmem_ld32(taddr + 2 * c, a[0]);
-          tmem_ld32(taddr + 2 * c + 32, a[1]);
-          float2 sc = make_float2(1.f, 1.f);
-          if constexpr (kF8) sc = *reinterpret_cast<const float2*>(cs + 2 * (c + lane));
-          tc_wait_ld();
-          uint32_t o[16];
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          if (!empty) {
+            tmem_ld32(taddr + c, v);
+            tc_wait_ld();
+          } else {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const uint32_t* v = a[q >> 3] + 4 * (q & 7);
-            float g0 = __uint_as_float(v[0]), u0 = __uint_as_float(v[1]);
-            float g1 = __uint_as_float(v[2]), u1 = __uint_as_float(v[3]);
-            if constexpr (kF8) {
-              g0 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q);
-              u0 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q);
-              g1 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q + 1);
-              u1 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q + 1);
-            }
-            const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
-            const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
-            o[q] = pack_bf16x2(h0, h1);
+            for (int q = 0; q < 32; ++q) v[q] = 0u;
           }
-          if (warp_rows > 0) store_chunk(o, nb * H + c, row_w0, warp_rows, row, dst + c);
-        }
-      } else if constexpr (kDown) {
-        // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
-        // same traffic); values past the fp16 range saturate and are reported
-        // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait.
-        // amax = max |acc| over the row (NaN if any is NaN): since rounding is
-        // monotonic, some |w * acc| exceeds the fp16 range iff |w| * amax does.
-        __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
-        float amax = 0.f;
-        constexpr int STEP = (BN / NCH) >= 64 ? 64 : 32;
-#pragma unroll 1
-        for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
-          uint32_t v[2][32];
-          tmem_ld32(taddr + c0, v[0]);
-          if (STEP == 64) tmem_ld32(taddr + c0 + 32, v[1]);
-          tc_wait_ld();
+          const int64_t n0 = static_cast<int64_t>(nb) * BN + c;
 #pragma unroll
-          for (int half = 0; half < STEP / 32; ++half) {
+          for (int q = 0; q < 32; ++q) dst[(n0 + q) * p.out_ld] = __uint_as_float(v[q]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
+          else
+            mbar_arrive(smem_u32(&tempty_bar[acc]));
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    } else {
+      // Tiles are decoded one ahead: the next tile's place (and, down, the
+      // gate weight of this thread's row in it) is fetched before this tile's
+      // accumulator is waited for, so the load latency hides behind this tile.
+      int dec_e = 0;  // group cursor of decode_tile
+      int nx_nb = 0, nx_row0 = 0, nx_rows = 0, nx_e = 0;
+      float nx_w = 0.f;  // down: gate weight; F8 up: row scale
+      auto decode_next = [&](int t) {
+        int mu, gstart, gcount;
+        decode_tile<MODE == kModeRouter>(t, prefix, n_groups, p.n_blocks, dec_e, nx_nb, mu);
+        group_rows(p, grp_s, dec_e, gstart, gcount);
+        const int mb = unit_block(p.units, mu, rank, gcount);
+        nx_row0 = gstart + mb * C::BM;
+        nx_rows = min(C::BM, gcount - mb * C::BM);
+        nx_e = dec_e;
+        if (MODE == kModeDown || MODE == kModeBwdAct)
+          nx_w = r_in_tile < nx_rows ? (p.row_w ? p.row_w[nx_row0 + r_in_tile] : 1.f) : 0.f;
+        if (MODE == kModeUpF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
+        // F8 down: the gate weight times the row's and the expert's scales
+        if (MODE == kModeDownF8)
+          nx_w = r_in_tile < nx_rows
+                     ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] * p.col_scale[dec_e]
+                     : 0.f;
+      };
+      if (unit0 < total_tiles) decode_next(unit0);
+      for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
+        const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows, e_tile = nx_e;
+        const float wr = nx_w;
+        if (tau + unit_stride < total_tiles) decode_next(tau + unit_stride);
+        int w = 1;
+        if (lane == 0)
+          w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
+                                p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, w, 0)) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(acc * BN);
+        const bool valid = r_in_tile < rows_valid;
+        const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
+        const int warp_rows = max(0, min(32, rows_valid - ew * 32));
+        const int64_t row_w0 = static_cast<int64_t>(row0) + ew * 32;
+        if constexpr (MODE == kModeUp || MODE == kModeUpF8) {
+          // h columns [ch*H/NCH, (ch+1)*H/NCH) of this tile; accumulator
+          // columns 2j and 2j+1 hold the gate and linear branch of h column j.
+          // F8: the accumulator is a sum of code products; times the row's and
+          // the output channel's scale it is the product of the dequantised
+          // operands.  Lane l holds the two channel scales of h column c + l.
+          constexpr int H = BN / 2;
+          __nv_bfloat16* dst = p.out_bf16 + row * p.out_ld + static_cast<int64_t>(nb) * H;
+          const float* cs = kF8 ? p.col_scale + static_cast<int64_t>(e_tile) * p.b_rows_per_expert + nb * BN : nullptr;
+#pragma unroll 1
+          for (int c = ch * (H / NCH); c < (ch + 1) * (H / NCH); c += 32) {
+            uint32_t a[2][32];
+            tmem_ld32(taddr + 2 * c, a[0]);
+            tmem_ld32(taddr + 2 * c + 32, a[1]);
+            float2 sc = make_float2(1.f, 1.f);
+            if constexpr (kF8) sc = *reinterpret_cast<const float2*>(cs + 2 * (c + lane));
+            tc_wait_ld();
             uint32_t o[16];
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-              const float a = __uint_as_float(v[half][2 * q]), b = __uint_as_float(v[half][2 * q + 1]);
-              amax = fmax_nan(amax, fmax_nan(fabsf(a), fabsf(b)));
-              o[q] = pack_half2_satfinite(wr * a, wr * b);
+              const uint32_t* v = a[q >> 3] + 4 * (q & 7);
+              float g0 = __uint_as_float(v[0]), u0 = __uint_as_float(v[1]);
+              float g1 = __uint_as_float(v[2]), u1 = __uint_as_float(v[3]);
+              if constexpr (kF8) {
+                g0 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q);
+                u0 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q);
+                g1 *= wr * __shfl_sync(0xffffffffu, sc.x, 2 * q + 1);
+                u1 *= wr * __shfl_sync(0xffffffffu, sc.y, 2 * q + 1);
+              }
+              const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+              const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
+              o[q] = pack_bf16x2(h0, h1);
             }
-            const int c = c0 + 32 * half;
-            if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
+            if (warp_rows > 0) store_chunk(o, nb * H + c, row_w0, warp_rows, row, dst + c);
           }
-        }
-        if (valid && !(fabsf(wr) * amax <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
-      } else if (ch == 0) {
-        // router (first four epilogue warps only): the three column groups
-        // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum plus
-        // the bias is the logit
-        constexpr int EB = BN / 3;
-        const int e0 = nb * EB;
-        float* dst = p.out_f32 + row * p.out_ld;
+        } else if constexpr (kDown) {
+          // ys = w * acc stored as fp16 (3 more mantissa bits than bf16 at the
+          // same traffic); values past the fp16 range saturate and are reported
+          // columns [ch*BN/NCH, (ch+1)*BN/NCH), two 32-column TMEM loads per wait.
+          // amax = max |acc| over the row (NaN if any is NaN): since rounding is
+          // monotonic, some |w * acc| exceeds the fp16 range iff |w| * amax does.
+          __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
+          float amax = 0.f;
+          constexpr int STEP = (BN / NCH) >= 64 ? 64 : 32;
 #pragma unroll 1
-        for (int c = 0; c < EB; c += 16) {
-          uint32_t a[16], b[16], q[16];
-          tmem_ld16(taddr + c, a);
-          tmem_ld16(taddr + EB + c, b);
-          tmem_ld16(taddr + 2 * EB + c, q);
-          tc_wait_ld();
-          if (valid) {
+          for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
+            uint32_t v[2][32];
+            tmem_ld32(taddr + c0, v[0]);
+            if (STEP == 64) tmem_ld32(taddr + c0 + 32, v[1]);
+            tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int ecol = e0 + c + j;
-              if (ecol < p.out_cols) {
-                float v = (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(q[j]);
-                if (p.bias) v += p.bias[ecol];
-                dst[ecol] = v;
+            for (int half = 0; half < STEP / 32; ++half) {
+              uint32_t o[16];
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const float a = __uint_as_float(v[half][2 * q]), b = __uint_as_float(v[half][2 * q + 1]);
+                amax = fmax_nan(amax, fmax_nan(fabsf(a), fabsf(b)));
+                o[q] = pack_half2_satfinite(wr * a, wr * b);
+              }
+              const int c = c0 + 32 * half;
+              if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
+            }
+          }
+          if (valid && !(fabsf(wr) * amax <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
+        } else if constexpr (MODE == kModeUpPre) {
+          // the accumulator itself, (g, u) pairs of the packed W1/W3 rows, in
+          // fp32: 128 contiguous bytes of this thread's row per 32 columns
+          float* dst = p.out_f32 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
+#pragma unroll 1
+          for (int c = ch * (BN / NCH); c < (ch + 1) * (BN / NCH); c += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c, v);
+            tc_wait_ld();
+            if (valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+          }
+        } else if constexpr (MODE == kModeBwdAct) {
+          // Accumulator column c is dh'[r, j] = dy[t_r] . W2e[j, :] for channel
+          // j = nb*BN + c (no gate weight).  With the stored pre-activations g,
+          // u of that channel, s = sigmoid(g), a = g s:
+          //   dh = w dh',  du = dh a,  dg = dh u s (1 + g (1 - s)),
+          // written as bf16 pairs like (g, u); w h = w a u for the down weight's
+          // gradient; and sum_j dh'[r, j] h[r, j], this tile's part of the
+          // gate weight's gradient <dy, o> (SonicMoE's dS without the expert
+          // outputs), one partial per row and n-block.
+          const int64_t ld2 = 2 * p.out_ld;
+          float dw_acc = 0.f;
+#pragma unroll 1
+          for (int c = ch * (BN / NCH); c < (ch + 1) * (BN / NCH); c += 32) {
+            const int64_t j0 = static_cast<int64_t>(nb) * BN + c;
+            uint32_t v[32];
+            tmem_ld32(taddr + c, v);
+            float4 pre[16];
+            const float4* src = reinterpret_cast<const float4*>(p.pre + row * ld2 + 2 * j0);
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) pre[i] = src[i];
+            }
+            tc_wait_ld();
+            if (valid) {
+              uint32_t og[32], oh[16];
+#pragma unroll
+              for (int q = 0; q < 32; ++q) {
+                const float g = (&pre[q >> 1].x)[2 * (q & 1)], u = (&pre[q >> 1].x)[2 * (q & 1) + 1];
+                const float sg = 1.0f / (1.0f + __expf(-g));
+                const float a = g * sg;
+                const float h = a * u;
+                const float dhu = __uint_as_float(v[q]);
+                dw_acc = fmaf(dhu, h, dw_acc);
+                const float dh = wr * dhu;
+                og[q] = pack_bf16x2(dh * u * (sg * (1.0f + g * (1.0f - sg))), dh * a);
+                if (q & 1) {
+                  const float hp = __uint_as_float(oh[q >> 1]);
+                  oh[q >> 1] = pack_bf16x2(hp, wr * h);
+                } else {
+                  oh[q >> 1] = __float_as_uint(wr * h);
+                }
+              }
+              uint4* dg = reinterpret_cast<uint4*>(p.out_bf16 + row * ld2 + 2 * j0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dg[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
+              uint4* dhw = reinterpret_cast<uint4*>(p.out2_bf16 + row * p.out_ld + j0);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) dhw[i] = make_uint4(oh[4 * i], oh[4 * i + 1], oh[4 * i + 2], oh[4 * i + 3]);
+            }
+          }
+          if (valid) p.out2_f32[row * p.parts + nb * NCH + ch] = dw_acc;
+        } else if constexpr (MODE == kModeRouter) {
+          if (ch == 0) {
+          // router (first four epilogue warps only): the three column groups
+          // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum plus
+          // the bias is the logit
+          constexpr int EB = BN / 3;
+          const int e0 = nb * EB;
+          float* dst = p.out_f32 + row * p.out_ld;
+#pragma unroll 1
+          for (int c = 0; c < EB; c += 16) {
+            uint32_t a[16], b[16], q[16];
+            tmem_ld16(taddr + c, a);
+            tmem_ld16(taddr + EB + c, b);
+            tmem_ld16(taddr + 2 * EB + c, q);
+            tc_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int ecol = e0 + c + j;
+                if (ecol < p.out_cols) {
+                  float v = (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(q[j]);
+                  if (p.bias) v += p.bias[ecol];
+                  dst[ecol] = v;
+                }
               }
             }
           }
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          // the TMEM reads are complete (tcgen05.wait::ld) and nothing written
+          // here is read by the MMA thread: a relaxed arrival suffices
+          if (PAIR)
+            mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's MMA waits on it
+          else
+            mbar_arrive(smem_u32(&tempty_bar[acc]));
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        // the TMEM reads are complete (tcgen05.wait::ld) and nothing written
-        // here is read by the MMA thread: a relaxed arrival suffices
-        if (PAIR)
-          mbar_arrive_cluster_relaxed(map_to_cta(smem_u32(&tempty_bar[acc]), 0));  // the even CTA's MMA waits on it
-        else
-          mbar_arrive(smem_u32(&tempty_bar[acc]));
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
     }
     if (lane == 0) bulk_wait_all();  // our TMA stores have landed before the CTA exits
     __syncwarp();
@@ -682,9 +891,11 @@ static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 template <int BN, int MODE, bool PAIR>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                        cudaStream_t stream) {
-  const bool wide = ((MODE == kModeUp || MODE == kModeUpF8) && p.num_kb <= 24) ||
+  const bool wide = ((MODE == kModeUp || MODE == kModeUpF8 || MODE == kModeUpPre) && p.num_kb <= 24) ||
                     ((MODE == kModeDown || MODE == kModeDownF8) && p.num_kb <= 8);
-  if (MODE != kModeRouter && wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+  if constexpr (MODE != kModeRouter && MODE != kModeBwdAct && MODE != kModeWgrad) {
+    if (wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+  }
   return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
 }
 
@@ -1021,6 +1232,101 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   return (BN == 256)   ? launch_gemm<256, kModeDown, false>(tmA, tmB1, tmC, p, stream)
          : (BN == 128) ? launch_gemm<128, kModeDown, false>(tmA, tmB1, tmC, p, stream)
                        : launch_gemm<64, kModeDown, false>(tmA, tmB1, tmC, p, stream);
+}
+
+// ------------------------------------------------------------- backward
+// The backward GEMMs run on SM pairs with odd last blocks as half-empty pairs
+// (M-grouped ones) over the padded row layout: offsets are the padded first
+// rows, counts the true row counts.
+
+// gl[r] = xp[r] W13p_e^T: the up-projection's pre-activations (g, u) of each
+// channel, interleaved as the packed weight rows, fp32 [rows_cap, 2n].
+int launch_expert_up_pre(const __nv_bfloat16* xp, const __nv_bfloat16* W13p, const int32_t* counts,
+                         const int32_t* offsets, float* gl, int d, int n, int E, int64_t rows_cap,
+                         int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  const int BN = (n % 128 == 0) ? 256 : 128;
+  CUtensorMap tmA, tmB;
+  if (!make_map_bf16(&tmA, xp, d, rows_cap, 128)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN / 2)) return MOE_ERR_CUDA;
+  const CUtensorMap& tmC = tmA;  // the epilogue stores directly
+  GemmParams p = base_params(status, timeout_ns);
+  p.counts = counts;
+  p.offsets = offsets;
+  p.out_f32 = gl;
+  p.out_ld = 2 * n;
+  p.E = E;
+  p.num_kb = d / 64;
+  p.n_blocks = 2 * n / BN;
+  p.b_rows_per_expert = 2 * n;
+  p.units = 3;
+  return BN == 256 ? launch_gemm<256, kModeUpPre, true>(tmA, tmB, tmC, p, stream)
+                   : launch_gemm<128, kModeUpPre, true>(tmA, tmB, tmC, p, stream);
+}
+
+// dh' = dyp W2_e^T (W2 as given, [E * n, d]: rows are the K-major channels),
+// then the SwiGLU backward in the epilogue: dgl = (dg, du) pairs (bf16, as
+// gl), hw = w h and dw_part[r, nb] = sum over the n-block of dh' h.
+int launch_bwd_act(const __nv_bfloat16* dyp, const __nv_bfloat16* W2, const int32_t* counts, const int32_t* offsets,
+                   const float* row_w, const float* gl, __nv_bfloat16* dgl, __nv_bfloat16* hw, float* dw_part, int d,
+                   int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  const int BN = bwd_act_block(n);
+  CUtensorMap tmA, tmB;
+  if (!make_map_bf16(&tmA, dyp, d, rows_cap, 128)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, W2, d, static_cast<uint64_t>(E) * n, BN / 2)) return MOE_ERR_CUDA;
+  GemmParams p = base_params(status, timeout_ns);
+  p.counts = counts;
+  p.offsets = offsets;
+  p.row_w = row_w;
+  p.pre = gl;
+  p.out_bf16 = dgl;
+  p.out2_bf16 = hw;
+  p.out2_f32 = dw_part;
+  p.out_ld = n;
+  p.parts = n / BN;
+  p.E = E;
+  p.num_kb = d / 64;
+  p.n_blocks = n / BN;
+  p.b_rows_per_expert = n;
+  p.units = 3;
+  const CUtensorMap& tmC = tmA;  // the epilogue stores directly
+  return BN == 256   ? launch_gemm<256, kModeBwdAct, true>(tmA, tmB, tmC, p, stream)
+         : BN == 128 ? launch_gemm<128, kModeBwdAct, true>(tmA, tmB, tmC, p, stream)
+                     : launch_gemm<64, kModeBwdAct, true>(tmA, tmB, tmC, p, stream);
+}
+
+// Weight gradient of every group: out[g] = A_g^T B_g over the group's rows,
+// A [rows_cap, M] and B [rows_cap, N] row-major (read MN-major), fp32
+// out[g][N][M] (or, interleaved, even M to out and odd M to out2 as
+// [g][N][M/2]).  Rows past a group's count up to its padded end must be zero.
+int launch_wgrad(const __nv_bfloat16* A, const __nv_bfloat16* B, const int32_t* counts, const int32_t* offsets,
+                 int M, int N, int E, int64_t rows_cap, float* out, float* out2, int32_t* status,
+                 uint64_t timeout_ns, cudaStream_t stream) {
+  if (M % 128 != 0 || N % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  const bool pair = (M % 256 == 0) && (N % 128 == 0);
+  const int BN = (N % 256 == 0) ? 256 : (N % 128 == 0 ? 128 : 64);
+  CUtensorMap tmA, tmB;
+  if (!make_map_bf16(&tmA, A, M, rows_cap, 64)) return MOE_ERR_CUDA;
+  if (!make_map_bf16(&tmB, B, N, rows_cap, 64)) return MOE_ERR_CUDA;
+  GemmParams p = base_params(status, timeout_ns);
+  p.counts = counts;
+  p.offsets = offsets;
+  p.out_f32 = out;
+  p.out2_f32 = out2;
+  p.interleave = out2 != nullptr;
+  p.out_ld = p.interleave ? M / 2 : M;
+  p.out_group_stride = static_cast<int64_t>(N) * p.out_ld;
+  p.E = E;
+  p.num_kb = 0;
+  p.n_blocks = N / BN;
+  p.m_units = M / (pair ? 256 : 128);
+  p.units = 0;
+  const CUtensorMap& tmC = tmA;
+  if (pair)
+    return BN == 256 ? launch_gemm<256, kModeWgrad, true>(tmA, tmB, tmC, p, stream)
+                     : launch_gemm<128, kModeWgrad, true>(tmA, tmB, tmC, p, stream);
+  return BN == 256   ? launch_gemm<256, kModeWgrad, false>(tmA, tmB, tmC, p, stream)
+         : BN == 128 ? launch_gemm<128, kModeWgrad, false>(tmA, tmB, tmC, p, stream)
+                     : launch_gemm<64, kModeWgrad, false>(tmA, tmB, tmC, p, stream);
 }
 
 int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }

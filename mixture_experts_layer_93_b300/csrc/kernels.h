@@ -64,6 +64,17 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
 void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const int32_t* offsets, int E, int d,
                         __nv_bfloat16* out, int64_t rows_cap, cudaStream_t stream);
 inline int up_half_block(int n) { return (n % 128 == 0) ? 128 : 64; }
+// backward GEMMs (gemm.cu)
+inline int bwd_act_block(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
+int launch_expert_up_pre(const __nv_bfloat16* xp, const __nv_bfloat16* W13p, const int32_t* counts,
+                         const int32_t* offsets, float* gl, int d, int n, int E, int64_t rows_cap,
+                         int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+int launch_bwd_act(const __nv_bfloat16* dyp, const __nv_bfloat16* W2, const int32_t* counts, const int32_t* offsets,
+                   const float* row_w, const float* gl, __nv_bfloat16* dgl, __nv_bfloat16* hw, float* dw_part, int d,
+                   int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+int launch_wgrad(const __nv_bfloat16* A, const __nv_bfloat16* B, const int32_t* counts, const int32_t* offsets,
+                 int M, int N, int E, int64_t rows_cap, float* out, float* out2, int32_t* status,
+                 uint64_t timeout_ns, cudaStream_t stream);
 int num_sms();
 // router on the tensor cores: Wr split into three bf16 terms (see gemm.cu)
 int router_expert_block(int E);
@@ -82,6 +93,25 @@ void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t*
 // prepare.cu
 void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, const __nv_bfloat16* W2,
                             __nv_bfloat16* W13p, __nv_bfloat16* W2p, int E, int d, int n, cudaStream_t stream);
+
+void launch_prepare_weights_bwd(const __nv_bfloat16* W1, const __nv_bfloat16* W3, __nv_bfloat16* W13i, int E, int d,
+                                int n, cudaStream_t stream);
+
+// bwd.cu (backward pass around the backward GEMMs; padded row layout)
+int bwd_dwr_splits(int E, int d);
+void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, const int32_t* counts,
+                     const int32_t* offsets, int E, int64_t A, int32_t* offsets_p, int32_t* rowp, float* wp,
+                     cudaStream_t stream);
+void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E, int d, int n, __nv_bfloat16* xp,
+                         __nv_bfloat16* dyp, __nv_bfloat16* dgl, __nv_bfloat16* hw, cudaStream_t stream);
+void launch_router_bwd(const int32_t* rowp, const float* w, const float* dw_part, int parts, int T, int k, float* dl,
+                       float* dlp, cudaStream_t stream);
+void launch_bwd_dx(const __half* dxr, const int32_t* rowp, const int32_t* idx, const float* dl, const float* Wr,
+                   float* WrT, int T, int d, int E, int k, float* dx, cudaStream_t stream);
+void launch_bwd_dwr(const __nv_bfloat16* xp, const float* dlp, const int32_t* counts, const int32_t* offsets_p,
+                    int E, int d, float* part, float* dbpart, float* dWr, float* db, cudaStream_t stream);
+void launch_gather_rows_by_token(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T,
+                                 int k, int d, __nv_bfloat16* out, cudaStream_t stream);
 
 // selftest
 void launch_selftest_timeout(int32_t* status, uint64_t timeout_ns, cudaStream_t stream);

@@ -8,6 +8,8 @@
 // Interleaving gate and linear rows pairwise puts both halves of SwiGLU for
 // output column j in adjacent accumulator columns of every tile, whatever its
 // width, so the activation runs in the epilogue.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -48,6 +50,28 @@ void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, co
   // W2: [n, d] per expert -> W2p [d, n]
   dim3 g2((d + 31) / 32, (n + 31) / 32, E);
   transpose_pack_kernel<<<g2, 256, 0, stream>>>(W2, W2p, n, d, 0, static_cast<int64_t>(d) * n);
+}
+
+// Backward: W13i[e][i][2j] = W1[e][i][j], W13i[e][i][2j + 1] = W3[e][i][j],
+// the packed weight's transpose, so that dx = [dg du] W13i^T reads it K-major
+// with the same (g, u) column pairing as the pre-activations.
+__global__ void __launch_bounds__(256) interleave_w13_kernel(const __nv_bfloat16* __restrict__ W1,
+                                                             const __nv_bfloat16* __restrict__ W3,
+                                                             __nv_bfloat16* __restrict__ W13i, int64_t pairs) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < pairs;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    __nv_bfloat162 v;
+    v.x = W1[i];
+    v.y = W3[i];
+    reinterpret_cast<__nv_bfloat162*>(W13i)[i] = v;
+  }
+}
+
+void launch_prepare_weights_bwd(const __nv_bfloat16* W1, const __nv_bfloat16* W3, __nv_bfloat16* W13i, int E, int d,
+                                int n, cudaStream_t stream) {
+  const int64_t pairs = static_cast<int64_t>(E) * d * n;
+  const int blocks = static_cast<int>(std::min<int64_t>((pairs + 255) / 256, static_cast<int64_t>(num_sms()) * 32));
+  interleave_w13_kernel<<<blocks, 256, 0, stream>>>(W1, W3, W13i, pairs);
 }
 
 }  // namespace moe

@@ -493,7 +493,7 @@ def sigmoid(z) -> np.ndarray:
 
 
 def moe_backward(x, Wr, bias, W1, W3, W2, dy, k: int, tile: int = 128, mode: str = ROUND_OFF,
-                 seed: int = 0) -> dict:
+                 seed: int = 0, logits=None, magnitudes: bool = False) -> dict:
     """Gradients of the scalar sum_t <dy[t], y[t]> with respect to every input
     of moe_forward, fp64.
 
@@ -518,17 +518,26 @@ def moe_backward(x, Wr, bias, W1, W3, W2, dy, k: int, tile: int = 128, mode: str
     The selection itself is piecewise constant in the logits, so no gradient
     flows through it (nor through token rounding's choice of sets).  Returns
     a dict with dx [T, d], dWr [d, E], db [E], dW1, dW3 [E, d, n], dW2 [E, n, d]
-    and dL [T, E], dw (per token, the list of its set's dw)."""
+    and dL [T, E], dw (per token, the list of its set's dw).  `logits`, as in
+    route(), replaces the gate network's output for the selection and the
+    gate weights (dWr, db and the router part of dx still follow L = x Wr + b).
+    With `magnitudes`, the dict also holds, for dx, dW1, dW3 and dW2, the sum
+    of the absolute values of the terms each element adds up (the same
+    products with every factor replaced by its magnitude): the scale an
+    element's rounding error is measured against."""
     x64 = _f64(x)
     dy64 = _f64(dy)
     T, d = x64.shape
     E, _, n = np.shape(W1)
-    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, seed=seed)
+    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, logits=logits, seed=seed)
     dx = np.zeros((T, d), dtype=F64)
     dW1 = np.zeros((E, d, n), dtype=F64)
     dW3 = np.zeros((E, d, n), dtype=F64)
     dW2 = np.zeros((E, n, d), dtype=F64)
     dw = [np.zeros(len(s), dtype=F64) for s in sets]
+    if magnitudes:
+        mag = {"dx": np.zeros((T, d)), "dW1": np.zeros((E, d, n)), "dW3": np.zeros((E, d, n)),
+               "dW2": np.zeros((E, n, d))}
     for e in range(E):
         pairs = [(t, j) for t, s in enumerate(sets) for j, se in enumerate(s) if int(se) == e]
         if not pairs:
@@ -549,6 +558,12 @@ def moe_backward(x, Wr, bias, W1, W3, W2, dy, k: int, tile: int = 128, mode: str
         dW1[e] = X.T @ dg
         dW3[e] = X.T @ du
         np.add.at(dx, ts, dg @ W1e.T + du @ W3e.T)
+        if magnitudes:
+            aX = np.abs(X)
+            mag["dW2"][e] = np.abs(h).T @ np.abs(w[:, None] * dy64[ts])
+            mag["dW1"][e] = aX.T @ np.abs(dg)
+            mag["dW3"][e] = aX.T @ np.abs(du)
+            np.add.at(mag["dx"], ts, np.abs(dg) @ np.abs(W1e).T + np.abs(du) @ np.abs(W3e).T)
         dwe = np.sum(dh_unweighted * h, axis=1)   # <dy, h W2e>
         for (t, j), v in zip(pairs, dwe):
             dw[t][j] = v
@@ -559,5 +574,9 @@ def moe_backward(x, Wr, bias, W1, W3, W2, dy, k: int, tile: int = 128, mode: str
     dWr = x64.T @ dL
     db = dL.sum(axis=0)
     dx = dx + dL @ _f64(Wr).T
-    return {"dx": dx, "dWr": dWr, "db": db, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dL": dL, "dw": dw,
-            "sets": sets, "weights": weights}
+    out = {"dx": dx, "dWr": dWr, "db": db, "dW1": dW1, "dW3": dW3, "dW2": dW2, "dL": dL, "dw": dw,
+           "sets": sets, "weights": weights}
+    if magnitudes:
+        mag["dx"] += np.abs(dL) @ np.abs(_f64(Wr)).T
+        out.update({key + "_mag": v for key, v in mag.items()})
+    return out

@@ -55,3 +55,21 @@ def valid_topk(L64_row: np.ndarray, chosen, margin: float) -> bool:
     if rest.size == 0:
         return True
     return float(L64_row[chosen].min()) >= float(L64_row[rest].max()) - 2 * margin
+
+
+# Gradients of the backward pass: each element is a sum of products whose
+# bf16-stored operand (the activation gradient, w h) carries one rounding of
+# relative size <= 2^-8, the rest being fp32 arithmetic.  The bar is the
+# elementwise bound |g - g_ref| <= 2^-7 * sum|terms| (twice the rounding, for
+# the fp32 parts) plus the spec mean relative error.
+GRAD_REL = 2.0 ** -7
+
+
+def assert_grad_close(g, g_ref, mag, what="grad"):
+    g64, r64, m64 = to64(g), to64(g_ref), to64(mag)
+    assert np.all(np.isfinite(g64)), f"{what}: non-finite values"
+    s = err_stats(g64, r64)
+    excess = np.abs(g64 - r64) - GRAD_REL * m64
+    assert np.all(excess <= 1e-6 * s["rms"] + 1e-30), f"{what}: {s}, worst excess {excess.max():.3e}"
+    assert s["mean_rel"] <= MEAN_REL, f"{what}: {s}"
+    return s

@@ -117,3 +117,22 @@ def test_product_refuses_cpu_tensors():
     Wr = torch.zeros(64, 4)
     with pytest.raises(ValueError, match="CUDA"):
         B.moe_router_logits(x, Wr, None, None)
+
+
+def test_backward_workspace_and_host_checks(lib):
+    p = ctypes.c_void_p(4096)
+    odd = ctypes.c_void_p(4096 + 8)
+    s = B.make_shape(256, 128, 64, 8, 2)
+    need = B.moe_backward_workspace_bytes(s)
+    # the forward's arrays plus at least the padded x, dy, pre-activation and w*h rows
+    capp = 256 * 2 + 63 * 8
+    assert need >= B.moe_workspace_bytes(s) + capp * (2 * 128 + 2 * 128 + 4 * 64 + 2 * 64)
+    args = [p, p, None, p, p, p, p, p, p, None, p, p, p, p]
+    assert lib.moe_backward(ctypes.byref(s), *args, need - 1, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_backward(ctypes.byref(s), *([None] + args[1:]), need, None) == B.MOE_ERR_INVALID
+    assert lib.moe_backward(ctypes.byref(s), *([odd] + args[1:]), need, None) == B.MOE_ERR_INVALID
+    # unsupported: token rounding, d not a multiple of 128
+    for bad in (B.make_shape(256, 128, 64, 8, 2, tile=128, round="nearest"), B.make_shape(256, 192, 64, 8, 2)):
+        assert B.moe_backward_workspace_bytes(bad) == 0
+        assert lib.moe_backward(ctypes.byref(bad), *args, 1 << 40, None) == B.MOE_ERR_UNSUPPORTED
+    assert lib.moe_prepare_weights_bwd(ctypes.byref(s), p, None, p, None) == B.MOE_ERR_INVALID

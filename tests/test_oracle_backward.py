@@ -135,3 +135,18 @@ def test_backward_is_linear_in_dy():
     g12 = O.moe_backward(*args, dy1 + 2.0 * dy2, k=2)
     for key in KEYS.values():
         np.testing.assert_allclose(g12[key], g1[key] + 2.0 * g2[key], rtol=1e-10, atol=1e-12)
+
+
+def test_magnitudes_bound_the_gradients():
+    """Each magnitude is the sum of |terms| of its element: never below the
+    element itself (triangle inequality), equal to it when no terms cancel."""
+    rng = np.random.default_rng(8)
+    p = _layer(rng, 40, 6, 5, 4)
+    dy = rng.normal(size=(40, 6))
+    g = O.moe_backward(p["x"], p["Wr"], p["bias"], p["W1"], p["W3"], p["W2"], dy, k=2, magnitudes=True)
+    for key in ("dx", "dW1", "dW3", "dW2"):
+        assert np.all(np.abs(g[key]) <= g[key + "_mag"] * (1 + 1e-12) + 1e-300), key
+    # all-positive operands: nothing cancels in dW2 = sum (w h)^T dy when h, dy > 0
+    q = {kk: np.abs(v) for kk, v in p.items()}
+    g2 = O.moe_backward(q["x"], q["Wr"], q["bias"], q["W1"], q["W3"], q["W2"], np.abs(dy), k=2, magnitudes=True)
+    np.testing.assert_allclose(g2["dW2_mag"], g2["dW2"], rtol=1e-12)

@@ -1,0 +1,216 @@
+"""Parity of the backward pass (moe_backward, through the C ABI) against the
+oracle's moe_backward.
+
+Both sides select experts from the same fp32 logits (the oracle is handed the
+GPU's logits for the selection and the gate weights), so the sets agree
+exactly; every gradient must then meet the layer tolerance
+  max |g - g_ref| <= 2e-2 rms(g_ref),  sum |g - g_ref| / sum |g_ref| <= 5e-3
+where the expert-path gradients (dx, dW1, dW3, dW2), whose bf16 operands carry
+one rounding, are held to the elementwise bound |g - g_ref| <= 2^-7 sum|terms|
+instead of the max-error term; identities that hold exactly on the device
+are checked exactly: a
+softmax over one logit passes no gradient (k = 1: dWr = db = 0), an expert
+no token selects gets zero weight gradients, and two runs agree bitwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_layer_93_b300 import binding as B
+from mixture_experts_layer_93_b300 import inputs as I
+from oracle import moe_oracle as O
+
+from moe_testlib import assert_grad_close, assert_moe_close, to64
+
+pytestmark = pytest.mark.gpu
+
+GRADS = [("dx", "dx"), ("dWr", "dWr"), ("dbias", "db"), ("dW1", "dW1"), ("dW3", "dW3"), ("dW2", "dW2")]
+
+
+def check_grads(out, ref, skip=()):
+    for key, rkey in GRADS:
+        if key in skip:
+            continue
+        if rkey + "_mag" in ref:
+            assert_grad_close(out[key], ref[rkey], ref[rkey + "_mag"], what=key)
+        else:
+            assert_moe_close(out[key], ref[rkey], what=key)
+
+
+def _setup(cfg, dev, seed, dead_expert=False):
+    inp = I.make_inputs(cfg, device=dev, seed=seed)
+    if dead_expert:
+        bias = torch.zeros(cfg.E, device=dev) if inp["bias"] is None else inp["bias"].clone()
+        bias[-1] = -1.0e4  # never selected
+        inp["bias"] = bias
+    g = torch.Generator(device="cpu").manual_seed(seed + 1)
+    dy = torch.randn(cfg.T, cfg.d, generator=g).to(torch.bfloat16).to(dev)
+    s = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k)
+    W13p, _ = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    W13i = B.moe_prepare_weights_bwd(inp["W1"], inp["W3"])
+    return inp, dy, s, W13p, W13i
+
+
+def _run(inp, dy, s, W13p, W13i, dev):
+    ws = B.Workspace(s, dev, backward=True)
+    out = B.moe_backward(s, inp["x"], inp["Wr"], inp["bias"], W13p, W13i, inp["W2"], dy, ws)
+    torch.cuda.synchronize()
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    logits = ws.view("logits", torch.float32, s.T * s.E).view(s.T, s.E).clone()
+    return out, logits
+
+
+SHAPES = [  # T, d, n, E, k: single-SM and SM-pair tiles, ragged experts, n % 128 != 0
+    (256, 128, 64, 8, 2),
+    (700, 256, 128, 6, 2),
+    (600, 512, 256, 5, 3),
+    (300, 384, 192, 4, 2),
+    (500, 256, 64, 64, 4),
+    (129, 256, 320, 3, 3),
+]
+
+
+@pytest.mark.parametrize("T,d,n,E,k", SHAPES)
+def test_backward_matches_oracle(cuda_device, T, d, n, E, k):
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="normal", bias_scale=0.5)
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=T + d + E)
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    ref = O.moe_backward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], dy, k=k,
+                         logits=logits.cpu().numpy(), magnitudes=True)
+    check_grads(out, ref)
+
+
+def test_backward_k1_has_no_router_gradient(cuda_device):
+    cfg = I.MoEConfig("t", T=300, d=256, n=128, E=5, k=1, bias="normal", bias_scale=0.5)
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=3)
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    assert torch.all(out["dWr"] == 0) and torch.all(out["dbias"] == 0)
+    ref = O.moe_backward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], dy, k=1,
+                         logits=logits.cpu().numpy(), magnitudes=True)
+    check_grads(out, ref, skip=("dWr", "dbias"))
+
+
+def test_backward_unselected_expert_gets_zero(cuda_device):
+    cfg = I.MoEConfig("t", T=400, d=256, n=128, E=6, k=2, bias="normal", bias_scale=0.5)
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=4, dead_expert=True)
+    ws = B.Workspace(s, cuda_device, backward=True)
+    # poison the outputs: every element must be written
+    out = {k: torch.full(shape, float("nan"), device=cuda_device) for k, shape in
+           [("dx", (400, 256)), ("dWr", (256, 6)), ("dbias", (6,)), ("dW1", (6, 256, 128)), ("dW3", (6, 256, 128)),
+            ("dW2", (6, 128, 256))]}
+    B.moe_backward(s, inp["x"], inp["Wr"], inp["bias"], W13p, W13i, inp["W2"], dy, ws, out=out)
+    torch.cuda.synchronize()
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    counts = ws.view("counts", torch.int32, 6).cpu()
+    assert counts[-1] == 0
+    for key in ("dW1", "dW3", "dW2"):
+        assert torch.all(out[key][-1] == 0), key
+        assert torch.isfinite(out[key]).all(), key
+    assert torch.all(out["dWr"][:, -1] == 0) and out["dbias"][-1] == 0
+    logits = ws.view("logits", torch.float32, 400 * 6).view(400, 6).cpu().numpy()
+    ref = O.moe_backward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], dy, k=2, logits=logits, magnitudes=True)
+    check_grads(out, ref)
+
+
+def test_backward_is_deterministic(cuda_device):
+    cfg = I.MoEConfig("t", T=900, d=256, n=256, E=8, k=2, bias="normal", bias_scale=0.5)
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=5)
+    a, _ = _run(inp, dy, s, W13p, W13i, cuda_device)
+    b, _ = _run(inp, dy, s, W13p, W13i, cuda_device)
+    for key, _ in GRADS:
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_backward_tiny_config(cuda_device):
+    cfg = I.get_config("tiny")
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=0)
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    ref = O.moe_backward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], dy, k=cfg.k,
+                         logits=logits.cpu().numpy(), magnitudes=True)
+    check_grads(out, ref)
+    # the logit gradient of every token sums to zero, so do dbias and the rows of dWr
+    dWr = to64(out["dWr"])
+    assert np.all(np.abs(dWr.sum(axis=1)) <= 1e-4 * np.abs(dWr).max() * cfg.E)
+
+
+def _sampled_reference(inp, dy, logits, k, e, J, toks):
+    """fp64 gradients the oracle's formulas give for expert e's channels J
+    (dW1[e][:, J], dW3[e][:, J], dW2[e][J, :]) and for the tokens `toks`
+    (dx), with their magnitudes; selection and gate weights from the fp32
+    logits, as moe_backward (oracle) takes them."""
+    L = logits.astype(np.float64)
+    idx = O.topk(L, k)
+    w = O.gate_weights(L, idx)
+    x64 = to64(inp["x"])
+    dy64 = to64(dy)
+    rows = np.argwhere(idx == e)               # (t, j) pairs routed to e, in token order
+    ts, js = rows[:, 0], rows[:, 1]
+    we = w[ts, js]
+    W1J, W3J = to64(inp["W1"][e][:, J]), to64(inp["W3"][e][:, J])
+    W2J = to64(inp["W2"][e][J, :])
+    X = x64[ts]
+    g, u = X @ W1J, X @ W3J
+    s = O.sigmoid(g)
+    a = g * s
+    h = a * u
+    dh = we[:, None] * (dy64[ts] @ W2J.T)
+    dg, du = dh * u * (s * (1 + g * (1 - s))), dh * a
+    out = {"dW1": X.T @ dg, "dW3": X.T @ du, "dW2": (we[:, None] * h).T @ dy64[ts],
+           "dW1_mag": np.abs(X).T @ np.abs(dg), "dW3_mag": np.abs(X).T @ np.abs(du),
+           "dW2_mag": np.abs(we[:, None] * h).T @ np.abs(dy64[ts])}
+    # dx of sampled tokens: every selected expert in full, plus the gate network
+    Wr = to64(inp["Wr"])
+    dx = np.zeros((len(toks), x64.shape[1]))
+    mag = np.zeros_like(dx)
+    cache = {}
+    for i, t in enumerate(toks):
+        dws = []
+        for j in range(k):
+            ej = int(idx[t, j])
+            if ej not in cache:
+                if len(cache) >= 4:  # bound the host memory of widened weights
+                    cache.clear()
+                cache[ej] = (to64(inp["W1"][ej]), to64(inp["W3"][ej]), to64(inp["W2"][ej]))
+            W1e, W3e, W2e = cache[ej]
+            gt, ut = x64[t] @ W1e, x64[t] @ W3e
+            st = O.sigmoid(gt)
+            at = gt * st
+            dhu = dy64[t] @ W2e.T
+            dws.append(float(dhu @ (at * ut)))
+            dgt, dut = w[t, j] * dhu * ut * (st * (1 + gt * (1 - st))), w[t, j] * dhu * at
+            dx[i] += W1e @ dgt + W3e @ dut
+            mag[i] += np.abs(W1e) @ np.abs(dgt) + np.abs(W3e) @ np.abs(dut)
+        dws = np.array(dws)
+        dl = w[t] * (dws - np.dot(w[t], dws))
+        dx[i] += Wr[:, idx[t]] @ dl
+        mag[i] += np.abs(Wr[:, idx[t]]) @ np.abs(dl)
+    out.update(dx=dx, dx_mag=mag)
+    return out
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixtral", "dsv3"])
+def test_backward_full_size_sampled(cuda_device, name):
+    """The full-size layers in the bench's launch configuration: sampled
+    weight-gradient channels of two experts and sampled tokens' dx against
+    the oracle's formulas; dWr and dbias by the zero sum over experts."""
+    cfg = I.get_config(name)
+    inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=0)
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    logits = logits.cpu().numpy()
+    rng = np.random.default_rng(1)
+    toks = np.sort(rng.choice(cfg.T, size=6, replace=False))
+    for e in rng.choice(cfg.E, size=2, replace=False):
+        J = np.sort(rng.choice(cfg.n, size=6, replace=False))
+        ref = _sampled_reference(inp, dy, logits, cfg.k, int(e), J, toks)
+        Jt = torch.from_numpy(J).to(cuda_device)
+        assert_grad_close(out["dW1"][e][:, Jt], ref["dW1"], ref["dW1_mag"], what=f"dW1[{e}]")
+        assert_grad_close(out["dW3"][e][:, Jt], ref["dW3"], ref["dW3_mag"], what=f"dW3[{e}]")
+        assert_grad_close(out["dW2"][e][Jt, :], ref["dW2"], ref["dW2_mag"], what=f"dW2[{e}]")
+    assert_grad_close(out["dx"][torch.from_numpy(toks).to(cuda_device)], ref["dx"], ref["dx_mag"], what="dx")
+    dWr = to64(out["dWr"])
+    assert np.all(np.abs(dWr.sum(axis=1)) <= 1e-4 * np.sqrt(np.mean(dWr ** 2)) * cfg.E)
+    db = to64(out["dbias"])
+    assert abs(db.sum()) <= 1e-4 * np.sqrt(np.mean(db ** 2)) * cfg.E
+    del out
+    torch.cuda.empty_cache()
