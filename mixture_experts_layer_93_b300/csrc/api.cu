@@ -92,7 +92,7 @@ int64_t layout_bwd(const moe_shape* s, int64_t* off_fwd, int64_t* off) {
   const int64_t S = bwd_dwr_splits(s->E, s->d);
   const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4,
                                        capp * d * 2, capp * d * 2, capp * 2 * n * 4,
-                                       capp * 2 * n * 2, capp * n * 2, capp * (n / bwd_act_block(s->n)) * 4, capp * d * 2,
+                                       capp * 2 * n * 2, capp * n * 2, capp * bwd_act_parts(s->n) * 4, capp * d * 2,
                                        A * 4,        capp * 4,     E * d * 4,
                                        S * E * d * 4, S * E * 4};
   int64_t pos = base;
@@ -510,7 +510,7 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
                            n, E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
   // 4. gate weights -> logits
-  launch_router_bwd(rowp, w, dw_part, n / bwd_act_block(n), T, k, dl, dlp, st);
+  launch_router_bwd(rowp, w, dw_part, bwd_act_parts(n), T, k, dl, dlp, st);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 5. weight gradients: dW2 = (w h)^T dy, dW1 / dW3 = x^T (dg, du)
   if ((rc = launch_wgrad(dyp, hw, counts, offsets_p, d, n, E, capp, dW2, nullptr, status, kDefaultTimeoutNs, st)) !=

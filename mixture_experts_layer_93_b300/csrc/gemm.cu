@@ -772,22 +772,24 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           // outputs), one partial per row and n-block.
           const int64_t ld2 = 2 * p.out_ld;
           float dw_acc = 0.f;
+          // 16 channels per step: 16 accumulator columns, 32 fp32
+          // pre-activations (128 bytes of this thread's row)
 #pragma unroll 1
-          for (int c = ch * (BN / NCH); c < (ch + 1) * (BN / NCH); c += 32) {
+          for (int c = ch * (BN / NCH); c < (ch + 1) * (BN / NCH); c += 16) {
             const int64_t j0 = static_cast<int64_t>(nb) * BN + c;
-            uint32_t v[32];
-            tmem_ld32(taddr + c, v);
-            float4 pre[16];
+            uint32_t v[16];
+            tmem_ld16(taddr + c, v);
+            float4 pre[8];
             const float4* src = reinterpret_cast<const float4*>(p.pre + row * ld2 + 2 * j0);
             if (valid) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) pre[i] = src[i];
+              for (int i = 0; i < 8; ++i) pre[i] = src[i];
             }
             tc_wait_ld();
             if (valid) {
-              uint32_t og[32], oh[16];
+              uint32_t og[16], oh[8];
 #pragma unroll
-              for (int q = 0; q < 32; ++q) {
+              for (int q = 0; q < 16; ++q) {
                 const float g = (&pre[q >> 1].x)[2 * (q & 1)], u = (&pre[q >> 1].x)[2 * (q & 1) + 1];
                 const float sg = 1.0f / (1.0f + __expf(-g));
                 const float a = g * sg;
@@ -805,10 +807,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
               }
               uint4* dg = reinterpret_cast<uint4*>(p.out_bf16 + row * ld2 + 2 * j0);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) dg[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
+              for (int i = 0; i < 4; ++i) dg[i] = make_uint4(og[4 * i], og[4 * i + 1], og[4 * i + 2], og[4 * i + 3]);
               uint4* dhw = reinterpret_cast<uint4*>(p.out2_bf16 + row * p.out_ld + j0);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) dhw[i] = make_uint4(oh[4 * i], oh[4 * i + 1], oh[4 * i + 2], oh[4 * i + 3]);
+              for (int i = 0; i < 2; ++i) dhw[i] = make_uint4(oh[4 * i], oh[4 * i + 1], oh[4 * i + 2], oh[4 * i + 3]);
             }
           }
           if (valid) p.out2_f32[row * p.parts + nb * NCH + ch] = dw_acc;
@@ -893,10 +895,17 @@ static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
                        cudaStream_t stream) {
   const bool wide = ((MODE == kModeUp || MODE == kModeUpF8 || MODE == kModeUpPre) && p.num_kb <= 24) ||
                     ((MODE == kModeDown || MODE == kModeDownF8) && p.num_kb <= 8);
-  if constexpr (MODE != kModeRouter && MODE != kModeBwdAct && MODE != kModeWgrad) {
-    if (wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+  if constexpr (MODE == kModeBwdAct) {
+    // the SwiGLU backward's epilogue (fp32 pre-activation loads, the
+    // activation's derivative) outlasts a tile's MMAs with four warps
+    (void)wide;
+    return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+  } else {
+    if constexpr (MODE != kModeRouter && MODE != kModeWgrad) {
+      if (wide) return launch_gemm_epi<BN, MODE, PAIR, 8>(tmA, tmB, tmC, p, stream);
+    }
+    return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
   }
-  return launch_gemm_epi<BN, MODE, PAIR, 4>(tmA, tmB, tmC, p, stream);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1282,7 +1291,7 @@ int launch_bwd_act(const __nv_bfloat16* dyp, const __nv_bfloat16* W2, const int3
   p.out2_bf16 = hw;
   p.out2_f32 = dw_part;
   p.out_ld = n;
-  p.parts = n / BN;
+  p.parts = bwd_act_parts(n);
   p.E = E;
   p.num_kb = d / 64;
   p.n_blocks = n / BN;

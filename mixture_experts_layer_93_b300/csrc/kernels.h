@@ -66,6 +66,8 @@ void launch_gather_rows(const __nv_bfloat16* x, const int32_t* row_token, const 
 inline int up_half_block(int n) { return (n % 128 == 0) ? 128 : 64; }
 // backward GEMMs (gemm.cu)
 inline int bwd_act_block(int n) { return (n % 256 == 0) ? 256 : (n % 128 == 0 ? 128 : 64); }
+// partial sums of <dh', h> per row: one per n-block and epilogue column half
+inline int bwd_act_parts(int n) { return 2 * (n / bwd_act_block(n)); }
 int launch_expert_up_pre(const __nv_bfloat16* xp, const __nv_bfloat16* W13p, const int32_t* counts,
                          const int32_t* offsets, float* gl, int d, int n, int E, int64_t rows_cap,
                          int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
