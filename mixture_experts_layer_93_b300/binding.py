@@ -451,7 +451,10 @@ class MoELayer:
         self.Wr = Wr.contiguous()
         self.bias = bias.contiguous() if bias is not None else None
         self.W13p, self.W2p = moe_prepare_weights(W1.contiguous(), W3.contiguous(), W2.contiguous())
+        self.W13i = None          # backward only: W1/W3 interleaved, built on the first backward
+        self._W1, self._W3, self._W2 = W1, W3, W2
         self._ws = {}
+        self._bws = {}
 
     def shape(self, T: int) -> moe_shape:
         return make_shape(T, self.d, self.n, self.E, self.k, self.tile, self.round, self.seed)
@@ -468,3 +471,19 @@ class MoELayer:
         return moe_forward(self.shape(T), x, self.Wr, self.bias, self.W13p, self.W2p, ws, y)
 
     __call__ = forward
+
+    def backward_workspace(self, T: int, device) -> Workspace:
+        key = (T, str(device))
+        if key not in self._bws:
+            self._bws[key] = Workspace(self.shape(T), device, backward=True)
+        return self._bws[key]
+
+    def backward(self, x, dy) -> dict:
+        """Gradients of sum <dy, forward(x)>: {dx, dWr, dbias, dW1, dW3, dW2}
+        (fp32), by recomputation (moe_backward); dy bf16 [T, d]."""
+        if self.W13i is None:
+            self.W13i = moe_prepare_weights_bwd(self._W1.contiguous(), self._W3.contiguous())
+        T = x.shape[0]
+        ws = self.backward_workspace(T, x.device)
+        return moe_backward(self.shape(T), x, self.Wr, self.bias, self.W13p, self.W13i, self._W2.contiguous(), dy,
+                            ws, want_dbias=self.bias is not None)
