@@ -79,6 +79,7 @@ struct GemmParams {
   int m_units;               // Wgrad: M tile units per group
   int64_t out_group_stride;  // Wgrad: elements between the outputs of consecutive groups
   int interleave;            // Wgrad: even M rows go to out_f32, odd ones to out2_f32, at row M / 2
+  int m_fast;                // Wgrad: tile order within a group, M units fastest (else N blocks)
 };
 
 constexpr int kProducerWarps = 4;
@@ -194,14 +195,20 @@ __device__ __forceinline__ void group_rows(const GemmParams& p, const int2* grp_
 }
 
 // Weight-gradient tiles: every group has m_units x n_blocks tiles (empty
-// groups too: their gradient is zero), n fastest, so the tiles that run
-// together share the group's A columns and its whole B.
+// groups too: their gradient is zero).  The tiles that run together share
+// one operand block and sweep the other operand of the group, which should
+// be the smaller one (it then stays in L2): n fastest sweeps B, m fastest A.
 __device__ __forceinline__ void wgrad_tile(int tau, const GemmParams& p, int& e, int& mu, int& nb) {
   const int per = p.m_units * p.n_blocks;
   e = tau / per;
   const int local = tau - e * per;
-  mu = local / p.n_blocks;
-  nb = local - mu * p.n_blocks;
+  if (p.m_fast) {
+    nb = local / p.m_units;
+    mu = local - nb * p.m_units;
+  } else {
+    mu = local / p.n_blocks;
+    nb = local - mu * p.n_blocks;
+  }
 }
 
 template <int BN, int MODE, bool PAIR, int EPI>
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (MODE != kModeRouter && MODE != kModeBwdAct && MODE != kModeWgrad) tma_prefetch_desc(&tmC);
+    if (MODE != kModeRouter && MODE != kModeBwdAct && MODE != kModeWgrad) tma_prefetch_desc(&tmC);  // UpPre: fp32 boxes
   } else if (warp == kMmaWarp) {
     if (PAIR) {
       tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
@@ -748,17 +755,18 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (valid && !(fabsf(wr) * amax <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
         } else if constexpr (MODE == kModeUpPre) {
           // the accumulator itself, (g, u) pairs of the packed W1/W3 rows, in
-          // fp32: 128 contiguous bytes of this thread's row per 32 columns
+          // fp32, through the TMA-store boxes as 32 rows x 16 columns (64-byte rows)
           float* dst = p.out_f32 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
 #pragma unroll 1
           for (int c = ch * (BN / NCH); c < (ch + 1) * (BN / NCH); c += 32) {
             uint32_t v[32];
             tmem_ld32(taddr + c, v);
             tc_wait_ld();
-            if (valid) {
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) d4[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            if (warp_rows > 0) {
+              const uint32_t(&lo)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&v[0]);
+              const uint32_t(&hi)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&v[16]);
+              store_chunk(lo, nb * BN + c, row_w0, warp_rows, row, dst + c);
+              store_chunk(hi, nb * BN + c + 16, row_w0, warp_rows, row, dst + c + 16);
             }
           }
         } else if constexpr (MODE == kModeBwdAct) {
@@ -954,6 +962,19 @@ static bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 output tile for the epilogue's TMA stores: box [32 rows, 16], 64-byte swizzle.
+static bool make_map_out32(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 4};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1254,10 +1275,10 @@ int launch_expert_up_pre(const __nv_bfloat16* xp, const __nv_bfloat16* W13p, con
                          const int32_t* offsets, float* gl, int d, int n, int E, int64_t rows_cap,
                          int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
   const int BN = (n % 128 == 0) ? 256 : 128;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmC;
   if (!make_map_bf16(&tmA, xp, d, rows_cap, 128)) return MOE_ERR_CUDA;
   if (!make_map_bf16(&tmB, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN / 2)) return MOE_ERR_CUDA;
-  const CUtensorMap& tmC = tmA;  // the epilogue stores directly
+  if (!make_map_out32(&tmC, gl, 2 * static_cast<uint64_t>(n), rows_cap)) return MOE_ERR_CUDA;
   GemmParams p = base_params(status, timeout_ns);
   p.counts = counts;
   p.offsets = offsets;
@@ -1328,6 +1349,7 @@ int launch_wgrad(const __nv_bfloat16* A, const __nv_bfloat16* B, const int32_t* 
   p.num_kb = 0;
   p.n_blocks = N / BN;
   p.m_units = M / (pair ? 256 : 128);
+  p.m_fast = M < N;  // sweep the narrower operand
   p.units = 0;
   const CUtensorMap& tmC = tmA;
   if (pair)
