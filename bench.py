@@ -344,12 +344,13 @@ def run_backward(args, world, rank, local):
         return
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    # launches per moe_backward: route + permute (5, or 6 when E > 256), padded
+    # launches per moe_backward: route + permute (4, 5 or 6, as the forward), padded
     # rows (2), zero padding, two gathers, pre-activations, SwiGLU backward,
     # router backward, dW2, dW1/dW3, dx rows (1, or 2 with separate odd
     # blocks), router transpose, dx, dWr partial and final
     dx_launches = 1 if 128.0 * E <= 0.15 * (T * k + 63 * E) else 2
-    launches = (5 if E <= 256 else 6) + 2 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
+    fused_route = 4 if (E <= 64 and k <= 8) else (5 if E <= 256 else 6)
+    launches = fused_route + 2 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -439,7 +440,8 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     # rounding off: route+permute fused (Wr split, router GEMM, fused top-k +
-    # histogram, scan, scatter: 5 launches; 6 when E > 256); rounding: route
+    # histogram, scan, scatter: 5 launches; 4 when E <= 64 and k <= 8, where
+    # the router GEMM's epilogue takes the top-k; 6 when E > 256); rounding: route
     # (Wr split, router GEMM, top-k: 3) then member, select, transpose, 2
     # offsets, sets + a 3-launch permutation (9).  up: row gather + SM-pair GEMM
     # + odd-block GEMM (A path 0) or one GEMM (paths 1, 2); down: SM-pair +
@@ -453,7 +455,8 @@ def run_ours(args, world, rank, local):
     if args.fp8:
         up_launches = 2  # quantising gather + one SM-pair e4m3 GEMM
         gemm_launches = 2  # down: h quantisation + one SM-pair e4m3 GEMM
-    route_launches = (5 if E <= 256 else 6) if mode == "off" else 3 + 9
+    fused_route = 4 if (E <= 64 and k <= 8) else (5 if E <= 256 else 6)
+    route_launches = fused_route if mode == "off" else 3 + 9
     launches_per_step = route_launches + up_launches + gemm_launches + 1
 
     def check(rc, what):

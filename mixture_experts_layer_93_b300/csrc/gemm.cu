@@ -32,6 +32,7 @@
 // copies land, frees its TMEM and returns.
 #include "common.cuh"
 #include "kernels.h"
+#include "topk.cuh"
 
 #include <algorithm>
 
@@ -80,6 +81,12 @@ struct GemmParams {
   int64_t out_group_stride;  // Wgrad: elements between the outputs of consecutive groups
   int interleave;            // Wgrad: even M rows go to out_f32, odd ones to out2_f32, at row M / 2
   int m_fast;                // Wgrad: tile order within a group, M units fastest (else N blocks)
+  // Router with the top-k fused (topk_k > 0): the tile covers every expert
+  int32_t* topk_idx;         // [T * k]
+  float* topk_w;             // [T * k]
+  int topk_k;                // <= kFusedTopk
+  int32_t* chunk_hist;       // [E * nchunks], zero on entry
+  int nchunks;
 };
 
 constexpr int kProducerWarps = 4;
@@ -824,31 +831,71 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (valid) p.out2_f32[row * p.parts + nb * NCH + ch] = dw_acc;
         } else if constexpr (MODE == kModeRouter) {
           if (ch == 0) {
-          // router (first four epilogue warps only): the three column groups
-          // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum plus
-          // the bias is the logit
-          constexpr int EB = BN / 3;
-          const int e0 = nb * EB;
-          float* dst = p.out_f32 + row * p.out_ld;
-#pragma unroll 1
-          for (int c = 0; c < EB; c += 16) {
-            uint32_t a[16], b[16], q[16];
-            tmem_ld16(taddr + c, a);
-            tmem_ld16(taddr + EB + c, b);
-            tmem_ld16(taddr + 2 * EB + c, q);
-            tc_wait_ld();
-            if (valid) {
+            // router (first four epilogue warps only): the three column groups
+            // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum
+            // plus the bias is the logit.  With topk_k > 0 the tile spans
+            // every expert, and the thread also takes its token's top-k
+            // (the 64-bit keys of topk.cuh, kept sorted by insertion), the
+            // gate weights and the chunk histogram, as topk_perm_hist_kernel
+            // does from the stored logits.
+            constexpr int EB = BN / 3;
+            const int e0 = nb * EB;
+            float* dst = p.out_f32 + row * p.out_ld;
+            uint64_t best[kFusedTopk];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int ecol = e0 + c + j;
-                if (ecol < p.out_cols) {
-                  float v = (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(q[j]);
-                  if (p.bias) v += p.bias[ecol];
-                  dst[ecol] = v;
+            for (int i = 0; i < kFusedTopk; ++i) best[i] = 0;  // below every real key
+            bool nan_seen = false;
+#pragma unroll 1
+            for (int c = 0; c < EB; c += 16) {
+              uint32_t a[16], b[16], q[16];
+              tmem_ld16(taddr + c, a);
+              tmem_ld16(taddr + EB + c, b);
+              tmem_ld16(taddr + 2 * EB + c, q);
+              tc_wait_ld();
+              if (valid) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  const int ecol = e0 + c + j;
+                  if (ecol < p.out_cols) {
+                    float v = (__uint_as_float(a[j]) + __uint_as_float(b[j])) + __uint_as_float(q[j]);
+                    if (p.bias) v += p.bias[ecol];
+                    dst[ecol] = v;
+                    if (p.topk_k > 0) {
+                      nan_seen |= (v != v);
+                      uint64_t key = topk_key(v, ecol);
+#pragma unroll
+                      for (int i = 0; i < kFusedTopk; ++i) {  // insert, carrying the smaller key down
+                        const uint64_t hi = best[i] > key ? best[i] : key;
+                        key = best[i] > key ? key : best[i];
+                        best[i] = hi;
+                      }
+                    }
+                  }
                 }
               }
             }
-          }
+            if (p.topk_k > 0 && valid) {
+              if (nan_seen) report_error(p.status, MOE_ERR_DEVICE_CHECK, static_cast<int32_t>(row));
+              // softmax over the selected logits, the sum in slot order
+              const float vmax = topk_key_value(best[0]);
+              float ex[kFusedTopk];
+              float sum = 0.f;
+#pragma unroll
+              for (int j = 0; j < kFusedTopk; ++j) {
+                ex[j] = j < p.topk_k ? expf(topk_key_value(best[j]) - vmax) : 0.f;
+                if (j < p.topk_k) sum += ex[j];
+              }
+#pragma unroll
+              for (int j = 0; j < kFusedTopk; ++j) {
+                if (j < p.topk_k) {
+                  const int64_t a_ = row * p.topk_k + j;
+                  const int32_t e = topk_key_expert(best[j]);
+                  p.topk_idx[a_] = e;
+                  p.topk_w[a_] = ex[j] / sum;
+                  atomicAdd(&p.chunk_hist[static_cast<int64_t>(e) * p.nchunks + a_ / kPermChunk], 1);
+                }
+              }
+            }
           }
         }
         tc_fence_before();
@@ -1363,7 +1410,8 @@ int launch_wgrad(const __nv_bfloat16* A, const __nv_bfloat16* B, const int32_t* 
 int router_expert_block(int E) { return E <= 16 ? 16 : (E <= 32 ? 32 : 64); }
 
 int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
-                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream, int k,
+                     int32_t* topk_idx, float* topk_w, int32_t* chunk_hist) {
   const int EB = router_expert_block(E);
   const int BN = 3 * EB;
   const int nblk = (E + EB - 1) / EB;
@@ -1385,6 +1433,14 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
   p.b_rows_per_expert = 0;
   p.gather = 0;
   p.units = 3;  // pairs of 128-row blocks; an odd last block runs as a half-empty pair
+  if (k > 0) {
+    if (!router_fuses_topk(E, k) || !topk_idx || !topk_w || !chunk_hist) return MOE_ERR_INVALID;
+    p.topk_k = k;
+    p.topk_idx = topk_idx;
+    p.topk_w = topk_w;
+    p.chunk_hist = chunk_hist;
+    p.nchunks = static_cast<int>(perm_num_chunks(static_cast<int64_t>(T) * k));
+  }
   if (BN == 48) return launch_gemm<48, kModeRouter, true>(tmA, tmB, tmC, p, stream);
   if (BN == 96) return launch_gemm<96, kModeRouter, true>(tmA, tmB, tmC, p, stream);
   return launch_gemm<192, kModeRouter, true>(tmA, tmB, tmC, p, stream);

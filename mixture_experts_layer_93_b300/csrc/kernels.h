@@ -22,6 +22,11 @@ inline int64_t perm_num_chunks(int64_t A) { return (A + kPermChunk - 1) / kPermC
 void launch_topk_permute(const float* logits, int T, int E, int k, int32_t* idx, float* w, int32_t* chunk_hist,
                          int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
                          float* row_w, int32_t* status, cudaStream_t stream);
+// The scan and the scatter of launch_topk_permute, for chunk counts already
+// made (by the router epilogue).
+void launch_perm_scan_scatter(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
+                              int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                              float* row_w, cudaStream_t stream);
 void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
                     int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
                     float* row_w, int32_t* status, cudaStream_t stream);
@@ -85,8 +90,14 @@ size_t router_split_elems(int d, int E);
 // kernel (its chunk counts).
 void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cudaStream_t stream,
                          int32_t* zero = nullptr, int64_t zero_count = 0);
+// k > 0 (router_fuses_topk): the epilogue also writes the top-k ids and gate
+// weights and counts them into chunk_hist (zero on entry), as the fused
+// top-k + histogram kernel does.
+constexpr int kFusedTopk = 8;
+inline bool router_fuses_topk(int E, int k) { return E <= 64 && k <= kFusedTopk; }
 int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
-                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+                     int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream, int k = 0,
+                     int32_t* topk_idx = nullptr, float* topk_w = nullptr, int32_t* chunk_hist = nullptr);
 
 // combine.cu
 void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, float* y, int T, int d,

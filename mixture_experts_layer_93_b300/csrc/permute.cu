@@ -278,6 +278,13 @@ void launch_topk_permute(const float* logits, int T, int E, int k, int32_t* idx,
             : nv <= 4 ? topk_perm_hist_kernel<4>
                       : topk_perm_hist_kernel<8>;
   launch_pdl(kern, (T + 7) / 8, 256, 0, stream, 1, logits, T, E, k, idx, w, nchunks, chunk_hist, status);
+  launch_perm_scan_scatter(idx, w, A, k, E, chunk_hist, counts, offsets, src, dst, row_token, row_w, stream);
+}
+
+void launch_perm_scan_scatter(const int32_t* idx, const float* w, int64_t A, int k, int E, int32_t* chunk_hist,
+                              int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
+                              float* row_w, cudaStream_t stream) {
+  const int nchunks = static_cast<int>(perm_num_chunks(A));
   launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, 1, chunk_hist, E, nchunks, counts, offsets);
   launch_pdl(perm_scatter_kernel, nchunks, kPermWarps * 32, static_cast<size_t>(kPermWarps) * E * sizeof(int32_t),
              stream, 1, static_cast<const int32_t*>(idx), static_cast<const float*>(w),
