@@ -255,7 +255,7 @@ def run_backward(args, world, rank, local):
     if args.tokens:
         cfg = cfg.with_tokens(args.tokens)
     T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
-    shape = B.make_shape(T, d, n, E, k)
+    shape = B.make_shape(T, d, n, E, k, cfg.tile, args.round, args.seed)
     inp = I.make_inputs(cfg, device=dev, seed=rank)
     g = torch.Generator(device=dev).manual_seed(1000 + rank)
     dy = torch.randn(T, d, generator=g, device=dev).to(torch.bfloat16)
@@ -345,17 +345,23 @@ def run_backward(args, world, rank, local):
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     # launches per moe_backward: route + permute (4, 5 or 6, as the forward), padded
-    # rows (2), zero padding, two gathers, pre-activations, SwiGLU backward,
+    # offsets and rows (2), expert of each row, zero padding, two gathers,
+    # pre-activations, SwiGLU backward,
     # router backward, dW2, dW1/dW3, dx rows (1, or 2 with separate odd
     # blocks), router transpose, dx, dWr partial and final
-    dx_launches = 1 if 128.0 * E <= 0.15 * (T * k + 63 * E) else 2
+    capp = T * k + (E * cfg.tile if args.round != "off" else 0) + 63 * E
+    dx_launches = 1 if 128.0 * E <= 0.15 * capp else 2
+    # (rounding: route 3 + round 9 in place of route + permute, and no rows kernel)
     fused_route = 4 if (E <= 64 and k <= 8) else (5 if E <= 256 else 6)
-    launches = fused_route + 2 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
+    if args.round != "off":
+        fused_route = 3 + 9 - 1
+    launches = fused_route + 2 + 1 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.description + ", backward pass", "T": T, "d": d, "n": n, "E": E, "k": k,
+                   "round": args.round, "tile": cfg.tile if args.round != "off" else None,
                    "flops_per_step": flops, "outputs": "dx, dWr, dbias, dW1, dW3, dW2 in fp32",
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},

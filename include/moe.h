@@ -335,8 +335,9 @@ int moe_forward_fp8(const moe_shape* s, const void* x, const float* Wr, const fl
  * GEMMs' operands), each row's input gradient from the experts in fp16
  * (saturation is reported as for ys);
  * every sum runs in a fixed order, so results are bitwise reproducible.
- * Requires round == MOE_ROUND_OFF, d % 128 == 0 (n % 64 == 0 as always),
- * else MOE_ERR_UNSUPPORTED. */
+ * With token rounding (s->round != MOE_ROUND_OFF) the rounded sets of the
+ * forward are recomputed and held fixed the same way.  Requires d % 128 == 0
+ * (n % 64 == 0 as always), else MOE_ERR_UNSUPPORTED. */
 
 /* Workspace bytes of moe_backward (0 for an invalid or unsupported shape). */
 size_t moe_backward_workspace_bytes(const moe_shape* s);

@@ -81,19 +81,21 @@ int check_ws(const moe_shape* s, void* ws, size_t ws_bytes, bool fp8 = false) {
 // Backward workspace: the forward's slots, then the backward's arrays over
 // the padded row layout (each expert's rows padded to a multiple of 64).
 enum BwdSlot {
-  kOffP, kRowP, kWp, kXp, kDyp, kGl, kDgl, kHw, kDwPart, kDxr, kDl, kDlp, kWrT, kDwrPart, kDbPart, kNumBwdSlots
+  kOffP, kRowP, kWp, kEpr, kXp, kDyp, kGl, kDgl, kHw, kDwPart, kDxr, kDl, kDlp, kWrT, kDwrPart, kDbPart,
+  kNumBwdSlots
 };
 
-inline int64_t padded_cap(const moe_shape* s) { return static_cast<int64_t>(s->T) * s->k + 63 * int64_t(s->E); }
+// rows of the padded layout: the forward's rows plus up to 63 padding rows per expert
+inline int64_t padded_cap(const moe_shape* s) { return row_cap(s) + 63 * int64_t(s->E); }
 
 int64_t layout_bwd(const moe_shape* s, int64_t* off_fwd, int64_t* off) {
   const int64_t base = layout(s, off_fwd);
   const int64_t T = s->T, E = s->E, A = T * s->k, capp = padded_cap(s), d = s->d, n = s->n;
   const int64_t S = bwd_dwr_splits(s->E, s->d);
-  const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4,
+  const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4, capp * 4,
                                        capp * d * 2, capp * d * 2, capp * 2 * n * 4,
                                        capp * 2 * n * 2, capp * n * 2, capp * bwd_act_parts(s->n) * 4, capp * d * 2,
-                                       A * 4,        capp * 4,     E * d * 4,
+                                       capp * 4,     capp * 4,     E * d * 4,
                                        S * E * d * 4, S * E * 4};
   int64_t pos = base;
   for (int i = 0; i < kNumBwdSlots; ++i) {
@@ -103,7 +105,7 @@ int64_t layout_bwd(const moe_shape* s, int64_t* off_fwd, int64_t* off) {
   return pos;
 }
 
-bool bwd_shape_ok(const moe_shape* s) { return s->round == MOE_ROUND_OFF && s->d % 128 == 0 && s->n % 64 == 0; }
+bool bwd_shape_ok(const moe_shape* s) { return s->d % 128 == 0 && s->n % 64 == 0; }
 
 }  // namespace
 
@@ -490,6 +492,9 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   int32_t* offsets_p = at<int32_t>(ws, off[kOffP]);
   int32_t* rowp = at<int32_t>(ws, off[kRowP]);
   float* wp = at<float>(ws, off[kWp]);
+  int32_t* epr = at<int32_t>(ws, off[kEpr]);
+  int32_t* tok_offsets = at<int32_t>(ws, off_f[kTokOffsets]);
+  int32_t* tok_rows = at<int32_t>(ws, off_f[kTokRows]);
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, off[kXp]);
   __nv_bfloat16* dyp = at<__nv_bfloat16>(ws, off[kDyp]);
   float* gl = at<float>(ws, off[kGl]);
@@ -502,25 +507,48 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   float* WrT = at<float>(ws, off[kWrT]);
   int32_t* status = status_of(ws);
 
-  // 1. routing, recomputed: the same kernels and bits as the forward
-  int rc = moe_route_permute(s, x, Wr, bias, logits, idx, w, counts, offsets, src, dst, row_token, row_w, ws,
-                             ws_bytes, stream);
-  if (rc != MOE_OK) return rc;
-  // 2. padded rows, zero padding, gathered x and dy
-  launch_bwd_rows(idx, w, dst, counts, offsets, E, A, offsets_p, rowp, wp, st);
+  // 1. routing, recomputed: the same kernels and bits as the forward.  Each
+  // token's rows form a list (rows, tok_offs) with a weight per row (wrow).
+  int rc;
+  const int32_t* rows;
+  const int32_t* tok_offs;
+  const float* wrow;
+  if (s->round == MOE_ROUND_OFF) {
+    if ((rc = moe_route_permute(s, x, Wr, bias, logits, idx, w, counts, offsets, src, dst, row_token, row_w, ws,
+                                ws_bytes, stream)) != MOE_OK)
+      return rc;
+    launch_bwd_pad_offsets(counts, E, offsets_p, st);
+    launch_bwd_rows(idx, w, dst, offsets, offsets_p, A, rowp, wp, st);
+    rows = rowp;
+    tok_offs = nullptr;
+    wrow = wp;
+  } else {
+    if ((rc = moe_route(s, x, Wr, bias, logits, idx, w, ws, stream)) != MOE_OK) return rc;
+    if ((rc = moe_token_round(s, logits, idx, counts, offsets, row_token, row_w, tok_offsets, tok_rows, ws, ws_bytes,
+                              stream)) != MOE_OK)
+      return rc;
+    // rounded counts are multiples of the tile (64, 128 or 256): the padded
+    // offsets equal the forward's, so its rows and row weights serve as they are
+    launch_bwd_pad_offsets(counts, E, offsets_p, st);
+    rows = tok_rows;
+    tok_offs = tok_offsets;
+    wrow = row_w;
+  }
+  // 2. expert of each row, zero padding, gathered x and dy
+  launch_bwd_expert_of_rows(counts, offsets_p, E, epr, st);
   launch_bwd_zero_pad(counts, offsets_p, E, d, n, xp, dyp, dgl, hw, st);
-  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(x), rowp, nullptr, T, k, d, xp, st);
-  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(dy), rowp, nullptr, T, k, d, dyp, st);
+  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(x), rows, tok_offs, T, k, d, xp, st);
+  launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(dy), rows, tok_offs, T, k, d, dyp, st);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 3. pre-activations, then the SwiGLU backward fused into dh' = dy W2^T
   if ((rc = launch_expert_up_pre(xp, static_cast<const __nv_bfloat16*>(W13p), counts, offsets_p, gl, d, n, E, capp,
                                  status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
-  if ((rc = launch_bwd_act(dyp, static_cast<const __nv_bfloat16*>(W2), counts, offsets_p, wp, gl, dgl, hw, dw_part, d,
+  if ((rc = launch_bwd_act(dyp, static_cast<const __nv_bfloat16*>(W2), counts, offsets_p, wrow, gl, dgl, hw, dw_part, d,
                            n, E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
   // 4. gate weights -> logits
-  launch_router_bwd(rowp, w, dw_part, bwd_act_parts(n), T, k, dl, dlp, st);
+  launch_router_bwd(rows, tok_offs, wrow, dw_part, bwd_act_parts(n), T, k, dl, dlp, st);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 5. weight gradients: dW2 = (w h)^T dy, dW1 / dW3 = x^T (dg, du)
   if ((rc = launch_wgrad(dyp, hw, counts, offsets_p, d, n, E, capp, dW2, nullptr, status, kDefaultTimeoutNs, st)) !=
@@ -533,7 +561,7 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   if ((rc = launch_expert_down(dgl, static_cast<const __nv_bfloat16*>(W13i), counts, offsets_p, nullptr, dxr, d, 2 * n,
                                E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
-  launch_bwd_dx(dxr, rowp, idx, dl, Wr, WrT, T, d, E, k, dx, st);
+  launch_bwd_dx(dxr, rows, tok_offs, epr, dl, Wr, WrT, T, d, E, k, dx, st);
   // 7. dWr = x^T dL, db = sum dL
   launch_bwd_dwr(xp, dlp, counts, offsets_p, E, d, at<float>(ws, off[kDwrPart]), at<float>(ws, off[kDbPart]), dWr,
                  dbias, st);

@@ -7,8 +7,12 @@
 //
 // Row layout: the forward's expert-grouped rows, each expert's segment padded
 // to a multiple of 64 rows with zero rows, so that the weight-gradient GEMMs
-// (K = the expert's rows) read whole 64-row k-blocks.  Every reduction here
-// runs in a fixed order: the results are bitwise reproducible.
+// (K = the expert's rows) read whole 64-row k-blocks.  (Token rounding makes
+// every count a multiple of the tile, 64, 128 or 256, so its rows need no
+// padding.)  A token's rows are a list: k consecutive entries t*k .. t*k+k-1
+// without rounding, or entries tok_offsets[t] .. tok_offsets[t+1]-1 of its
+// rounded set.  Every reduction here runs in a fixed order: the results are
+// bitwise reproducible.
 #include <algorithm>
 
 #include "common.cuh"
@@ -50,6 +54,7 @@ __global__ void __launch_bounds__(1024) bwd_pad_offsets_kernel(const int32_t* __
 }
 
 // rowp[a] = padded row of assignment a; wp[rowp[a]] = its gate weight.
+// (The top-k path; with rounding the rows and weights come from the round.)
 __global__ void bwd_rows_kernel(const int32_t* __restrict__ idx, const float* __restrict__ w,
                                 const int32_t* __restrict__ dst, const int32_t* __restrict__ offsets,
                                 const int32_t* __restrict__ offsets_p, int64_t A, int32_t* __restrict__ rowp,
@@ -85,12 +90,37 @@ __global__ void __launch_bounds__(256) bwd_zero_pad_kernel(const int32_t* __rest
   for (int g = threadIdx.x; g < n / 8; g += blockDim.x) reinterpret_cast<uint4*>(hw + row * n)[g] = z;
 }
 
-// Gate-weight and logit gradients, a warp per token (lane j = slot j):
-//   dw_j = sum of the row's n-block partials (in n-block order)
-//   dL_j = w_j (dw_j - sum_i w_i dw_i)   (softmax over the selected logits)
-// written per assignment (dl) and per padded row (dlp).
-__global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restrict__ rowp,
-                                                         const float* __restrict__ w,
+// epr[r] = e for the rows offsets_p[e] .. offsets_p[e] + counts[e] - 1.
+__global__ void __launch_bounds__(256) bwd_expert_of_rows_kernel(const int32_t* __restrict__ counts,
+                                                                 const int32_t* __restrict__ offsets_p,
+                                                                 int32_t* __restrict__ epr) {
+  pdl_wait();
+  pdl_trigger();
+  const int e = blockIdx.x;
+  const int32_t first = offsets_p[e], cnt = counts[e];
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) epr[first + i] = e;
+}
+
+// First and end entry of token t's row list.
+__device__ __forceinline__ void token_entries(const int32_t* tok_offsets, int t, int k, int64_t& r0, int64_t& r1) {
+  if (tok_offsets) {
+    r0 = tok_offsets[t];
+    r1 = tok_offsets[t + 1];
+  } else {
+    r0 = static_cast<int64_t>(t) * k;
+    r1 = r0 + k;
+  }
+}
+
+// Gate-weight and logit gradients, a warp per token; lane l takes the
+// entries l, l+32, ... of the token's list:
+//   dw_i = sum of the row's partials (in partial order)
+//   dL_i = w_i (dw_i - sum_j w_j dw_j)   (softmax over the selected logits)
+// written per list entry (dl) and per padded row (dlp).  The sum over j is
+// each lane's entries in order, then a fixed butterfly over the lanes.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restrict__ rows,
+                                                         const int32_t* __restrict__ tok_offsets,
+                                                         const float* __restrict__ wp,
                                                          const float* __restrict__ dw_part, int parts, int T, int k,
                                                          float* __restrict__ dl, float* __restrict__ dlp) {
   pdl_wait();
@@ -98,21 +128,26 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restri
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= T) return;
-  const int64_t a = static_cast<int64_t>(t) * k + lane;
-  float dwj = 0.f, wj = 0.f;
-  int rp = 0;
-  if (lane < k) {
-    rp = rowp[a];
-    wj = w[a];
+  int64_t r0, r1;
+  token_entries(tok_offsets, t, k, r0, r1);
+  auto dw_of = [&](int32_t rp) {
     const float* pp = dw_part + static_cast<int64_t>(rp) * parts;
-    for (int i = 0; i < parts; ++i) dwj += pp[i];
+    float v = 0.f;
+    for (int i = 0; i < parts; ++i) v += pp[i];
+    return v;
+  };
+  float dot = 0.f;
+  for (int64_t i = r0 + lane; i < r1; i += 32) {
+    const int32_t rp = rows[i];
+    dot += wp[rp] * dw_of(rp);
   }
-  float dot = wj * dwj;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-  if (lane < k) {
-    const float v = wj * (dwj - dot);
-    dl[a] = v;
+  for (int64_t i = r0 + lane; i < r1; i += 32) {
+    const int32_t rp = rows[i];
+    const float wj = wp[rp];
+    const float v = wj * (dw_of(rp) - dot);
+    dl[i] = v;
     dlp[rp] = v;
   }
 }
@@ -128,13 +163,14 @@ __global__ void transpose_router_kernel(const float* __restrict__ Wr, int d, int
   }
 }
 
-// dx[t] = sum over the token's slots j (in slot order) of
-//   dxr[rowp_j] + dL_j * Wr[:, e_j]
+// dx[t] = sum over the token's list entries i (in list order) of
+//   dxr[row_i] + dL_i * Wr[:, expert of row_i]
 // (the expert paths' input gradient plus the gate network's).  Each thread
 // owns 8 columns.
 __global__ void __launch_bounds__(256) bwd_dx_kernel(const __half* __restrict__ dxr,
-                                                     const int32_t* __restrict__ rowp,
-                                                     const int32_t* __restrict__ idx, const float* __restrict__ dl,
+                                                     const int32_t* __restrict__ rows,
+                                                     const int32_t* __restrict__ tok_offsets,
+                                                     const int32_t* __restrict__ epr, const float* __restrict__ dl,
                                                      const float* __restrict__ WrT, int T, int d, int k,
                                                      float* __restrict__ dx) {
   pdl_wait();
@@ -147,12 +183,13 @@ __global__ void __launch_bounds__(256) bwd_dx_kernel(const __half* __restrict__ 
   float acc[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int64_t a = static_cast<int64_t>(t) * k + j;
-    const int64_t row = rowp[a];
+  int64_t r0, r1;
+  token_entries(tok_offsets, t, k, r0, r1);
+  for (int64_t a = r0; a < r1; ++a) {
+    const int64_t row = rows[a];
     const float l = dl[a];
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(dxr + row * d) + g);
-    const float4* wr = reinterpret_cast<const float4*>(WrT + static_cast<int64_t>(idx[a]) * d) + 2 * g;
+    const float4* wr = reinterpret_cast<const float4*>(WrT + static_cast<int64_t>(epr[row]) * d) + 2 * g;
     const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
     const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
     const uint32_t h[4] = {v.x, v.y, v.z, v.w};
@@ -248,13 +285,14 @@ int bwd_dwr_splits(int E, int d) {
   return std::max(1, std::min(64, (2 * num_sms() + blocks - 1) / blocks));
 }
 
-void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, const int32_t* counts,
-                     const int32_t* offsets, int E, int64_t A, int32_t* offsets_p, int32_t* rowp, float* wp,
-                     cudaStream_t stream) {
+void launch_bwd_pad_offsets(const int32_t* counts, int E, int32_t* offsets_p, cudaStream_t stream) {
   launch_pdl(bwd_pad_offsets_kernel, 1, 1024, 0, stream, 1, counts, E, offsets_p);
+}
+
+void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, const int32_t* offsets,
+                     const int32_t* offsets_p, int64_t A, int32_t* rowp, float* wp, cudaStream_t stream) {
   const unsigned blocks = static_cast<unsigned>(std::min<int64_t>((A + 255) / 256, num_sms() * 8));
-  launch_pdl(bwd_rows_kernel, blocks, 256, 0, stream, 1, idx, w, dst, offsets, static_cast<const int32_t*>(offsets_p),
-             A, rowp, wp);
+  launch_pdl(bwd_rows_kernel, blocks, 256, 0, stream, 1, idx, w, dst, offsets, offsets_p, A, rowp, wp);
 }
 
 void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E, int d, int n, __nv_bfloat16* xp,
@@ -262,19 +300,26 @@ void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E,
   launch_pdl(bwd_zero_pad_kernel, dim3(E, kPadRows - 1), 256, 0, stream, 1, counts, offsets_p, d, n, xp, dyp, dgl, hw);
 }
 
-void launch_router_bwd(const int32_t* rowp, const float* w, const float* dw_part, int parts, int T, int k, float* dl,
-                       float* dlp, cudaStream_t stream) {
-  launch_pdl(router_bwd_kernel, (T + 7) / 8, 256, 0, stream, 1, rowp, w, dw_part, parts, T, k, dl, dlp);
+void launch_bwd_expert_of_rows(const int32_t* counts, const int32_t* offsets_p, int E, int32_t* epr,
+                               cudaStream_t stream) {
+  launch_pdl(bwd_expert_of_rows_kernel, E, 256, 0, stream, 1, counts, offsets_p, epr);
 }
 
-void launch_bwd_dx(const __half* dxr, const int32_t* rowp, const int32_t* idx, const float* dl, const float* Wr,
-                   float* WrT, int T, int d, int E, int k, float* dx, cudaStream_t stream) {
+void launch_router_bwd(const int32_t* rows, const int32_t* tok_offsets, const float* wp, const float* dw_part,
+                       int parts, int T, int k, float* dl, float* dlp, cudaStream_t stream) {
+  launch_pdl(router_bwd_kernel, (T + 7) / 8, 256, 0, stream, 1, rows, tok_offsets, wp, dw_part, parts, T, k, dl,
+             dlp);
+}
+
+void launch_bwd_dx(const __half* dxr, const int32_t* rows, const int32_t* tok_offsets, const int32_t* epr,
+                   const float* dl, const float* Wr, float* WrT, int T, int d, int E, int k, float* dx,
+                   cudaStream_t stream) {
   const int64_t wt = static_cast<int64_t>(d) * E;
   launch_pdl(transpose_router_kernel, static_cast<unsigned>(std::min<int64_t>((wt + 255) / 256, num_sms() * 8)), 256,
              0, stream, 1, Wr, d, E, WrT);
   const int64_t total = static_cast<int64_t>(T) * (d / 8);
-  launch_pdl(bwd_dx_kernel, static_cast<unsigned>((total + 255) / 256), 256, 0, stream, 1, dxr, rowp, idx, dl,
-             static_cast<const float*>(WrT), T, d, k, dx);
+  launch_pdl(bwd_dx_kernel, static_cast<unsigned>((total + 255) / 256), 256, 0, stream, 1, dxr, rows, tok_offsets, epr,
+             dl, static_cast<const float*>(WrT), T, d, k, dx);
 }
 
 void launch_bwd_dwr(const __nv_bfloat16* xp, const float* dlp, const int32_t* counts, const int32_t* offsets_p,

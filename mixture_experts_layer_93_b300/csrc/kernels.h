@@ -112,15 +112,19 @@ void launch_prepare_weights_bwd(const __nv_bfloat16* W1, const __nv_bfloat16* W3
 
 // bwd.cu (backward pass around the backward GEMMs; padded row layout)
 int bwd_dwr_splits(int E, int d);
-void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, const int32_t* counts,
-                     const int32_t* offsets, int E, int64_t A, int32_t* offsets_p, int32_t* rowp, float* wp,
-                     cudaStream_t stream);
+void launch_bwd_pad_offsets(const int32_t* counts, int E, int32_t* offsets_p, cudaStream_t stream);
+void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, const int32_t* offsets,
+                     const int32_t* offsets_p, int64_t A, int32_t* rowp, float* wp, cudaStream_t stream);
 void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E, int d, int n, __nv_bfloat16* xp,
                          __nv_bfloat16* dyp, __nv_bfloat16* dgl, __nv_bfloat16* hw, cudaStream_t stream);
-void launch_router_bwd(const int32_t* rowp, const float* w, const float* dw_part, int parts, int T, int k, float* dl,
-                       float* dlp, cudaStream_t stream);
-void launch_bwd_dx(const __half* dxr, const int32_t* rowp, const int32_t* idx, const float* dl, const float* Wr,
-                   float* WrT, int T, int d, int E, int k, float* dx, cudaStream_t stream);
+// rows / tok_offsets: each token's row list (tok_offsets NULL: k entries per token)
+void launch_bwd_expert_of_rows(const int32_t* counts, const int32_t* offsets_p, int E, int32_t* epr,
+                               cudaStream_t stream);
+void launch_router_bwd(const int32_t* rows, const int32_t* tok_offsets, const float* wp, const float* dw_part,
+                       int parts, int T, int k, float* dl, float* dlp, cudaStream_t stream);
+void launch_bwd_dx(const __half* dxr, const int32_t* rows, const int32_t* tok_offsets, const int32_t* epr,
+                   const float* dl, const float* Wr, float* WrT, int T, int d, int E, int k, float* dx,
+                   cudaStream_t stream);
 void launch_bwd_dwr(const __nv_bfloat16* xp, const float* dlp, const int32_t* counts, const int32_t* offsets_p,
                     int E, int d, float* part, float* dbpart, float* dWr, float* db, cudaStream_t stream);
 void launch_gather_rows_by_token(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T,

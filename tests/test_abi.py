@@ -131,8 +131,11 @@ def test_backward_workspace_and_host_checks(lib):
     assert lib.moe_backward(ctypes.byref(s), *args, need - 1, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_backward(ctypes.byref(s), *([None] + args[1:]), need, None) == B.MOE_ERR_INVALID
     assert lib.moe_backward(ctypes.byref(s), *([odd] + args[1:]), need, None) == B.MOE_ERR_INVALID
-    # unsupported: token rounding, d not a multiple of 128
-    for bad in (B.make_shape(256, 128, 64, 8, 2, tile=128, round="nearest"), B.make_shape(256, 192, 64, 8, 2)):
-        assert B.moe_backward_workspace_bytes(bad) == 0
-        assert lib.moe_backward(ctypes.byref(bad), *args, 1 << 40, None) == B.MOE_ERR_UNSUPPORTED
+    # unsupported: d not a multiple of 128
+    bad = B.make_shape(256, 192, 64, 8, 2)
+    assert B.moe_backward_workspace_bytes(bad) == 0
+    assert lib.moe_backward(ctypes.byref(bad), *args, 1 << 40, None) == B.MOE_ERR_UNSUPPORTED
+    # token rounding: rows up to the rounded capacity
+    r = B.make_shape(256, 128, 64, 8, 2, tile=128, round="nearest")
+    assert B.moe_backward_workspace_bytes(r) >= B.moe_workspace_bytes(r) + B.moe_row_capacity(r) * 2 * 128 * 2
     assert lib.moe_prepare_weights_bwd(ctypes.byref(s), p, None, p, None) == B.MOE_ERR_INVALID

@@ -80,6 +80,28 @@ def test_backward_matches_oracle(cuda_device, T, d, n, E, k):
     check_grads(out, ref)
 
 
+@pytest.mark.parametrize("T,d,n,E,k,tile,mode", [(700, 256, 128, 6, 2, 64, "nearest"), (900, 256, 192, 8, 3, 128, "up"),
+                                                 (1000, 128, 64, 16, 2, 64, "stochastic"),
+                                                 (300, 256, 128, 4, 1, 256, "nearest")])
+def test_backward_with_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
+    """The rounded sets (tokens joining or leaving experts, sets of any size,
+    empty ones included) are recomputed and held fixed; gradients against the
+    oracle's backward of the rounded layer on the same fp32 logits."""
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="normal", bias_scale=0.5)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=T + E)
+    g = torch.Generator(device="cpu").manual_seed(T)
+    dy = torch.randn(T, d, generator=g).to(torch.bfloat16).to(cuda_device)
+    s = B.make_shape(T, d, n, E, k, tile=tile, round=mode, seed=7)
+    W13p, _ = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
+    W13i = B.moe_prepare_weights_bwd(inp["W1"], inp["W3"])
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    ref = O.moe_backward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], dy, k=k, tile=tile,
+                         mode=mode, seed=7, logits=logits.cpu().numpy(), magnitudes=True)
+    sizes = np.array([len(st) for st in ref["sets"]])
+    assert np.any(sizes != k)  # rounding changed some sets
+    check_grads(out, ref)
+
+
 def test_backward_k1_has_no_router_gradient(cuda_device):
     cfg = I.MoEConfig("t", T=300, d=256, n=128, E=5, k=1, bias="normal", bias_scale=0.5)
     inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=3)
