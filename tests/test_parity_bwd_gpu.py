@@ -211,7 +211,7 @@ def _sampled_reference(inp, dy, logits, k, e, J, toks):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mixtral", "dsv3"])
+@pytest.mark.parametrize("name", ["mixtral", "dsv3", "b7", "skew"])
 def test_backward_full_size_sampled(cuda_device, name):
     """The full-size layers in the bench's launch configuration: sampled
     weight-gradient channels of two experts and sampled tokens' dx against
@@ -234,5 +234,42 @@ def test_backward_full_size_sampled(cuda_device, name):
     assert np.all(np.abs(dWr.sum(axis=1)) <= 1e-4 * np.sqrt(np.mean(dWr ** 2)) * cfg.E)
     db = to64(out["dbias"])
     assert abs(db.sum()) <= 1e-4 * np.sqrt(np.mean(db ** 2)) * cfg.E
+    del out
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_backward_full_size_rounded_skew(cuda_device):
+    """The skewed layer with nearest rounding to 128 at full size: the rounded
+    sets from the device against the oracle's rounding of the same logits,
+    then sampled channels of two experts against the formulas on those sets."""
+    cfg = I.get_config("skew")
+    inp, dy, _, W13p, W13i = _setup(cfg, cuda_device, seed=0)
+    s = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, tile=128, round="nearest")
+    out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
+    logits = logits.cpu().numpy()
+    L = logits.astype(np.float64)
+    r = O.token_round(L, O.topk(L, cfg.k), 128, O.ROUND_NEAREST)
+    member = r["member"]
+    rng = np.random.default_rng(3)
+    x64, dy64 = to64(inp["x"]), to64(dy)
+    for e in rng.choice(cfg.E, size=2, replace=False):
+        e = int(e)
+        ts = np.flatnonzero(member[:, e])
+        assert ts.size % 128 == 0
+        we = np.array([O.softmax(L[t, r["sets"][t]])[list(r["sets"][t]).index(e)] for t in ts])
+        J = np.sort(rng.choice(cfg.n, size=6, replace=False))
+        X = x64[ts]
+        W1J, W3J, W2J = to64(inp["W1"][e][:, J]), to64(inp["W3"][e][:, J]), to64(inp["W2"][e][J, :])
+        g, u = X @ W1J, X @ W3J
+        sg = O.sigmoid(g)
+        a = g * sg
+        dh = we[:, None] * (dy64[ts] @ W2J.T)
+        dg, du = dh * u * (sg * (1 + g * (1 - sg))), dh * a
+        Jt = torch.from_numpy(J).to(cuda_device)
+        assert_grad_close(out["dW1"][e][:, Jt], X.T @ dg, np.abs(X).T @ np.abs(dg), what=f"dW1[{e}]")
+        assert_grad_close(out["dW3"][e][:, Jt], X.T @ du, np.abs(X).T @ np.abs(du), what=f"dW3[{e}]")
+        hw = we[:, None] * a * u
+        assert_grad_close(out["dW2"][e][Jt, :], hw.T @ dy64[ts], np.abs(hw).T @ np.abs(dy64[ts]), what=f"dW2[{e}]")
     del out
     torch.cuda.empty_cache()
