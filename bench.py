@@ -632,6 +632,8 @@ def run_ours(args, world, rank, local):
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": tokens_per_s,
+        # rows the expert GEMMs ran on (R = T*k without rounding): executed FLOPs
+        "executed_tflops": world * 6.0 * R * d * n * args.steps / (total_ms * 1e-3) / 1e12,
         "frac_of_bf16_peak": value / world / peak_t,
         "frac_of_bf16_sustained_peak": value / world / sustained,
         "roofline": roofline,
