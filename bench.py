@@ -533,6 +533,43 @@ def run_ours(args, world, rank, local):
     value = world * active * args.steps / (total_ms * 1e-3) / 1e12
     tokens_per_s = world * T * args.steps / (total_ms * 1e-3)
 
+    # ------------------------------------------------ optional: the same layer replayed as one CUDA graph
+    graph_line = None
+    if args.graph:
+        def forward_on(st_ptr):
+            if args.fp8:
+                check(L.moe_forward_fp8(sp, P(x), P(Wr), P(bias), P(W13q), P(sW13), P(W2q), P(sW2), P(y), ws.ptr,
+                                        ws.nbytes, st_ptr), "forward_fp8")
+            else:
+                check(L.moe_forward(sp, P(x), P(Wr), P(bias), P(W13p), P(W2p), P(y), ws.ptr, ws.nbytes, st_ptr),
+                      "forward")
+
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        forward_on(ctypes.c_void_p(gstream.cuda_stream))   # warm-up outside the capture
+        stream.wait_stream(gstream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            forward_on(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            gev[i][0].record(stream)
+            graph.replay()
+            gev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        B.moe_check_device_status(ws)
+        g_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in gev), world, dev)
+        graph_line = {"value": world * cfg.active_flops() * args.steps / (g_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "ms_per_step": g_ms / args.steps,
+                      "how": "moe_forward captured once into a CUDA graph, replayed per step (L2 flushed between)"}
+
     # ------------------------------------------------ e2e: through moe_forward, host buffers
     # Each step copies its x from pinned host memory, runs moe_forward and
     # copies its y back.  Steps alternate between two streams (each with its
@@ -645,6 +682,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    if graph_line is not None:
+        line["graph"] = graph_line
     if inp_host is not None:
         ntok, secs, desc, threads = oracle_sample_time(cfg, inp_host, mode, budget_s=args.cpu_seconds)
         tps = ntok / secs
@@ -673,6 +712,8 @@ def main():
     ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
                     help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
                          "rows, 2 = per-lane cp.async of token rows")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time moe_forward replayed from one captured CUDA graph")
     ap.add_argument("--backward", action="store_true",
                     help="measure the backward pass (moe_backward) instead of the forward")
     args = ap.parse_args()

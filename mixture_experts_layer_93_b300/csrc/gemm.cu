@@ -1037,37 +1037,51 @@ int num_sms() {
   return sms > 0 ? sms : 1;
 }
 
+// Per device, the first launch of each kernel variant sets its shared-memory
+// size and finds its persistent grid (the SM pairs that can be resident at
+// once); later launches, including those captured into a CUDA graph, only
+// launch.
+constexpr int kMaxGemmDevices = 64;
+
 template <int BN, int MODE, bool PAIR, int EPI>
 static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BN, PAIR, EPI>;
   auto kern = moe_gemm_kernel<BN, MODE, PAIR, EPI>;
   constexpr int kGemmThreads = gemm_threads(EPI);
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (!PAIR) {
-    if (launch_pdl(kern, num_sms(), kGemmThreads, C::SMEM_BYTES, stream, 1, tmA, tmB, tmC, p) != cudaSuccess)
+  static int grid_of[kMaxGemmDevices] = {0};  // 0: not yet prepared on that device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxGemmDevices) return MOE_ERR_CUDA;
+  if (grid_of[dev] == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
       return MOE_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    int grid = num_sms();
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cfg.stream = nullptr;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      // persistent: as many clusters as can be resident at once (SM pairs
+      // that share a GPC), so no cluster waits for a second wave
+      int clusters = 0;
+      cfg.gridDim = dim3(num_sms() & ~1);
+      if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        (void)cudaGetLastError();
+        clusters = num_sms() / 2;
+      }
+      grid = 2 * std::min(clusters, num_sms() / 2);
+    }
+    grid_of[dev] = grid;
   }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // persistent: as many clusters as can be resident at once (SM pairs that
-  // share a GPC), so no cluster waits for a second wave
-  int clusters = 0;
-  cfg.gridDim = dim3(num_sms() & ~1);
-  if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) clusters = num_sms() / 2;
-  const int grid = 2 * std::min(clusters, num_sms() / 2);
-  if (launch_pdl(kern, grid, kGemmThreads, C::SMEM_BYTES, stream, 2, tmA, tmB, tmC, p) != cudaSuccess)
+  if (launch_pdl(kern, grid_of[dev], kGemmThreads, C::SMEM_BYTES, stream, PAIR ? 2 : 1, tmA, tmB, tmC, p) !=
+      cudaSuccess)
     return MOE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
