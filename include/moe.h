@@ -355,8 +355,9 @@ int moe_prepare_weights_bwd(const moe_shape* s, const void* W1, const void* W3, 
  *   out: dx [T, d], dWr [d, E], dbias [E] (NULL: not written), dW1 and dW3
  *        [E, d, n], dW2 [E, n, d], all fp32, every element written (an expert
  *        without tokens gets zero weight gradients).
- * ws (moe_backward_workspace_bytes) is caller-owned device memory, 16-byte
- * aligned; its status word reports device-side errors as for moe_forward.
+ * x, dy, dx, dW1, dW3, dW2 and ws 16-byte aligned.  ws
+ * (moe_backward_workspace_bytes) is caller-owned device memory; its status
+ * word reports device-side errors as for moe_forward.
  * Asynchronous on `stream`. */
 int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                  const void* W13p, const void* W13i, const void* W2, const void* dy, float* dx,

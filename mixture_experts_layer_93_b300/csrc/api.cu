@@ -471,7 +471,8 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
                  float* dW3, float* dW2, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !x || !Wr || !W13p || !W13i || !W2 || !dy || !dx || !dWr || !dW1 || !dW3 || !dW2)
     return MOE_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(W13p) || !aligned16(W13i) || !aligned16(W2) || !aligned16(dy) || !aligned16(dx))
+  if (!aligned16(x) || !aligned16(W13p) || !aligned16(W13i) || !aligned16(W2) || !aligned16(dy) || !aligned16(dx) ||
+      !aligned16(dW1) || !aligned16(dW3) || !aligned16(dW2))
     return MOE_ERR_INVALID;
   if (!bwd_shape_ok(s)) return MOE_ERR_UNSUPPORTED;
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
