@@ -3,7 +3,12 @@
 // Up-projection:   h[r]  = bf16( silu(x[t_r] W1_e) * (x[t_r] W3_e) )
 // Down-projection: ys[r] = fp16( w_r * (h[r] W2_e) )
 // Router:          L[t]  = x[t] Wr + b, with Wr split exactly into three
-//                  bf16 terms (hi, mid, lo) held as three column groups of B
+//                  bf16 terms (hi, mid, lo) held as three column groups of B;
+//                  with at most 64 experts the epilogue also takes the top-k
+// e4m3 variants of the up- and down-projection (scaled codes, kind::f8f6f4)
+// Backward:        the pre-activations (g, u) in fp32; dh' = dy W2^T with the
+//                  SwiGLU backward in its epilogue; the weight gradients, whose
+//                  K is each expert's rows, from MN-major operands
 //
 // The row gather is fused into the operand load, the SwiGLU activation and the
 // gate weight into the epilogue, and loads overlap the MMAs ("SonicMoE: 加速
@@ -18,9 +23,11 @@
 //               16-byte cp.async from all four warps, written straight into
 //               the 128-byte-swizzled layout, each lane arriving on the stage
 //               barrier when its copies land (non-blocking).
-//   warp 4      TMEM allocator; lane 0 issues tcgen05.mma (M=128, N=BN,
-//               K=16, bf16 -> fp32 in tensor memory) and tcgen05.commit.
-//   warps 5..8  epilogue: tcgen05.ld of the accumulator (warp w owns TMEM
+//   warp 4      TMEM allocator; lane 0 issues tcgen05.mma (M=128, or 256
+//               on an SM pair with cta_group::2; N=BN, K=16 bf16 or 32 e4m3
+//               -> fp32 in tensor memory) and tcgen05.commit.
+//   warps 5..8  epilogue (5..8 and 10..13 with eight warps, two per lane
+//               quadrant): tcgen05.ld of the accumulator (warp w owns TMEM
 //               lanes 32*(w%4)..+31 = 32 rows), fused activation / scaling,
 //               stores.  Two accumulators in TMEM so the epilogue of one tile
 //               overlaps the MMAs of the next.
