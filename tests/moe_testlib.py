@@ -61,7 +61,7 @@ def valid_topk(L64_row: np.ndarray, chosen, margin: float) -> bool:
 # bf16-stored operand (the activation gradient, w h) carries one rounding of
 # relative size <= 2^-8, the rest being fp32 arithmetic.  The bar is the
 # elementwise bound |g - g_ref| <= 2^-7 * sum|terms| (twice the rounding, for
-# the fp32 parts) plus the spec mean relative error.
+# the fp32 parts) plus the layer's mean relative error bound.
 GRAD_REL = 2.0 ** -7
 
 

@@ -4,7 +4,7 @@ The quantisation decides integers (the e4m3 codes), so it is compared bit for
 bit: codes and fp32 scales equal the oracle's.  Given identical codes, the
 up-projection is checked like the bf16 one (h within one bf16 rounding of the
 fp64 product of the dequantised operands) and the whole layer against the
-oracle's FP8 layer within the benchmark spec's tolerance.
+oracle's FP8 layer within the layer tolerance.
 """
 import numpy as np
 import pytest
