@@ -67,6 +67,8 @@ SHAPES = [  # T, d, n, E, k: single-SM and SM-pair tiles, ragged experts, n % 12
     (300, 384, 192, 4, 2),
     (500, 256, 64, 64, 4),
     (129, 256, 320, 3, 3),
+    (200, 128, 64, 300, 3),   # E > 256: the separate top-k and permutation kernels
+    (64, 128, 128, 1, 1),     # one expert: a dense FFN, no router gradient
 ]
 
 
