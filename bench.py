@@ -352,7 +352,7 @@ def run_backward(args, world, rank, local):
     capp = T * k + (E * cfg.tile if args.round != "off" else 0) + 63 * E
     dx_launches = 1 if 128.0 * E <= 0.15 * capp else 2
     # (rounding: route 3 + round 9 in place of route + permute, and no rows kernel)
-    fused_route = 4 if (E <= 64 and k <= 8) else (5 if E <= 256 else 6)
+    fused_route = 4 if (E <= 256 and k <= 8) else (5 if E <= 256 else 6)
     if args.round != "off":
         fused_route = 3 + 9 - 1
     launches = fused_route + 2 + 1 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
@@ -446,8 +446,8 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     st = ctypes.c_void_p(stream.cuda_stream)
     # rounding off: route+permute fused (Wr split, router GEMM, fused top-k +
-    # histogram, scan, scatter: 5 launches; 4 when E <= 64 and k <= 8, where
-    # the router GEMM's epilogue takes the top-k; 6 when E > 256); rounding: route
+    # histogram, scan, scatter: 5 launches; 4 when k <= 8, where the router
+    # GEMM's epilogue takes the top-k; 6 when E > 256); rounding: route
     # (Wr split, router GEMM, top-k: 3) then member, select, transpose, 2
     # offsets, sets + a 3-launch permutation (9).  up: row gather + SM-pair GEMM
     # + odd-block GEMM (A path 0) or one GEMM (paths 1, 2); down: SM-pair +
@@ -461,7 +461,7 @@ def run_ours(args, world, rank, local):
     if args.fp8:
         up_launches = 2  # quantising gather + one SM-pair e4m3 GEMM
         gemm_launches = 2  # down: h quantisation + one SM-pair e4m3 GEMM
-    fused_route = 4 if (E <= 64 and k <= 8) else (5 if E <= 256 else 6)
+    fused_route = 4 if (E <= 256 and k <= 8) else (5 if E <= 256 else 6)
     route_launches = fused_route if mode == "off" else 3 + 9
     launches_per_step = route_launches + up_launches + gemm_launches + 1
 

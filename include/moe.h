@@ -156,7 +156,7 @@ int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w
  * "硬件加速的考量", section 自定义核与核融合: gate scores, top-k, and the
  * grouping that collects each expert's tokens).  Same outputs, bit for bit, as
  * moe_route followed by moe_permute with topk_w given, in fewer launches:
- * for E <= 64 and k <= 8 the router GEMM's epilogue takes each token's top-k
+ * for E <= 256 and k <= 8 the router GEMM's epilogue takes each token's top-k
  * and gate weights and counts each chunk's assignments per expert (integer
  * atomics); for E <= 256 one kernel does that from the stored logits; the
  * scan of the counts and the scatter follow.  (E > 256 runs the separate

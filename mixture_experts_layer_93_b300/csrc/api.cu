@@ -222,7 +222,7 @@ int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const 
                       fused ? static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k) : 0);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (router_fuses_topk(s->E, s->k)) {
-    // the router tile spans every expert: top-k and chunk counts in its epilogue
+    // top-k and chunk counts in the router GEMM's epilogue
     const int rst = launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
                                      status_of(ws), kDefaultTimeoutNs, as_stream(stream), s->k, topk_idx, topk_w,
                                      chunk_hist);

@@ -339,6 +339,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int total_tiles = kWgrad ? p.E * p.m_units * p.n_blocks : prefix[n_groups] * p.n_blocks;
+  // The i-th tile of this CTA (pair): unit0 + i * unit_stride.  The router
+  // with the top-k fused takes all n-blocks of one m-unit in a row instead,
+  // so that a thread has seen every expert of its token before the next one.
+  const bool by_unit = MODE == kModeRouter && p.topk_k > 0 && p.n_blocks > 1;
+  auto tau_of = [&](int i) -> int {
+    if (by_unit) return (unit0 + (i / p.n_blocks) * unit_stride) * p.n_blocks + (i % p.n_blocks);
+    return unit0 + i * unit_stride;
+  };
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
@@ -407,7 +415,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       uint32_t phase = 0;
       bool ok = true;
       int e = 0;  // group cursor of decode_tile
-      for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
         int nb, mu, gstart, gcount;
         decode_tile<MODE == kModeRouter>(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, grp_s, e, gstart, gcount);
@@ -498,7 +506,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status,
                                kWaitMmaTmemEmpty, p.timeout_ns))
           break;
@@ -562,7 +570,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tau = unit0; tau < total_tiles && ok; tau += unit_stride) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&afull_bar[stage]), phase, abort_flag, p.status, kWaitRelay,
                                  p.timeout_ns)) {
@@ -687,11 +695,15 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                      ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] * p.col_scale[dec_e]
                      : 0.f;
       };
-      if (unit0 < total_tiles) decode_next(unit0);
-      for (int tau = unit0; tau < total_tiles; tau += unit_stride) {
+      if (tau_of(0) < total_tiles) decode_next(tau_of(0));
+      // router with the top-k fused: the token's best keys so far (across
+      // the n-blocks of one m-unit) and whether a logit was NaN
+      uint64_t best[kFusedTopk];
+      bool nan_seen = false;
+      for (int it = 0, tau = tau_of(0); tau < total_tiles; tau = tau_of(++it)) {
         const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows, e_tile = nx_e;
         const float wr = nx_w;
-        if (tau + unit_stride < total_tiles) decode_next(tau + unit_stride);
+        if (tau_of(it + 1) < total_tiles) decode_next(tau_of(it + 1));
         int w = 1;
         if (lane == 0)
           w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
@@ -840,18 +852,19 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (ch == 0) {
             // router (first four epilogue warps only): the three column groups
             // hold x*hi, x*mid, x*lo of the same EB experts; their fp32 sum
-            // plus the bias is the logit.  With topk_k > 0 the tile spans
-            // every expert, and the thread also takes its token's top-k
-            // (the 64-bit keys of topk.cuh, kept sorted by insertion), the
-            // gate weights and the chunk histogram, as topk_perm_hist_kernel
-            // does from the stored logits.
+            // plus the bias is the logit.  With topk_k > 0 the thread also
+            // takes its token's top-k over the n-blocks of its m-unit, which
+            // this CTA runs in a row (the 64-bit keys of topk.cuh, kept sorted
+            // by insertion), then the gate weights and the chunk histogram,
+            // as topk_perm_hist_kernel does from the stored logits.
             constexpr int EB = BN / 3;
             const int e0 = nb * EB;
             float* dst = p.out_f32 + row * p.out_ld;
-            uint64_t best[kFusedTopk];
+            if (nb == 0) {
 #pragma unroll
-            for (int i = 0; i < kFusedTopk; ++i) best[i] = 0;  // below every real key
-            bool nan_seen = false;
+              for (int i = 0; i < kFusedTopk; ++i) best[i] = 0;  // below every real key
+              nan_seen = false;
+            }
 #pragma unroll 1
             for (int c = 0; c < EB; c += 16) {
               uint32_t a[16], b[16], q[16];
@@ -881,7 +894,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                 }
               }
             }
-            if (p.topk_k > 0 && valid) {
+            if (p.topk_k > 0 && valid && nb == p.n_blocks - 1) {  // the token's last expert block
               if (nan_seen) report_error(p.status, MOE_ERR_DEVICE_CHECK, static_cast<int32_t>(row));
               // softmax over the selected logits, the sum in slot order
               const float vmax = topk_key_value(best[0]);

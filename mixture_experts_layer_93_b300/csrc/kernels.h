@@ -92,9 +92,10 @@ void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cuda
                          int32_t* zero = nullptr, int64_t zero_count = 0);
 // k > 0 (router_fuses_topk): the epilogue also writes the top-k ids and gate
 // weights and counts them into chunk_hist (zero on entry), as the fused
-// top-k + histogram kernel does.
+// top-k + histogram kernel does; an SM pair then runs all n-blocks (64
+// experts each) of one row block in a row.
 constexpr int kFusedTopk = 8;
-inline bool router_fuses_topk(int E, int k) { return E <= 64 && k <= kFusedTopk; }
+inline bool router_fuses_topk(int E, int k) { return E <= 256 && k <= kFusedTopk; }
 int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
                      int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream, int k = 0,
                      int32_t* topk_idx = nullptr, float* topk_w = nullptr, int32_t* chunk_hist = nullptr);
