@@ -344,18 +344,17 @@ def run_backward(args, world, rank, local):
         return
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    # launches per moe_backward: route + permute (4, 5 or 6, as the forward), padded
-    # offsets and rows (2), expert of each row, zero padding, two gathers,
-    # pre-activations, SwiGLU backward,
-    # router backward, dW2, dW1/dW3, dx rows (1, or 2 with separate odd
-    # blocks), router transpose, dx, dWr partial and final
+    # launches per moe_backward: route + permute (4, 5 or 6, as the forward;
+    # with rounding route 3 + round 9, and no rows kernel), padded offsets and
+    # rows (2), zero padding, two gathers, pre-activations, SwiGLU backward,
+    # router backward, dW2, dW1/dW3, router transpose, dx rows (1, or 2 with
+    # separate odd blocks), the rows' sum per token, dWr partial and final
     capp = T * k + (E * cfg.tile if args.round != "off" else 0) + 63 * E
     dx_launches = 1 if 128.0 * E <= 0.15 * capp else 2
-    # (rounding: route 3 + round 9 in place of route + permute, and no rows kernel)
     fused_route = 4 if (E <= 256 and k <= 8) else (5 if E <= 256 else 6)
     if args.round != "off":
         fused_route = 3 + 9 - 1
-    launches = fused_route + 2 + 1 + 1 + 2 + 1 + 1 + 1 + 2 + dx_launches + 2 + 2
+    launches = fused_route + 2 + 1 + 2 + 1 + 1 + 1 + 2 + 1 + dx_launches + 1 + 2
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,

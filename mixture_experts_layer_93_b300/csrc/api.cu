@@ -81,8 +81,7 @@ int check_ws(const moe_shape* s, void* ws, size_t ws_bytes, bool fp8 = false) {
 // Backward workspace: the forward's slots, then the backward's arrays over
 // the padded row layout (each expert's rows padded to a multiple of 64).
 enum BwdSlot {
-  kOffP, kRowP, kWp, kEpr, kXp, kDyp, kGl, kDgl, kHw, kDwPart, kDxr, kDl, kDlp, kWrT, kDwrPart, kDbPart,
-  kNumBwdSlots
+  kOffP, kRowP, kWp, kXp, kDyp, kGl, kDgl, kHw, kDwPart, kDxr, kDlp, kWrT, kDwrPart, kDbPart, kNumBwdSlots
 };
 
 // rows of the padded layout: the forward's rows plus up to 63 padding rows per expert
@@ -92,10 +91,10 @@ int64_t layout_bwd(const moe_shape* s, int64_t* off_fwd, int64_t* off) {
   const int64_t base = layout(s, off_fwd);
   const int64_t T = s->T, E = s->E, A = T * s->k, capp = padded_cap(s), d = s->d, n = s->n;
   const int64_t S = bwd_dwr_splits(s->E, s->d);
-  const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4, capp * 4,
+  const int64_t sizes[kNumBwdSlots] = {(E + 1) * 4, A * 4,       capp * 4,
                                        capp * d * 2, capp * d * 2, capp * 2 * n * 4,
                                        capp * 2 * n * 2, capp * n * 2, capp * bwd_act_parts(s->n) * 4, capp * d * 2,
-                                       capp * 4,     capp * 4,     E * d * 4,
+                                       capp * 4,     E * d * 4,
                                        S * E * d * 4, S * E * 4};
   int64_t pos = base;
   for (int i = 0; i < kNumBwdSlots; ++i) {
@@ -493,7 +492,6 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   int32_t* offsets_p = at<int32_t>(ws, off[kOffP]);
   int32_t* rowp = at<int32_t>(ws, off[kRowP]);
   float* wp = at<float>(ws, off[kWp]);
-  int32_t* epr = at<int32_t>(ws, off[kEpr]);
   int32_t* tok_offsets = at<int32_t>(ws, off_f[kTokOffsets]);
   int32_t* tok_rows = at<int32_t>(ws, off_f[kTokRows]);
   __nv_bfloat16* xp = at<__nv_bfloat16>(ws, off[kXp]);
@@ -503,7 +501,6 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   __nv_bfloat16* hw = at<__nv_bfloat16>(ws, off[kHw]);
   float* dw_part = at<float>(ws, off[kDwPart]);
   __half* dxr = at<__half>(ws, off[kDxr]);
-  float* dl = at<float>(ws, off[kDl]);
   float* dlp = at<float>(ws, off[kDlp]);
   float* WrT = at<float>(ws, off[kWrT]);
   int32_t* status = status_of(ws);
@@ -535,8 +532,7 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
     tok_offs = tok_offsets;
     wrow = row_w;
   }
-  // 2. expert of each row, zero padding, gathered x and dy
-  launch_bwd_expert_of_rows(counts, offsets_p, E, epr, st);
+  // 2. zero padding, gathered x and dy
   launch_bwd_zero_pad(counts, offsets_p, E, d, n, xp, dyp, dgl, hw, st);
   launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(x), rows, tok_offs, T, k, d, xp, st);
   launch_gather_rows_by_token(static_cast<const __nv_bfloat16*>(dy), rows, tok_offs, T, k, d, dyp, st);
@@ -549,7 +545,7 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
                            n, E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
   // 4. gate weights -> logits
-  launch_router_bwd(rows, tok_offs, wrow, dw_part, bwd_act_parts(n), T, k, dl, dlp, st);
+  launch_router_bwd(rows, tok_offs, wrow, dw_part, bwd_act_parts(n), T, k, dlp, st);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   // 5. weight gradients: dW2 = (w h)^T dy, dW1 / dW3 = x^T (dg, du)
   if ((rc = launch_wgrad(dyp, hw, counts, offsets_p, d, n, E, capp, dW2, nullptr, status, kDefaultTimeoutNs, st)) !=
@@ -558,11 +554,13 @@ int moe_backward(const moe_shape* s, const void* x, const float* Wr, const float
   if ((rc = launch_wgrad(dgl, xp, counts, offsets_p, 2 * n, d, E, capp, dW1, dW3, status, kDefaultTimeoutNs, st)) !=
       MOE_OK)
     return rc;
-  // 6. dx: the expert paths ([dg du] W13i^T per row, fp16) and the gate network
-  if ((rc = launch_expert_down(dgl, static_cast<const __nv_bfloat16*>(W13i), counts, offsets_p, nullptr, dxr, d, 2 * n,
-                               E, capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
+  // 6. dx: per row the expert path [dg du] W13i^T plus the gate network's
+  // dL Wr[:, e] (fp16), then each token's rows summed in list order
+  launch_transpose_router(Wr, d, E, WrT, st);
+  if ((rc = launch_expert_dx(dgl, static_cast<const __nv_bfloat16*>(W13i), counts, offsets_p, dlp, WrT, dxr, d, n, E,
+                             capp, status, kDefaultTimeoutNs, st)) != MOE_OK)
     return rc;
-  launch_bwd_dx(dxr, rows, tok_offs, epr, dl, Wr, WrT, T, d, E, k, dx, st);
+  launch_combine(dxr, tok_offs, rows, dx, T, d, k, st);
   // 7. dWr = x^T dL, db = sum dL
   launch_bwd_dwr(xp, dlp, counts, offsets_p, E, d, at<float>(ws, off[kDwrPart]), at<float>(ws, off[kDbPart]), dWr,
                  dbias, st);

@@ -90,17 +90,6 @@ __global__ void __launch_bounds__(256) bwd_zero_pad_kernel(const int32_t* __rest
   for (int g = threadIdx.x; g < n / 8; g += blockDim.x) reinterpret_cast<uint4*>(hw + row * n)[g] = z;
 }
 
-// epr[r] = e for the rows offsets_p[e] .. offsets_p[e] + counts[e] - 1.
-__global__ void __launch_bounds__(256) bwd_expert_of_rows_kernel(const int32_t* __restrict__ counts,
-                                                                 const int32_t* __restrict__ offsets_p,
-                                                                 int32_t* __restrict__ epr) {
-  pdl_wait();
-  pdl_trigger();
-  const int e = blockIdx.x;
-  const int32_t first = offsets_p[e], cnt = counts[e];
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) epr[first + i] = e;
-}
-
 // First and end entry of token t's row list.
 __device__ __forceinline__ void token_entries(const int32_t* tok_offsets, int t, int k, int64_t& r0, int64_t& r1) {
   if (tok_offsets) {
@@ -116,13 +105,13 @@ __device__ __forceinline__ void token_entries(const int32_t* tok_offsets, int t,
 // entries l, l+32, ... of the token's list:
 //   dw_i = sum of the row's partials (in partial order)
 //   dL_i = w_i (dw_i - sum_j w_j dw_j)   (softmax over the selected logits)
-// written per list entry (dl) and per padded row (dlp).  The sum over j is
-// each lane's entries in order, then a fixed butterfly over the lanes.
+// written per padded row (dlp).  The sum over j is each lane's entries in
+// order, then a fixed butterfly over the lanes.
 __global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restrict__ rows,
                                                          const int32_t* __restrict__ tok_offsets,
                                                          const float* __restrict__ wp,
                                                          const float* __restrict__ dw_part, int parts, int T, int k,
-                                                         float* __restrict__ dl, float* __restrict__ dlp) {
+                                                         float* __restrict__ dlp) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -146,9 +135,7 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const int32_t* __restri
   for (int64_t i = r0 + lane; i < r1; i += 32) {
     const int32_t rp = rows[i];
     const float wj = wp[rp];
-    const float v = wj * (dw_of(rp) - dot);
-    dl[i] = v;
-    dlp[rp] = v;
+    dlp[rp] = wj * (dw_of(rp) - dot);
   }
 }
 
@@ -161,48 +148,6 @@ __global__ void transpose_router_kernel(const float* __restrict__ Wr, int d, int
     const int e = static_cast<int>(i / d), c = static_cast<int>(i % d);
     WrT[i] = Wr[static_cast<int64_t>(c) * E + e];
   }
-}
-
-// dx[t] = sum over the token's list entries i (in list order) of
-//   dxr[row_i] + dL_i * Wr[:, expert of row_i]
-// (the expert paths' input gradient plus the gate network's).  Each thread
-// owns 8 columns.
-__global__ void __launch_bounds__(256) bwd_dx_kernel(const __half* __restrict__ dxr,
-                                                     const int32_t* __restrict__ rows,
-                                                     const int32_t* __restrict__ tok_offsets,
-                                                     const int32_t* __restrict__ epr, const float* __restrict__ dl,
-                                                     const float* __restrict__ WrT, int T, int d, int k,
-                                                     float* __restrict__ dx) {
-  pdl_wait();
-  pdl_trigger();
-  const int groups = d / 8;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<int64_t>(T) * groups) return;
-  const int t = static_cast<int>(i / groups);
-  const int g = static_cast<int>(i % groups);
-  float acc[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-  int64_t r0, r1;
-  token_entries(tok_offsets, t, k, r0, r1);
-  for (int64_t a = r0; a < r1; ++a) {
-    const int64_t row = rows[a];
-    const float l = dl[a];
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(dxr + row * d) + g);
-    const float4* wr = reinterpret_cast<const float4*>(WrT + static_cast<int64_t>(epr[row]) * d) + 2 * g;
-    const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
-    const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 f = unpack_half2(h[q]);
-      acc[2 * q] += fmaf(l, wv[2 * q], f.x);
-      acc[2 * q + 1] += fmaf(l, wv[2 * q + 1], f.y);
-    }
-  }
-  float4* out = reinterpret_cast<float4*>(dx + static_cast<int64_t>(t) * d) + 2 * g;
-  out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // dWr[:, e] = sum over expert e's rows of dL_r x_r, db[e] = sum of dL_r.
@@ -300,26 +245,15 @@ void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E,
   launch_pdl(bwd_zero_pad_kernel, dim3(E, kPadRows - 1), 256, 0, stream, 1, counts, offsets_p, d, n, xp, dyp, dgl, hw);
 }
 
-void launch_bwd_expert_of_rows(const int32_t* counts, const int32_t* offsets_p, int E, int32_t* epr,
-                               cudaStream_t stream) {
-  launch_pdl(bwd_expert_of_rows_kernel, E, 256, 0, stream, 1, counts, offsets_p, epr);
-}
-
 void launch_router_bwd(const int32_t* rows, const int32_t* tok_offsets, const float* wp, const float* dw_part,
-                       int parts, int T, int k, float* dl, float* dlp, cudaStream_t stream) {
-  launch_pdl(router_bwd_kernel, (T + 7) / 8, 256, 0, stream, 1, rows, tok_offsets, wp, dw_part, parts, T, k, dl,
-             dlp);
+                       int parts, int T, int k, float* dlp, cudaStream_t stream) {
+  launch_pdl(router_bwd_kernel, (T + 7) / 8, 256, 0, stream, 1, rows, tok_offsets, wp, dw_part, parts, T, k, dlp);
 }
 
-void launch_bwd_dx(const __half* dxr, const int32_t* rows, const int32_t* tok_offsets, const int32_t* epr,
-                   const float* dl, const float* Wr, float* WrT, int T, int d, int E, int k, float* dx,
-                   cudaStream_t stream) {
+void launch_transpose_router(const float* Wr, int d, int E, float* WrT, cudaStream_t stream) {
   const int64_t wt = static_cast<int64_t>(d) * E;
   launch_pdl(transpose_router_kernel, static_cast<unsigned>(std::min<int64_t>((wt + 255) / 256, num_sms() * 8)), 256,
              0, stream, 1, Wr, d, E, WrT);
-  const int64_t total = static_cast<int64_t>(T) * (d / 8);
-  launch_pdl(bwd_dx_kernel, static_cast<unsigned>((total + 255) / 256), 256, 0, stream, 1, dxr, rows, tok_offsets, epr,
-             dl, static_cast<const float*>(WrT), T, d, k, dx);
 }
 
 void launch_bwd_dwr(const __nv_bfloat16* xp, const float* dlp, const int32_t* counts, const int32_t* offsets_p,

@@ -49,7 +49,7 @@ namespace moe {
 // Wgrad are the backward pass (see their epilogues).
 enum GemmMode : int {
   kModeUp = 0, kModeDown = 1, kModeRouter = 2, kModeUpF8 = 3, kModeDownF8 = 4,
-  kModeUpPre = 5, kModeBwdAct = 6, kModeWgrad = 7
+  kModeUpPre = 5, kModeBwdAct = 6, kModeWgrad = 7, kModeDxRows = 8
 };
 
 struct GemmParams {
@@ -94,6 +94,9 @@ struct GemmParams {
   int topk_k;                // <= kFusedTopk
   int32_t* chunk_hist;       // [E * nchunks], zero on entry
   int nchunks;
+  // DxRows: out = acc + row_add[r] * col_add[group][col] (the gate network's term)
+  const float* row_add;      // [cap]
+  const float* col_add;      // [E * out_ld]
 };
 
 constexpr int kProducerWarps = 4;
@@ -232,7 +235,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   using C = GemmCfg<BN, PAIR, EPI>;
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   constexpr bool kF8 = MODE == kModeUpF8 || MODE == kModeDownF8;
-  constexpr bool kDown = MODE == kModeDown || MODE == kModeDownF8;
+  constexpr bool kDown = MODE == kModeDown || MODE == kModeDownF8 || MODE == kModeDxRows;
   constexpr bool kWgrad = MODE == kModeWgrad;
   static_assert(!kF8 || PAIR, "the e4m3 GEMMs run on SM pairs");
   static_assert(!kWgrad || (C::B_ROWS % 64 == 0 && EPI == 4), "weight-gradient tiles: 64-wide B blocks");
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         nx_row0 = gstart + mb * C::BM;
         nx_rows = min(C::BM, gcount - mb * C::BM);
         nx_e = dec_e;
-        if (MODE == kModeDown || MODE == kModeBwdAct)
+        if (MODE == kModeDown || MODE == kModeBwdAct || MODE == kModeDxRows)
           nx_w = r_in_tile < nx_rows ? (p.row_w ? p.row_w[nx_row0 + r_in_tile] : 1.f) : 0.f;
         if (MODE == kModeUpF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
         // F8 down: the gate weight times the row's and the expert's scales
@@ -759,6 +762,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           __half* dst = p.out_f16 + row * p.out_ld + static_cast<int64_t>(nb) * BN;
           float amax = 0.f;
           constexpr int STEP = (BN / NCH) >= 64 ? 64 : 32;
+          // DxRows adds l * col_add[e][col] (the same 32 columns for every lane:
+          // broadcast loads) and checks the range of the sum
+          [[maybe_unused]] float l_row = 0.f;
+          [[maybe_unused]] const float* cadd = nullptr;
+          if constexpr (MODE == kModeDxRows) {
+            l_row = valid ? p.row_add[row] : 0.f;
+            cadd = p.col_add + static_cast<int64_t>(e_tile) * p.out_ld + static_cast<int64_t>(nb) * BN;
+          }
 #pragma unroll 1
           for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
             uint32_t v[2][32];
@@ -768,17 +779,33 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 #pragma unroll
             for (int half = 0; half < STEP / 32; ++half) {
               uint32_t o[16];
+              if constexpr (MODE == kModeDxRows) {
+                const float4* ca = reinterpret_cast<const float4*>(cadd + c0 + 32 * half);
 #pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const float a = __uint_as_float(v[half][2 * q]), b = __uint_as_float(v[half][2 * q + 1]);
-                amax = fmax_nan(amax, fmax_nan(fabsf(a), fabsf(b)));
-                o[q] = pack_half2_satfinite(wr * a, wr * b);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  const float4 cv = __ldg(ca + q4);
+                  const float a0 = fmaf(l_row, cv.x, wr * __uint_as_float(v[half][4 * q4]));
+                  const float b0 = fmaf(l_row, cv.y, wr * __uint_as_float(v[half][4 * q4 + 1]));
+                  const float a1 = fmaf(l_row, cv.z, wr * __uint_as_float(v[half][4 * q4 + 2]));
+                  const float b1 = fmaf(l_row, cv.w, wr * __uint_as_float(v[half][4 * q4 + 3]));
+                  amax = fmax_nan(amax, fmax_nan(fmax_nan(fabsf(a0), fabsf(b0)), fmax_nan(fabsf(a1), fabsf(b1))));
+                  o[2 * q4] = pack_half2_satfinite(a0, b0);
+                  o[2 * q4 + 1] = pack_half2_satfinite(a1, b1);
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  const float a = __uint_as_float(v[half][2 * q]), b = __uint_as_float(v[half][2 * q + 1]);
+                  amax = fmax_nan(amax, fmax_nan(fabsf(a), fabsf(b)));
+                  o[q] = pack_half2_satfinite(wr * a, wr * b);
+                }
               }
               const int c = c0 + 32 * half;
               if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
             }
           }
-          if (valid && !(fabsf(wr) * amax <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
+          const float range = (MODE == kModeDxRows) ? amax : fabsf(wr) * amax;
+          if (valid && !(range <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
         } else if constexpr (MODE == kModeUpPre) {
           // the accumulator itself, (g, u) pairs of the packed W1/W3 rows, in
           // fp32, through the TMA-store boxes as 32 rows x 16 columns (64-byte rows)
@@ -969,7 +996,7 @@ template <int BN, int MODE, bool PAIR>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                        cudaStream_t stream) {
   const bool wide = ((MODE == kModeUp || MODE == kModeUpF8 || MODE == kModeUpPre) && p.num_kb <= 24) ||
-                    ((MODE == kModeDown || MODE == kModeDownF8) && p.num_kb <= 8);
+                    ((MODE == kModeDown || MODE == kModeDownF8 || MODE == kModeDxRows) && p.num_kb <= 8);
   if constexpr (MODE == kModeBwdAct) {
     // the SwiGLU backward's epilogue (fp32 pre-activation loads, the
     // activation's derivative) outlasts a tile's MMAs with four warps
@@ -1306,9 +1333,11 @@ int launch_expert_down_f8(const uint8_t* hq, const float* h_scale, const uint8_t
   return launch_gemm<BN, kModeDownF8, true>(tmA, tmB, tmC, p, stream);
 }
 
-int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
-                       const int32_t* offsets, const float* row_w, __half* ys, int d, int n, int E,
-                       int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+template <int MODE>
+static int launch_down_like(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
+                            const int32_t* offsets, const float* row_w, const float* row_add, const float* col_add,
+                            __half* ys, int d, int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns,
+                            cudaStream_t stream) {
   const int BN = (d % 256 == 0) ? 256 : (d % 128 == 0 ? 128 : 64);
   CUtensorMap tmA, tmB;
   if (!make_map_bf16(&tmA, h, n, rows_cap, 128)) return MOE_ERR_CUDA;
@@ -1319,6 +1348,8 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.counts = counts;
   p.offsets = offsets;
   p.row_w = row_w;
+  p.row_add = row_add;
+  p.col_add = col_add;
   p.out_f16 = ys;
   p.out_ld = d;
   p.E = E;
@@ -1328,21 +1359,37 @@ int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const i
   p.gather = 0;
   if (tails_in_pairs(E, rows_cap)) {
     p.units = 3;
-    return (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, tmC, p, stream)
-           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, tmC, p, stream)
-                         : launch_gemm<64, kModeDown, true>(tmA, tmB, tmC, p, stream);
+    return (BN == 256)   ? launch_gemm<256, MODE, true>(tmA, tmB, tmC, p, stream)
+           : (BN == 128) ? launch_gemm<128, MODE, true>(tmA, tmB, tmC, p, stream)
+                         : launch_gemm<64, MODE, true>(tmA, tmB, tmC, p, stream);
   }
   p.units = 1;
-  int st = (BN == 256)   ? launch_gemm<256, kModeDown, true>(tmA, tmB, tmC, p, stream)
-           : (BN == 128) ? launch_gemm<128, kModeDown, true>(tmA, tmB, tmC, p, stream)
-                         : launch_gemm<64, kModeDown, true>(tmA, tmB, tmC, p, stream);
+  int st = (BN == 256)   ? launch_gemm<256, MODE, true>(tmA, tmB, tmC, p, stream)
+           : (BN == 128) ? launch_gemm<128, MODE, true>(tmA, tmB, tmC, p, stream)
+                         : launch_gemm<64, MODE, true>(tmA, tmB, tmC, p, stream);
   if (st != MOE_OK) return st;
   CUtensorMap tmB1;
   if (!make_map_bf16(&tmB1, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;
   p.units = 2;
-  return (BN == 256)   ? launch_gemm<256, kModeDown, false>(tmA, tmB1, tmC, p, stream)
-         : (BN == 128) ? launch_gemm<128, kModeDown, false>(tmA, tmB1, tmC, p, stream)
-                       : launch_gemm<64, kModeDown, false>(tmA, tmB1, tmC, p, stream);
+  return (BN == 256)   ? launch_gemm<256, MODE, false>(tmA, tmB1, tmC, p, stream)
+         : (BN == 128) ? launch_gemm<128, MODE, false>(tmA, tmB1, tmC, p, stream)
+                       : launch_gemm<64, MODE, false>(tmA, tmB1, tmC, p, stream);
+}
+
+int launch_expert_down(const __nv_bfloat16* h, const __nv_bfloat16* W2p, const int32_t* counts,
+                       const int32_t* offsets, const float* row_w, __half* ys, int d, int n, int E,
+                       int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  return launch_down_like<kModeDown>(h, W2p, counts, offsets, row_w, nullptr, nullptr, ys, d, n, E, rows_cap, status,
+                                     timeout_ns, stream);
+}
+
+// Backward: dxr[r] = dgl[r] W13i_e^T + dL[r] Wr[:, e] (fp16), the expert
+// paths' input gradient and the gate network's for each row; K = 2n.
+int launch_expert_dx(const __nv_bfloat16* dgl, const __nv_bfloat16* W13i, const int32_t* counts,
+                     const int32_t* offsets, const float* dl_row, const float* WrT, __half* dxr, int d, int n,
+                     int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  return launch_down_like<kModeDxRows>(dgl, W13i, counts, offsets, nullptr, dl_row, WrT, dxr, d, 2 * n, E, rows_cap,
+                                       status, timeout_ns, stream);
 }
 
 // ------------------------------------------------------------- backward

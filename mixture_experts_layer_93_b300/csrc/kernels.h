@@ -79,6 +79,9 @@ int launch_expert_up_pre(const __nv_bfloat16* xp, const __nv_bfloat16* W13p, con
 int launch_bwd_act(const __nv_bfloat16* dyp, const __nv_bfloat16* W2, const int32_t* counts, const int32_t* offsets,
                    const float* row_w, const float* gl, __nv_bfloat16* dgl, __nv_bfloat16* hw, float* dw_part, int d,
                    int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+int launch_expert_dx(const __nv_bfloat16* dgl, const __nv_bfloat16* W13i, const int32_t* counts,
+                     const int32_t* offsets, const float* dl_row, const float* WrT, __half* dxr, int d, int n,
+                     int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns, cudaStream_t stream);
 int launch_wgrad(const __nv_bfloat16* A, const __nv_bfloat16* B, const int32_t* counts, const int32_t* offsets,
                  int M, int N, int E, int64_t rows_cap, float* out, float* out2, int32_t* status,
                  uint64_t timeout_ns, cudaStream_t stream);
@@ -119,13 +122,9 @@ void launch_bwd_rows(const int32_t* idx, const float* w, const int32_t* dst, con
 void launch_bwd_zero_pad(const int32_t* counts, const int32_t* offsets_p, int E, int d, int n, __nv_bfloat16* xp,
                          __nv_bfloat16* dyp, __nv_bfloat16* dgl, __nv_bfloat16* hw, cudaStream_t stream);
 // rows / tok_offsets: each token's row list (tok_offsets NULL: k entries per token)
-void launch_bwd_expert_of_rows(const int32_t* counts, const int32_t* offsets_p, int E, int32_t* epr,
-                               cudaStream_t stream);
 void launch_router_bwd(const int32_t* rows, const int32_t* tok_offsets, const float* wp, const float* dw_part,
-                       int parts, int T, int k, float* dl, float* dlp, cudaStream_t stream);
-void launch_bwd_dx(const __half* dxr, const int32_t* rows, const int32_t* tok_offsets, const int32_t* epr,
-                   const float* dl, const float* Wr, float* WrT, int T, int d, int E, int k, float* dx,
-                   cudaStream_t stream);
+                       int parts, int T, int k, float* dlp, cudaStream_t stream);
+void launch_transpose_router(const float* Wr, int d, int E, float* WrT, cudaStream_t stream);
 void launch_bwd_dwr(const __nv_bfloat16* xp, const float* dlp, const int32_t* counts, const int32_t* offsets_p,
                     int E, int d, float* part, float* dbpart, float* dWr, float* db, cudaStream_t stream);
 void launch_gather_rows_by_token(const __nv_bfloat16* x, const int32_t* tok_rows, const int32_t* tok_offsets, int T,
