@@ -173,18 +173,35 @@ __global__ void __launch_bounds__(256) dwr_partial_kernel(const __nv_bfloat16* _
 #pragma unroll
   for (int q = 0; q < 8; ++q) acc[q] = 0.f;
   float dsum = 0.f;
-  for (int i = split * 8 + warp; i < count; i += 8 * S) {
-    const float l = dlp[first + i];
+  // rows in order, four loads issued before their FMAs (same sums, more
+  // bytes in flight)
+  const int stride = 8 * S;
+  auto add_row = [&](float l, const uint4& v) {
     dsum += l;
-    if (col_ok) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(xp + (first + i) * d + c0));
-      const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = fmaf(l, bf16_lo(h[q]), acc[2 * q]);
-        acc[2 * q + 1] = fmaf(l, bf16_hi(h[q]), acc[2 * q + 1]);
-      }
+    for (int q = 0; q < 4; ++q) {
+      acc[2 * q] = fmaf(l, bf16_lo(h[q]), acc[2 * q]);
+      acc[2 * q + 1] = fmaf(l, bf16_hi(h[q]), acc[2 * q + 1]);
     }
+  };
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  int i = split * 8 + warp;
+  for (; i + 3 * stride < count; i += 4 * stride) {
+    float l[4];
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t r = first + i + u * stride;
+      l[u] = dlp[r];
+      v[u] = col_ok ? __ldg(reinterpret_cast<const uint4*>(xp + r * d + c0)) : zero4;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) add_row(l[u], v[u]);
+  }
+  for (; i < count; i += stride) {
+    const int64_t r = first + i;
+    add_row(dlp[r], col_ok ? __ldg(reinterpret_cast<const uint4*>(xp + r * d + c0)) : zero4);
   }
 #pragma unroll
   for (int q = 0; q < 8; ++q) red[warp][lane * 8 + q] = acc[q];
