@@ -350,6 +350,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     if (by_unit) return (unit0 + (i / p.n_blocks) * unit_stride) * p.n_blocks + (i % p.n_blocks);
     return unit0 + i * unit_stride;
   };
+  // the tile after tau (the it-th of this CTA): a plain stride step unless by_unit
+  auto tau_next = [&](int tau, int it) -> int { return by_unit ? tau_of(it + 1) : tau + unit_stride; };
 
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
@@ -418,7 +420,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       uint32_t phase = 0;
       bool ok = true;
       int e = 0;  // group cursor of decode_tile
-      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_next(tau, it), ++it) {
         int nb, mu, gstart, gcount;
         decode_tile<MODE == kModeRouter>(tau, prefix, n_groups, p.n_blocks, e, nb, mu);
         group_rows(p, grp_s, e, gstart, gcount);
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_next(tau, it), ++it) {
         if (!mbar_wait_bounded(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, p.status,
                                kWaitMmaTmemEmpty, p.timeout_ns))
           break;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_of(++it)) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles && ok; tau = tau_next(tau, it), ++it) {
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&afull_bar[stage]), phase, abort_flag, p.status, kWaitRelay,
                                  p.timeout_ns)) {
@@ -703,10 +705,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       // the n-blocks of one m-unit) and whether a logit was NaN
       uint64_t best[kFusedTopk];
       bool nan_seen = false;
-      for (int it = 0, tau = tau_of(0); tau < total_tiles; tau = tau_of(++it)) {
+      for (int it = 0, tau = tau_of(0); tau < total_tiles; tau = tau_next(tau, it), ++it) {
         const int nb = nx_nb, row0 = nx_row0, rows_valid = nx_rows, e_tile = nx_e;
         const float wr = nx_w;
-        if (tau_of(it + 1) < total_tiles) decode_next(tau_of(it + 1));
+        const int tau_n = tau_next(tau, it);
+        if (tau_n < total_tiles) decode_next(tau_n);
         int w = 1;
         if (lane == 0)
           w = mbar_wait_bounded(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, p.status, kWaitEpiTmemFull,
