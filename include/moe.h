@@ -17,6 +17,9 @@
  * Precision: x, the expert weights and h are bf16; every product accumulates
  * in fp32 (tensor memory); ys is stored as fp16 and y is fp32.
  *
+ * Also here: e4m3 variants of the two expert GEMMs (the FP8 block below) and
+ * the layer's backward pass by recomputation (moe_backward, at the end).
+ *
  * The gather of token rows into the up-projection and the SwiGLU activation
  * are fused into the grouped GEMM ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化",
  * sections "Gather 与加载融合" and the "关键 Kernel 对比" table).  The optional
