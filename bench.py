@@ -51,8 +51,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # launch, from an ncu capture of the current kernel on the full workload, keyed
 # by workload, A path and kernel revision; a kernel change bumps GEMM_REV and
 # drops stale entries.
-GEMM_REV = "cta-pair-pdl-fp8-bwd-modes-v10"
-UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 3023890688}  # mean of three launches
+GEMM_REV = "cta-pair-pdl-fp8-bwd-router-topk-v11"
+UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 3508259925}  # mean of three launches
 
 
 def load_peaks():
