@@ -23,6 +23,9 @@ on a bounded token sample on the host cores.
 the C ABI: routing, gathers and pre-activations recomputed, then the four
 backward GEMMs and the router gradient); `value` counts 12*T*k*d*n FLOPs per
 step (twice the forward's, recomputation not counted).
+
+--graph adds a `graph` key: moe_forward captured once into a CUDA graph and
+replayed per step.  --fp8 runs both expert GEMMs in e4m3.
 """
 from __future__ import annotations
 
