@@ -63,9 +63,11 @@ def test_backward_matches_finite_differences(T, d, n, E, k, seed):
         np.testing.assert_allclose(g[key], fd[name], rtol=1e-6, atol=1e-7, err_msg=name)
 
 
-def test_backward_with_token_rounding_matches_finite_differences():
+@pytest.mark.parametrize("mode", [O.ROUND_NEAREST, O.ROUND_UP, O.ROUND_STOCHASTIC])
+def test_backward_with_token_rounding_matches_finite_differences(mode):
     """Rounded sets are held fixed as well: tokens that joined an expert get
-    its gradient, tokens that left get none."""
+    its gradient, tokens that left get none (each rounding mode, the
+    stochastic one with a fixed seed)."""
     rng = np.random.default_rng(7)
     T, d, n, E, k = 9, 4, 3, 3, 1
     p = _layer(rng, T, d, n, E, scale=2.0)
@@ -78,11 +80,31 @@ def test_backward_with_token_rounding_matches_finite_differences():
         col = np.sort(L[:, e].astype(np.float64))
         assert np.min(np.diff(col)) > 1e-3
     assert _min_margin(p, k) > 1e-3
-    g = O.moe_backward(p["x"], p["Wr"], p["bias"], p["W1"], p["W3"], p["W2"], dy, k=k, tile=2,
-                       mode=O.ROUND_NEAREST)
-    fd = _finite_differences(p, dy, k, mode=O.ROUND_NEAREST, tile=2)
+    g = O.moe_backward(p["x"], p["Wr"], p["bias"], p["W1"], p["W3"], p["W2"], dy, k=k, tile=2, mode=mode, seed=5)
+    sizes = np.array([len(st) for st in g["sets"]])
+    assert np.any(sizes != k)  # the rounding changed some token's set
+    fd = _finite_differences_seeded(p, dy, k, mode=mode, tile=2, seed=5)
     for name, key in KEYS.items():
         np.testing.assert_allclose(g[key], fd[name], rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+def _finite_differences_seeded(p, dy, k, mode, tile, seed, h=1e-6):
+    def objective(q):
+        y = O.moe_forward(q["x"], q["Wr"], q["bias"], q["W1"], q["W3"], q["W2"], k=k, tile=tile, mode=mode,
+                          seed=seed)
+        return float(np.sum(dy * y))
+    out = {}
+    for name in ("x", "Wr", "bias", "W1", "W3", "W2"):
+        g = np.zeros_like(p[name])
+        for i in np.ndindex(p[name].shape):
+            q = {kk: v.copy() for kk, v in p.items()}
+            q[name][i] += h
+            fp = objective(q)
+            q[name][i] -= 2 * h
+            fm = objective(q)
+            g[i] = (fp - fm) / (2 * h)
+        out[name] = g
+    return out
 
 
 def test_router_gradient_vanishes_at_k1():
