@@ -1,6 +1,6 @@
 """Benchmark of the MoE-layer forward on B300: one JSON line on rank 0.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config mixtral]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config dsv3]
                     [--round off|nearest|up] [--impl ours|reference]
 
 A step is one pass of the whole layer (route, permute or round, up-projection
@@ -153,33 +153,71 @@ def max_over_ranks(v: float, world: int, device) -> float:
 
 
 # ------------------------------------------------------------ oracle arm
-def oracle_sample_time(cfg, inp_host, round_mode, budget_s: float, seed: int = 0):
-    """Times the oracle (as it stands) on sampled tokens until ~budget_s of CPU
-    work; returns (tokens, seconds, description)."""
-    from oracle import moe_oracle as O
-    rng = np.random.default_rng(seed)
-    # size the sample from a short probe: per-token cost is dominated by
-    # widening the touched experts' weights, so grow the sample geometrically
-    n = 8 if round_mode == "off" else min(cfg.T, 64)
-    total_tok, total_s, total_cpu = 0, 0.0, 0.0
-    while True:
-        toks = np.sort(rng.choice(cfg.T, size=min(n, cfg.T), replace=False))
-        t0, c0 = time.perf_counter(), time.process_time()
-        O.moe_forward(inp_host["x"], inp_host["Wr"], inp_host["bias"], inp_host["W1"], inp_host["W3"],
-                      inp_host["W2"], k=cfg.k, tile=cfg.tile, mode=round_mode, tokens=toks)
-        dt = time.perf_counter() - t0
-        total_cpu += time.process_time() - c0
-        total_tok += len(toks)
-        total_s += dt
-        if total_s >= budget_s:
-            break
-        if dt < budget_s / 4:
-            n = min(cfg.T, n * 2)
-    desc = (f"{total_tok} sampled tokens of the {cfg.name} workload (routing and expert FFN in fp64; "
-            f"expert weights widened per call), {total_s:.1f} s")
-    # threads actually used: process CPU time over wall time
-    threads = max(1, int(round(total_cpu / total_s))) if total_s > 0 else 1
-    return total_tok, total_s, desc, threads
+class OracleLayerSampler:
+    """Times the fp64 oracle (as it stands) on a bounded sample of the whole
+    workload, the same way for the CPU baseline of our arm and for the
+    reference arm.
+
+    One sample is:
+      1. the oracle's routing of every token (gate network, top-k, gate
+         weights; token rounding when on): O.route;
+      2. O.moe_forward over that routing for m seeded experts, i.e. each
+         sampled expert's SwiGLU FFN over every row routed to it (its weights
+         widened to fp64 inside the call, as the oracle does) and the
+         gate-weighted sum into y.
+    The oracle's time for the whole layer is estimated from the sample as
+    t_route + (E / m) * t_experts (the m experts are a uniform random draw,
+    so the scaled sum estimates all E).  m is fixed per workload from a
+    one-expert probe so that a sample takes about `budget_s`."""
+
+    def __init__(self, cfg, inp_host, round_mode, budget_s: float):
+        from oracle import moe_oracle as O
+        self.O, self.cfg, self.inp, self.mode = O, cfg, inp_host, round_mode
+        self.rng = np.random.default_rng(1234)
+        self._one(1)                        # the first call also pays one-time set-up
+        t_route, t_exp, _ = self._one(1)
+        per_expert = max(t_exp, 1e-3)
+        self.m = int(min(cfg.E, max(1, round((budget_s - t_route) / per_expert))))
+
+    def _one(self, m):
+        O, cfg, inp = self.O, self.cfg, self.inp
+        experts = np.sort(self.rng.choice(cfg.E, size=m, replace=False))
+        c0 = time.process_time()
+        t0 = time.perf_counter()
+        routing = O.route(inp["x"], inp["Wr"], inp["bias"], cfg.k, cfg.tile, self.mode)
+        t1 = time.perf_counter()
+        O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k, tile=cfg.tile,
+                      mode=self.mode, routing=routing, experts=experts)
+        t2 = time.perf_counter()
+        self.cpu = getattr(self, "cpu", 0.0) + time.process_time() - c0
+        self.wall = getattr(self, "wall", 0.0) + t2 - t0
+        return t1 - t0, t2 - t1, t2 - t0
+
+    def sample(self):
+        """One timed sample: (estimated whole-layer seconds, measured seconds)."""
+        t_route, t_exp, t_all = self._one(self.m)
+        return t_route + (self.cfg.E / self.m) * t_exp, t_all
+
+    def threads(self):
+        # threads actually used: process CPU time over wall time
+        return max(1, int(round(self.cpu / self.wall))) if getattr(self, "wall", 0) > 0 else 1
+
+    def describe(self, n_samples, measured_s):
+        return (f"{n_samples} samples of the {self.cfg.name} workload, each the fp64 routing of all "
+                f"{self.cfg.T} tokens plus the expert FFNs of {self.m} of {self.cfg.E} seeded experts over "
+                f"all their rows (weights widened per call); whole-layer time estimated as "
+                f"t_route + E/m * t_experts; {measured_s:.1f} s measured")
+
+
+def oracle_baseline(cfg, inp_host, round_mode, budget_s: float, n_samples: int = 3):
+    """The CPU-baseline object of our arm: the oracle's estimated whole-layer
+    throughput from n_samples samples of about budget_s / n_samples each."""
+    smp = OracleLayerSampler(cfg, inp_host, round_mode, budget_s / n_samples)
+    est, meas = zip(*(smp.sample() for _ in range(n_samples)))
+    t_layer = statistics.mean(est)
+    return {"value": 6.0 * cfg.k * cfg.d * cfg.n * cfg.T / t_layer / 1e12, "unit": "TFLOP/s",
+            "tokens_per_s": cfg.T / t_layer, "cores": smp.threads(), "host_cpus": os.cpu_count(),
+            "kind": "oracle", "sample": smp.describe(n_samples, sum(meas))}
 
 
 def run_reference(args, world, rank):
@@ -189,16 +227,45 @@ def run_reference(args, world, rank):
     inp = I.make_inputs(cfg, device="cpu", seed=0)
     if args.backward:
         inp["dy"] = torch.randn(cfg.T, cfg.d, generator=torch.Generator().manual_seed(1000)).to(torch.bfloat16)
-        sample = lambda budget_s, seed: oracle_backward_time(cfg, inp, budget_s, seed)  # noqa: E731
-    else:
-        sample = lambda budget_s, seed: oracle_sample_time(cfg, inp, args.round, budget_s, seed)  # noqa: E731
-    active_per_token = (12.0 if args.backward else 6.0) * cfg.k * cfg.d * cfg.n
+        run_reference_backward(args, cfg, inp)
+        return
+    # each step is one sample; the warm-up steps are samples too
+    budget = max(0.5, args.reference_seconds / max(args.steps, 1))
+    smp = OracleLayerSampler(cfg, inp, args.round, budget)
     for _ in range(args.warmup):
-        sample(0.0, 0)   # one small call each
+        smp.sample()
+    smp.cpu = smp.wall = 0.0
+    est, meas = [], []
+    for _ in range(args.steps):
+        e, m = smp.sample()
+        est.append(e)
+        meas.append(m)
+    t_layer = statistics.mean(est)
+    value = 6.0 * cfg.k * cfg.d * cfg.n * cfg.T / t_layer / 1e12
+    desc = smp.describe(args.steps, sum(meas))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(meas),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.description, "round": args.round, "sample": desc,
+                   "value_from": "whole-layer oracle time estimated from each step's sample; ms_per_step is "
+                                 "the sample's measured time"},
+        "tokens_per_s": cfg.T / t_layer,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": smp.threads(), "kind": "oracle",
+                         "sample": desc, "host_cpus": os.cpu_count()},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_backward(args, cfg, inp):
+    active_per_token = 12.0 * cfg.k * cfg.d * cfg.n
+    for _ in range(args.warmup):
+        oracle_backward_time(cfg, inp, 0.0, 0)   # one small call each
     times, toks, threads = [], 0, 1
     budget = max(1.0, args.reference_seconds / max(args.steps, 1))
     for i in range(args.steps):
-        nt, dt, desc, th = sample(budget, 100 + i)
+        nt, dt, desc, th = oracle_backward_time(cfg, inp, budget, 100 + i)
         times.append(dt)
         toks += nt
         threads = max(threads, th)
@@ -206,7 +273,7 @@ def run_reference(args, world, rank):
     tps = toks / total
     value = tps * active_per_token / 1e12
     line = {
-        "impl": "reference", "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.description, "round": args.round, "tokens_per_step": toks // args.steps},
@@ -259,7 +326,7 @@ def run_backward(args, world, rank, local):
         cfg = cfg.with_tokens(args.tokens)
     T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
     shape = B.make_shape(T, d, n, E, k, cfg.tile, args.round, args.seed)
-    inp = I.make_inputs(cfg, device=dev, seed=rank)
+    inp = I.make_replica_inputs(cfg, rank, device=dev)
     g = torch.Generator(device=dev).manual_seed(1000 + rank)
     dy = torch.randn(T, d, generator=g, device=dev).to(torch.bfloat16)
     W13p, _ = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
@@ -401,7 +468,7 @@ def run_ours(args, world, rank, local):
         cfg = replace(cfg, E=args.experts)
     mode = args.round
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
-    inp = I.make_inputs(cfg, device=dev, seed=rank)
+    inp = I.make_replica_inputs(cfg, rank, device=dev)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     W13q = sW13 = W2q = sW2 = None
     if args.fp8:
@@ -652,10 +719,20 @@ def run_ours(args, world, rank, local):
     comb_gbs = comb_bytes / (statistics.mean(stage_ms["combine"]) * 1e-3) / 1e9
     down_flops = 2.0 * R * n * d
     stage_summary = {s: round(statistics.mean(v), 4) for s, v in stage_ms.items()}
+    # routing stage, algorithmic bytes: x and Wr read once; logits, top-k ids
+    # and weights written once; with the permutation also counts, offsets and
+    # src, dst, row_token, row_w written once
+    route_stage = "route_permute" if mode == "off" else "route"
+    route_bytes = T * d * 2 + d * E * 4 + T * E * 4 + A * 8
+    if mode == "off":
+        route_bytes += (2 * E + 1) * 4 + A * 16
+    route_gbs = route_bytes / (statistics.mean(stage_ms[route_stage]) * 1e-3) / 1e9
     extra = {
         "stage_ms": stage_summary,
         "down_tflops": down_flops / (statistics.mean(stage_ms["down"]) * 1e-3) / 1e12,
         "combine_gbs": comb_gbs, "combine_frac_hbm": comb_gbs / hbm_peak,
+        route_stage + "_gbs": route_gbs, route_stage + "_frac_hbm": route_gbs / hbm_peak,
+        route_stage + "_bytes": route_bytes,
         "rows": R,
     }
     line = {
@@ -687,12 +764,41 @@ def run_ours(args, world, rank, local):
     if graph_line is not None:
         line["graph"] = graph_line
     if inp_host is not None:
-        ntok, secs, desc, threads = oracle_sample_time(cfg, inp_host, mode, budget_s=args.cpu_seconds)
-        tps = ntok / secs
-        line["cpu_baseline"] = {"value": tps * 6.0 * k * d * n / 1e12, "unit": "TFLOP/s", "tokens_per_s": tps,
-                                "cores": threads, "host_cpus": os.cpu_count(), "kind": "oracle",
-                                "sample": desc}
+        line["cpu_baseline"] = oracle_baseline(cfg, inp_host, mode, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+def launch_ranks(args) -> int:
+    """`--gpus N` without a launcher: start N ranks of this script, one per
+    GPU, with torch.distributed.run on this node (rendezvous on 127.0.0.1),
+    exactly as a torchrun launch of the same command would, and return the
+    launcher's exit status.  Rank 0 prints the JSON line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def run_dry(args, world, rank):
+    """The replica set-up without the GPU: each rank draws its replica's
+    inputs (tiny shapes allowed) on the CPU, the ranks meet at the barrier,
+    check that their weights are identical and their tokens are not, and
+    reduce a per-rank time with the max, as a measured run does."""
+    cfg = I.get_config(args.config)
+    inp = I.make_replica_inputs(cfg, rank, device="cpu")
+    dev = torch.device("cpu")
+    wsum = float(sum(inp[k_].double().abs().sum() for k_ in ("Wr", "W1", "W3", "W2")))
+    xsum = float(inp["x"].double().sum())
+    barrier(world)
+    same_w = max_over_ranks(wsum, world, dev) == -max_over_ranks(-wsum, world, dev)
+    distinct_x = world == 1 or max_over_ranks(xsum, world, dev) != -max_over_ranks(-xsum, world, dev)
+    t = max_over_ranks(1.0 + rank, world, dev)
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "n_gpus": world, "max_rank_time": t, "weights_identical": same_w,
+                          "tokens_distinct": distinct_x, "config": {"workload": cfg.description}}), flush=True)
 
 
 def main():
@@ -700,7 +806,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="mixtral", choices=sorted(I.CONFIGS))
+    ap.add_argument("--config", default="dsv3", choices=sorted(I.CONFIGS))
     ap.add_argument("--round", default="off", choices=["off", "nearest", "up", "stochastic"])
     ap.add_argument("--seed", type=int, default=0, help="seed of the stochastic rounding draws")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling of small cases only)")
@@ -718,7 +824,11 @@ def main():
                     help="also time moe_forward replayed from one captured CUDA graph")
     ap.add_argument("--backward", action="store_true",
                     help="measure the backward pass (moe_backward) instead of the forward")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="replica set-up, barrier and max-over-ranks only, on the CPU (no kernels)")
     args = ap.parse_args()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_ranks(args))
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
         # the oracle runs on rank 0 only; the other ranks exit without work
@@ -727,7 +837,10 @@ def main():
         return
     world, rank, local = dist_init(args)
     try:
-        (run_backward if args.backward else run_ours)(args, world, rank, local)
+        if args.dry_run:
+            run_dry(args, world, rank)
+        else:
+            (run_backward if args.backward else run_ours)(args, world, rank, local)
     finally:
         if world > 1:
             import torch.distributed as dist

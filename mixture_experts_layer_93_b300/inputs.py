@@ -124,6 +124,18 @@ def make_inputs(cfg: MoEConfig, device="cpu", seed: int = 0, weights: bool = Tru
     return out
 
 
+def make_replica_inputs(cfg: MoEConfig, rank: int, device="cpu") -> dict:
+    """Inputs of one data-parallel replica: every rank holds the same layer
+    (x, Wr, bias and weights drawn with seed 0, as make_inputs) and rank r > 0
+    replaces x with its own tokens, drawn from the same distribution with
+    seed 1_000_003 * r."""
+    out = make_inputs(cfg, device=device, seed=0)
+    if rank > 0:
+        g = _gen(torch.device(device), 1_000_003 * rank)
+        out["x"] = (torch.randn(cfg.T, cfg.d, generator=g, device=device) * cfg.x_std).to(torch.bfloat16)
+    return out
+
+
 def make_logits(T: int, E: int, device="cpu", seed: int = 0, ties: bool = True) -> torch.Tensor:
     """fp32 router logits [T, E].  With `ties`, values sit on a coarse grid
     (multiples of 1/4, including both signed zeros) so equal logits are common."""

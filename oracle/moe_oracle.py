@@ -314,13 +314,20 @@ def route(x, Wr, bias, k: int, tile: int = 128, mode: str = ROUND_OFF, tokens=No
 
 
 def moe_forward(x, Wr, bias, W1, W3, W2, k: int, tile: int = 128, mode: str = ROUND_OFF,
-                tokens=None, return_routing: bool = False, seed: int = 0):
+                tokens=None, return_routing: bool = False, seed: int = 0, routing=None, experts=None):
     """y[t] = sum_{e in S_t} w_te * FFN_e(x[t]) for the requested tokens, fp64.
 
     Dataflow of the moe_forward pseudocode ("MoE架构的物理瓶颈与扩展限制解析",
     section 工作原理) with both all-to-all steps removed (one GPU), and the
-    five steps of the fused kernel ("硬件加速的考量", section 自定义核与核融合)."""
-    tokens, sets, weights = route(x, Wr, bias, k, tile, mode, tokens, seed=seed)
+    five steps of the fused kernel ("硬件加速的考量", section 自定义核与核融合).
+
+    `routing`, when given, is the (tokens, sets, weights) that `route` returned
+    for these arguments and is used instead of routing again.  `experts`, when
+    given, restricts the sum to the experts listed (the terms of the others are
+    left out), so y over a partition of the experts adds up to the full y."""
+    if routing is None:
+        routing = route(x, Wr, bias, k, tile, mode, tokens, seed=seed)
+    tokens, sets, weights = routing
     x64 = _f64(x)
     d = x64.shape[1]
     y = np.zeros((len(tokens), d), dtype=F64)
@@ -331,7 +338,7 @@ def moe_forward(x, Wr, bias, W1, W3, W2, k: int, tile: int = 128, mode: str = RO
         for e, we in zip(s, w):
             pos_of[int(e)].append(p)
             w_of[int(e)].append(we)
-    for e in range(E):
+    for e in (range(E) if experts is None else sorted({int(v) for v in experts})):
         if not pos_of[e]:
             continue
         pos = np.array(pos_of[e], dtype=np.int64)

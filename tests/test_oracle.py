@@ -227,6 +227,44 @@ def test_token_subset_equals_full_rows():
         assert np.array_equal(sets_sub[i], sets_full[t])
 
 
+def test_expert_subset_and_given_routing():
+    """moe_forward restricted to a subset of experts keeps exactly the terms of
+    those experts (checked by explicit loops), the subsets of a partition add
+    up to the full layer, and routing passed in gives the same y as routing
+    inside the call."""
+    rng = np.random.default_rng(21)
+    T, d, n, E, k = 5, 4, 3, 5, 2
+    x = rng.normal(size=(T, d))
+    Wr = rng.normal(size=(d, E))
+    W1 = rng.normal(size=(E, d, n))
+    W3 = rng.normal(size=(E, d, n))
+    W2 = rng.normal(size=(E, n, d))
+    sub = [3, 0]
+    y_sub = O.moe_forward(x, Wr, None, W1, W3, W2, k=k, experts=sub)
+    for t in range(T):
+        logit = [sum(x[t, i] * Wr[i, e] for i in range(d)) for e in range(E)]
+        chosen = sorted(range(E), key=lambda e: (-np.float32(logit[e]), e))[:k]
+        m = max(logit[e] for e in chosen)
+        z = {e: math.exp(logit[e] - m) for e in chosen}
+        for i in range(d):
+            acc = 0.0
+            for e in chosen:
+                if e not in sub:
+                    continue
+                o = 0.0
+                for j in range(n):
+                    g = sum(x[t, q] * W1[e, q, j] for q in range(d))
+                    u = sum(x[t, q] * W3[e, q, j] for q in range(d))
+                    o += (g / (1.0 + math.exp(-g))) * u * W2[e, j, i]
+                acc += z[e] / sum(z.values()) * o
+            assert math.isclose(y_sub[t, i], acc, rel_tol=1e-11, abs_tol=1e-12)
+    full = O.moe_forward(x, Wr, None, W1, W3, W2, k=k)
+    parts = [O.moe_forward(x, Wr, None, W1, W3, W2, k=k, experts=p) for p in ([0, 3], [1], [2, 4])]
+    np.testing.assert_allclose(sum(parts), full, rtol=1e-13, atol=1e-14)
+    routing = O.route(x, Wr, None, k)
+    np.testing.assert_array_equal(O.moe_forward(x, Wr, None, W1, W3, W2, k=k, routing=routing), full)
+
+
 # -------------------------------------------------------------- logits
 def test_router_logits_one_hot_rows():
     rng = np.random.default_rng(12)
