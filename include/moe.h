@@ -20,11 +20,15 @@
  * Also here: e4m3 variants of the two expert GEMMs (the FP8 block below) and
  * the layer's backward pass by recomputation (moe_backward, at the end).
  *
- * The gather of token rows into the up-projection and the SwiGLU activation
- * are fused into the grouped GEMM ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化",
- * sections "Gather 与加载融合" and the "关键 Kernel 对比" table).  The optional
- * token rounding (same page, "3. Token Rounding 路由算法") rounds each expert's
- * row count to a multiple of a tile (moe_token_round).
+ * The SwiGLU activation is fused into the up-projection's epilogue and the
+ * gate weight into the down-projection's ("SonicMoE: 加速 MoE 模型的 IO 与 Tile
+ * 感知优化", the "关键 Kernel 对比" table).  The gather of token rows can also be
+ * fused into the up-projection's operand load (same page, "Gather 与加载融合";
+ * moe_expert_up with gather = 1 or 2), but moe_forward stages the rows with a
+ * token-order copy kernel and loads them with tiled TMA (gather = 0), which
+ * measured faster on B300.  The optional token rounding (same page, "3. Token
+ * Rounding 路由算法") rounds each expert's row count to a multiple of a tile
+ * (moe_token_round).
  *
  * Conventions (every entry point):
  *   - All tensor pointers are DEVICE pointers, 16-byte aligned, row-major and
@@ -184,9 +188,13 @@ int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const 
  * the process exits), so the shape must satisfy E * ceil(T*k / 2048) <=
  * 262144; larger shapes return MOE_ERR_WORKSPACE and launch nothing.  No
  * allocation or free of any kind happens in this call.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and caches it; make that first call before any
- *     stream capture on that device.
+ *   - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *     which allocates nothing) in the CUDA context current on the calling
+ *     thread, and launches into that context.  The address is not cached, so
+ *     a caller running in its own driver-API context, or calling again after
+ *     cudaDeviceReset, gets the address valid in its context.  The first call
+ *     in a context may load the library's kernels into it; make that first
+ *     call before any stream capture in that context.
  *   - All calls share the one array: two calls whose kernels overlap on the
  *     GPU (different streams, or different host threads) race and give wrong
  *     results.  Serialise them.
@@ -214,8 +222,8 @@ int moe_token_round(const moe_shape* s, const float* logits, const int32_t* topk
                     int32_t* tok_offsets, int32_t* tok_rows, void* ws, size_t ws_bytes,
                     void* stream);
 
-/* Up-projection grouped GEMM with the row gather fused into the operand load
- * and SwiGLU fused into the epilogue:
+/* Up-projection grouped GEMM over gathered token rows, with SwiGLU fused into
+ * the epilogue:
  *   for each expert e and row r in [offsets[e], offsets[e+1]):
  *     h[r, :] = bf16( silu(x[row_token[r]] W1_e) * (x[row_token[r]] W3_e) )
  *   silu(z) = z / (1 + exp(-z)); fp32 accumulation in tensor memory.
@@ -276,8 +284,9 @@ int moe_workspace_layout(const moe_shape* s, int64_t* offsets_out, int32_t n_out
  * e4m3(fp32(x * fp32(448 / amax))) rounded to nearest-even and saturated to
  * +-448; an all-zero row has scale 1 and codes 0.  Rows: tokens and the
  * output channels of the packed gate / linear weights (up-projection), rows
- * of the bf16 hidden h and one row per expert for all of W2
- * (down-projection).  Routing and the combine stay as in moe_forward. */
+ * of the bf16 hidden h and the output channels of W2, i.e. the rows of the
+ * packed W2p (down-projection).  A weight outlier therefore coarsens only its
+ * own channel's codes.  Routing and the combine stay as in moe_forward. */
 
 /* Workspace bytes of the FP8 entry points that quantise h
  * (moe_expert_down_fp8, moe_forward_fp8): moe_workspace_bytes plus the e4m3
@@ -286,7 +295,8 @@ size_t moe_workspace_bytes_fp8(const moe_shape* s);
 
 /* codes[rows, K] (e4m3 bytes) and scales[rows] fp32 of src[rows, K] bf16.
  * K % 16 == 0; src and codes 16-byte aligned.  For the weights, src is W13p
- * from moe_prepare_weights viewed as [E * 2n, d]. */
+ * from moe_prepare_weights viewed as [E * 2n, d], or W2p viewed as
+ * [E * d, n]. */
 int moe_quantize_rows_fp8(const void* src, int64_t rows, int32_t K, void* codes, float* scales,
                           void* stream);
 
@@ -301,18 +311,21 @@ int moe_expert_up_fp8(const moe_shape* s, const void* x, const void* W13q, const
                       const int32_t* counts, const int32_t* offsets, const int32_t* tok_offsets,
                       const int32_t* tok_rows, void* h, void* ws, size_t ws_bytes, void* stream);
 
-/* codes[E, m] and scales[E] with one scale per row of m elements (a whole
- * expert: W2p from moe_prepare_weights viewed as [E, d * n]).  m % 16 == 0. */
+/* codes[E, m] and scales[E] with one scale per row of m elements (one scale
+ * for a whole expert's matrix, e.g. W2p viewed as [E, d * n]).  m % 16 == 0.
+ * The FP8 GEMMs do not take these per-expert scales; they are here for
+ * callers that store weights that way. */
 int moe_quantize_experts_fp8(const void* src, int32_t E, int64_t m, void* codes, float* scales,
                              void* stream);
 
 /* Down-projection with e4m3 operands: h [moe_row_capacity, n] bf16 (as
  * moe_expert_up writes it) is quantised per row into the workspace
- * (moe_workspace_bytes_fp8), then ys[row] = w[row] * (code_h . code_W2) *
- * scale_h[row] * scale_W2[e] in fp32 (kind::f8f6f4 on SM pairs), stored fp16
- * as moe_expert_down (saturation reported alike).  W2q / sW2 from
- * moe_quantize_experts_fp8 of W2p.  Requires n % 128 == 0 and d % 256 == 0
- * (else MOE_ERR_UNSUPPORTED). */
+ * (moe_workspace_bytes_fp8), then ys[row][c] = w[row] * (code_h . code_W2[c]) *
+ * scale_h[row] * scale_W2[e * d + c] in fp32 (kind::f8f6f4 on SM pairs),
+ * stored fp16 as moe_expert_down (saturation reported alike).  W2q [E * d, n]
+ * / sW2 [E * d] from moe_quantize_rows_fp8 of W2p (one scale per output
+ * channel).  Requires n % 128 == 0 and d % 256 == 0 (else
+ * MOE_ERR_UNSUPPORTED). */
 int moe_expert_down_fp8(const moe_shape* s, const void* h, const void* W2q, const float* sW2,
                         const int32_t* counts, const int32_t* offsets, const float* row_w, void* ys,
                         void* ws, size_t ws_bytes, void* stream);

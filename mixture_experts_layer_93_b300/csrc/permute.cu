@@ -13,7 +13,6 @@
 #include "kernels.h"
 #include "topk.cuh"
 
-#include <mutex>
 
 namespace moe {
 
@@ -306,29 +305,24 @@ void launch_permute_list(const int32_t* expert_of, const float* w, const int32_t
 //
 // Its chunk histograms live in a file-scope device array instead of a
 // caller-provided workspace.  The host cannot pass that array's name to a
-// kernel (in host code it is only a stand-in symbol), so the device address is
-// looked up once per device with cudaGetSymbolAddress and cached.
+// kernel (in host code it is only a stand-in symbol), so its device address is
+// looked up with cudaGetSymbolAddress.  The address belongs to the CUDA context
+// that is current when it is looked up (each context loads its own copy of the
+// module), so it is looked up again on every call rather than cached: a
+// caller that runs in its own driver-API context, or calls again after
+// cudaDeviceReset, gets the address that is valid in its context.  The lookup
+// allocates nothing.
 namespace moe {
 
 constexpr int64_t kNoAllocScratchInts = 262144;  // 1 MiB
 static __device__ __align__(256) int32_t g_perm_scratch[kNoAllocScratchInts];
 
-constexpr int kMaxDevices = 64;
-static std::mutex g_scratch_mutex;
-static int32_t* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of g_perm_scratch on the current device (looked up on the
-// first call for that device); nullptr if the lookup fails.
+// Device address of g_perm_scratch in the current context; nullptr if the
+// lookup fails.
 static int32_t* noalloc_scratch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_perm_scratch) != cudaSuccess) return nullptr;
-    g_scratch_ptr[dev] = static_cast<int32_t*>(ptr);
-  }
-  return g_scratch_ptr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_perm_scratch) != cudaSuccess) return nullptr;
+  return static_cast<int32_t*>(ptr);
 }
 
 }  // namespace moe
