@@ -472,9 +472,9 @@ def run_ours(args, world, rank, local):
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     W13q = sW13 = W2q = sW2 = None
     if args.fp8:
-        # e4m3 GEMMs: codes with one scale per packed W1/W3 row and one per expert of W2
+        # e4m3 GEMMs: codes with one scale per packed W1/W3 row and per packed W2 row
         W13q, sW13 = B.moe_quantize_rows_fp8(W13p)
-        W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+        W2q, sW2 = B.moe_quantize_rows_fp8(W2p)
         del W13p, W2p
         W13p = W2p = None
     inp_host = None
@@ -742,7 +742,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
                    "up_gather": ["gather_kernel+tma", "tma_gather4", "cp_async"][args.gather],
-                   "expert_gemm_operands": "e4m3 (x per token, W1/W3 per channel, h per row, W2 per expert)"
+                   "expert_gemm_operands": "e4m3 (x per token, W1/W3 per channel, h per row, W2 per channel)"
                    if args.fp8 else "bf16",
                    "tile": cfg.tile if mode != "off" else None,
                    "l2": "256 MiB buffer written between timed steps; expert weights also exceed L2",

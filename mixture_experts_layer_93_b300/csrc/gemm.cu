@@ -10,12 +10,15 @@
 //                  SwiGLU backward in its epilogue; the weight gradients, whose
 //                  K is each expert's rows, from MN-major operands
 //
-// The row gather is fused into the operand load, the SwiGLU activation and the
-// gate weight into the epilogue, and loads overlap the MMAs ("SonicMoE: 加速
-// MoE 模型的 IO 与 Tile 感知优化": sections "2. IO 与计算重叠的 GPU Kernel",
-// "Gather 与加载融合" and the "关键 Kernel 对比" table, rows "Gather 融合",
-// "SwiGLU 融合", "MMA 与 IO 重叠").  The page's kernels use cp.async on
-// Hopper; here the roles map onto Blackwell hardware:
+// The SwiGLU activation and the gate weight are fused into the epilogue, and
+// loads overlap the MMAs ("SonicMoE: 加速 MoE 模型的 IO 与 Tile 感知优化":
+// sections "2. IO 与计算重叠的 GPU Kernel", "Gather 与加载融合" and the "关键
+// Kernel 对比" table, rows "Gather 融合", "SwiGLU 融合", "MMA 与 IO 重叠").  The
+// up-projection's A rows come either from a staging buffer the token-order
+// copy kernel filled (tiled TMA, `gather` 0, the forward's path) or straight
+// from x by a gather fused into the operand load (`gather` 1 and 2).  The
+// page's kernels use cp.async on Hopper; here the roles map onto Blackwell
+// hardware:
 //
 //   warps 0..3  producers.  B tiles (and A tiles of contiguous rows) come by
 //               tiled TMA, issued by warp 0.  Gathered A rows come either by
@@ -77,8 +80,7 @@ struct GemmParams {
   int32_t* status;
   uint64_t timeout_ns;
   const float* row_scale;    // F8: scale of each A row [cap]
-  const float* col_scale;    // F8 up: scale of each B row (output channel) [E * b_rows_per_expert];
-                             // F8 down: one scale per expert [E]
+  const float* col_scale;    // F8: scale of each B row (output channel) [E * b_rows_per_expert]
   // backward
   const float* pre;          // BwdAct: pre-activations (g, u interleaved) [cap, 2 * out_ld]
   __nv_bfloat16* out2_bf16;  // BwdAct: w * h [cap, out_ld]
@@ -694,11 +696,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         if (MODE == kModeDown || MODE == kModeBwdAct || MODE == kModeDxRows)
           nx_w = r_in_tile < nx_rows ? (p.row_w ? p.row_w[nx_row0 + r_in_tile] : 1.f) : 0.f;
         if (MODE == kModeUpF8) nx_w = r_in_tile < nx_rows ? p.row_scale[nx_row0 + r_in_tile] : 0.f;
-        // F8 down: the gate weight times the row's and the expert's scales
+        // F8 down: the gate weight times the row's scale (the output
+        // channels' scales are applied per column)
         if (MODE == kModeDownF8)
-          nx_w = r_in_tile < nx_rows
-                     ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] * p.col_scale[dec_e]
-                     : 0.f;
+          nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] : 0.f;
       };
       if (tau_of(0) < total_tiles) decode_next(tau_of(0));
       // router with the top-k fused: the token's best keys so far (across
@@ -773,6 +774,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
             l_row = valid ? p.row_add[row] : 0.f;
             cadd = p.col_add + static_cast<int64_t>(e_tile) * p.out_ld + static_cast<int64_t>(nb) * BN;
           }
+          // F8: each output column (a row of the packed W2) has its own scale;
+          // the same 32 columns for every lane: broadcast loads
+          [[maybe_unused]] const float* cscale = nullptr;
+          if constexpr (MODE == kModeDownF8)
+            cscale = p.col_scale + static_cast<int64_t>(e_tile) * p.b_rows_per_expert + static_cast<int64_t>(nb) * BN;
 #pragma unroll 1
           for (int c0 = ch * (BN / NCH); c0 < (ch + 1) * (BN / NCH); c0 += STEP) {
             uint32_t v[2][32];
@@ -782,7 +788,20 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 #pragma unroll
             for (int half = 0; half < STEP / 32; ++half) {
               uint32_t o[16];
-              if constexpr (MODE == kModeDxRows) {
+              if constexpr (MODE == kModeDownF8) {
+                const float4* cs4 = reinterpret_cast<const float4*>(cscale + c0 + 32 * half);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  const float4 sv = __ldg(cs4 + q4);
+                  const float a0 = wr * __uint_as_float(v[half][4 * q4]) * sv.x;
+                  const float b0 = wr * __uint_as_float(v[half][4 * q4 + 1]) * sv.y;
+                  const float a1 = wr * __uint_as_float(v[half][4 * q4 + 2]) * sv.z;
+                  const float b1 = wr * __uint_as_float(v[half][4 * q4 + 3]) * sv.w;
+                  amax = fmax_nan(amax, fmax_nan(fmax_nan(fabsf(a0), fabsf(b0)), fmax_nan(fabsf(a1), fabsf(b1))));
+                  o[2 * q4] = pack_half2_satfinite(a0, b0);
+                  o[2 * q4 + 1] = pack_half2_satfinite(a1, b1);
+                }
+              } else if constexpr (MODE == kModeDxRows) {
                 const float4* ca = reinterpret_cast<const float4*>(cadd + c0 + 32 * half);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
@@ -807,7 +826,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
               if (warp_rows > 0) store_chunk(o, nb * BN + c, row_w0, warp_rows, row, dst + c);
             }
           }
-          const float range = (MODE == kModeDxRows) ? amax : fabsf(wr) * amax;
+          const float range = (MODE == kModeDxRows || MODE == kModeDownF8) ? amax : fabsf(wr) * amax;
           if (valid && !(range <= kHalfMax)) report_error(p.status, MOE_ERR_DEVICE_CHECK, kYsOverflow);
         } else if constexpr (MODE == kModeUpPre) {
           // the accumulator itself, (g, u) pairs of the packed W1/W3 rows, in
@@ -1306,9 +1325,10 @@ int launch_expert_up_f8(const __nv_bfloat16* x, const uint8_t* W13q, const float
 }
 
 // e4m3 down-projection: hq [cap, n] codes with one scale per row, W2q
-// [E * d, n] codes with one scale per expert; the epilogue multiplies by the
-// gate weight times both scales and stores fp16 ys as the bf16 path.  n % 128
-// == 0 and d % 256 == 0; odd last blocks run as half-empty pairs.
+// [E * d, n] codes with one scale per row (output channel); the epilogue
+// multiplies by the gate weight, the row's scale and each column's scale and
+// stores fp16 ys as the bf16 path.  n % 128 == 0 and d % 256 == 0; odd last
+// blocks run as half-empty pairs.
 int launch_expert_down_f8(const uint8_t* hq, const float* h_scale, const uint8_t* W2q, const float* sW2,
                           const int32_t* counts, const int32_t* offsets, const float* row_w, __half* ys, int d,
                           int n, int E, int64_t rows_cap, int32_t* status, uint64_t timeout_ns,

@@ -58,8 +58,9 @@ Readings of the pages (where they are silent or at odds):
     scale 1 and codes 0).  Up-projection: rows are tokens (activations) and
     output channels (a row of the packed W1/W3).  Down-projection (the
     "fp8" layer): rows of the bf16 hidden h (as the up-projection stores it)
-    and one row per expert for all of W2.  The GEMMs run on the dequantised
-    values code * scale; routing and the combine stay as above.
+    and the output channels of W2 (each column of W2e [n, d], quantised over
+    its n elements).  The GEMMs run on the dequantised values code * scale;
+    routing and the combine stay as above.
   * Backward: the pages give no formulas, only that the gradients stay
     those of the MoE formula while intermediates are recomputed.  The
     reading is the exact gradient of the forward above for a given dy = dL/dy,
@@ -456,16 +457,15 @@ def bf16_round(a) -> np.ndarray:
 
 
 def quantized_expert_down_weight(W2e) -> np.ndarray:
-    """W2e [n, d] as the FP8 down-projection uses it: one scale for the
-    whole expert, dequantised."""
-    W = _f64(W2e)
-    return dequantized_rows_e4m3(W.reshape(1, -1)).reshape(W.shape)
+    """W2e [n, d] as the FP8 down-projection uses it: each output channel (a
+    column, n elements) quantised with its own scale, dequantised."""
+    return dequantized_rows_e4m3(_f64(W2e).T).T
 
 
 def moe_forward_fp8_full(x, Wr, bias, W1, W3, W2, k: int, tokens=None):
     """The layer with both expert GEMMs in e4m3: the up-projection as in
     moe_forward_fp8; h rounded to bf16 (as stored), quantised per row, and
-    multiplied by the per-expert quantised W2.  fp64 result."""
+    multiplied by W2 quantised per output channel.  fp64 result."""
     tokens, sets, weights = route(x, Wr, bias, k, tokens=tokens)
     x64 = _f64(x)
     xq = dequantized_rows_e4m3(x64[tokens])

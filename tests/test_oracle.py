@@ -488,18 +488,37 @@ def test_bf16_round_matches_torch():
     assert np.array_equal(O.bf16_round(a), ref)
 
 
-def test_fp8_down_weight_one_scale_per_expert():
+def test_fp8_down_weight_one_scale_per_output_channel():
+    """Each output channel (column of W2e [n, d]) has its own scale: its
+    largest element codes to exactly 448, and every element is within half
+    an e4m3 step of that channel's scale."""
     rng = np.random.default_rng(8)
-    W = rng.standard_normal((24, 40)) / 5
+    W = rng.standard_normal((24, 40)) / 5 * 10.0 ** rng.uniform(-2, 2, size=40)[None, :]
     Wh = O.quantized_expert_down_weight(W)
-    s = np.float32(np.abs(W).max()) / np.float32(448)
-    codes = Wh / np.float64(np.float32(s))
-    assert np.abs(np.abs(codes).max() - 448) < 1e-3
-    assert np.all(np.abs(Wh - W) <= 2.0 ** -4 * np.abs(W) + 2.0 ** -9 * float(s) + 1e-12)
+    s = (np.abs(W).max(axis=0).astype(np.float32) / np.float32(448)).astype(np.float64)
+    codes = Wh / s[None, :]
+    assert np.all(np.abs(np.abs(codes).max(axis=0) - 448) < 1e-3)
+    assert np.all(np.abs(Wh - W) <= 2.0 ** -4 * np.abs(W) + 2.0 ** -9 * s[None, :] + 1e-12)
+
+
+def test_fp8_down_weight_outlier_channel_stays_local():
+    """A planted outlier channel, 10^5 times the others, coarsens only its own
+    channel: the other channels keep e4m3's relative precision.  One scale for
+    the whole matrix (the failing control) would push them into e4m3's
+    subnormal range."""
+    rng = np.random.default_rng(9)
+    W = rng.standard_normal((64, 32)) / 8
+    W[:, 5] *= 1e5
+    rel = lambda a, b: np.abs(a - b) / np.abs(b)  # noqa: E731
+    per_channel = O.quantized_expert_down_weight(W)
+    others = np.delete(np.arange(32), 5)
+    assert rel(per_channel[:, others], W[:, others]).max() <= 2.0 ** -4 + 1e-12
+    one_scale = O.dequantized_rows_e4m3(W.reshape(1, -1)).reshape(W.shape)
+    assert rel(one_scale[:, others], W[:, others]).max() > 0.25
 
 
 def test_fp8_full_layer_within_quantisation_bound_of_fp8_up_layer():
-    """Quantising h per row and W2 per expert moves each output by at most the
+    """Quantising h per row and W2 per output channel moves each output by at most the
     e4m3 half-step of both factors: |dy| <= sum_e w_e (|h_e| |W2_e|) * 2^-3 (+ tiny)."""
     rng = np.random.default_rng(4)
     T, d, n, E, k = 30, 48, 40, 5, 2

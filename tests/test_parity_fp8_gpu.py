@@ -123,7 +123,7 @@ def test_expert_down_fp8(cuda_device, T, d, n, E, k):
     wcap = torch.zeros(cap)
     wcap[:A] = torch.rand(A, generator=g)
     _, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
-    W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+    W2q, sW2 = B.moe_quantize_rows_fp8(W2p)
     ys = B.moe_expert_down_fp8(s, hcap.to(cuda_device), W2q, sW2,
                                torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
                                torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap.to(cuda_device), ws)
@@ -140,13 +140,58 @@ def test_expert_down_fp8(cuda_device, T, d, n, E, k):
     assert np.all(np.abs(got - ref) <= 2.0 ** -11 * np.abs(ref) + 1e-5 * rms), err_stats(got, ref)
 
 
+def test_expert_down_fp8_outlier_channel(cuda_device):
+    """W2 with planted outlier output channels (10^4 times the others): with
+    one scale per output channel the other channels keep e4m3 precision, and
+    ys stays within one fp16 rounding of the oracle's product."""
+    T, d, n, E, k = 600, 256, 128, 4, 2
+    cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=31)
+    W2 = inp["W2"].float()
+    W2[:, :, 17] *= 1e4
+    W2[2, :, 200] *= 1e4
+    W2 = W2.to(torch.bfloat16)
+    counts, offsets, src, dst = _routing(T, E, k, seed=5)
+    A = T * k
+    g = torch.Generator(device="cpu").manual_seed(10)
+    s = B.make_shape(T, d, n, E, k)
+    ws = B.Workspace(s, cuda_device, fp8=True)
+    cap = B.moe_row_capacity(s)
+    hcap = torch.zeros(cap, n, dtype=torch.bfloat16)
+    hcap[:A] = (torch.randn(A, n, generator=g) * 0.1).to(torch.bfloat16)   # keeps ys in fp16 range
+    wcap = torch.zeros(cap)
+    wcap[:A] = torch.rand(A, generator=g)
+    _, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], W2)
+    W2q, sW2 = B.moe_quantize_rows_fp8(W2p)
+    ys = B.moe_expert_down_fp8(s, hcap.to(cuda_device), W2q, sW2,
+                               torch.from_numpy(counts.astype(np.int32)).to(cuda_device),
+                               torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), wcap.to(cuda_device), ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    hh = O.dequantized_rows_e4m3(hcap[:A].float().numpy())
+    ref = np.zeros((A, d))
+    exact = np.zeros((A, d))
+    for e in range(E):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 > r0:
+            wr = wcap[r0:r1].double().numpy()[:, None]
+            ref[r0:r1] = wr * (hh[r0:r1] @ O.quantized_expert_down_weight(W2[e]))
+            exact[r0:r1] = wr * (hh[r0:r1] @ to64(W2[e]))
+    got = to64(ys[:A])
+    mag = np.abs(ref)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -11 * mag + 1e-5 * np.sqrt(np.mean(ref ** 2, axis=0))[None, :])
+    # the ordinary channels stay close to the unquantised weights
+    others = np.setdiff1d(np.arange(d), [17, 200])
+    rel = np.abs(got[:, others] - exact[:, others]).sum() / np.abs(exact[:, others]).sum()
+    assert rel < 0.1, rel
+
+
 def _forward_fp8_and_check(cfg, dev, seed=0, tokens=None):
     inp = I.make_inputs(cfg, device=dev, seed=seed)
     s = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k)
     ws = B.Workspace(s, dev, fp8=True)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     W13q, sW13 = B.moe_quantize_rows_fp8(W13p)
-    W2q, sW2 = B.moe_quantize_experts_fp8(W2p)
+    W2q, sW2 = B.moe_quantize_rows_fp8(W2p)
     del W13p, W2p
     y = B.moe_forward_fp8(s, inp["x"], inp["Wr"], inp["bias"], W13q, sW13, W2q, sW2, ws)
     assert B.moe_check_device_status(ws) == B.MOE_OK
