@@ -73,3 +73,33 @@ def assert_grad_close(g, g_ref, mag, what="grad"):
     assert np.all(excess <= 1e-6 * s["rms"] + 1e-30), f"{what}: {s}, worst excess {excess.max():.3e}"
     assert s["mean_rel"] <= MEAN_REL, f"{what}: {s}"
     return s
+
+
+def stratified_tokens(offsets, row_token, T, seed, minimum=1024, cap_loaded=2048, per_expert=2, block=128):
+    """Token sample that reaches every expert's GEMM tiles: for each expert
+    with rows, the token of its first row, of its last row and of a random row
+    in its last `block`-row block, plus `per_expert` random rows; every token
+    of the least- and the most-loaded expert (at most `cap_loaded` of each,
+    drawn at random beyond that); then random tokens up to `minimum`.
+    offsets [E+1] and row_token [R] are the permutation's arrays (rows of an
+    expert contiguous).  Returns sorted unique token ids."""
+    rng = np.random.default_rng(seed)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    row_token = np.asarray(row_token, dtype=np.int64)
+    counts = np.diff(offsets)
+    toks = set()
+    for e in np.flatnonzero(counts > 0):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        last_lo = lo + ((hi - lo - 1) // block) * block
+        toks.update(int(row_token[r]) for r in (lo, hi - 1, int(rng.integers(last_lo, hi))))
+        toks.update(int(row_token[r]) for r in rng.integers(lo, hi, size=per_expert))
+    nz = np.flatnonzero(counts > 0)
+    for e in {int(nz[np.argmin(counts[nz])]), int(np.argmax(counts))}:
+        rows = row_token[offsets[e]:offsets[e + 1]]
+        if rows.size > cap_loaded:
+            rows = rng.choice(rows, size=cap_loaded, replace=False)
+        toks.update(int(t) for t in rows)
+    if len(toks) < min(minimum, T):
+        rest = np.setdiff1d(np.arange(T), np.fromiter(toks, dtype=np.int64))
+        toks.update(int(t) for t in rng.choice(rest, size=min(minimum, T) - len(toks), replace=False))
+    return np.array(sorted(toks), dtype=np.int64)

@@ -20,7 +20,7 @@ from mixture_experts_layer_93_b300 import binding as B
 from mixture_experts_layer_93_b300 import inputs as I
 from oracle import moe_oracle as O
 
-from moe_testlib import assert_grad_close, assert_moe_close, to64
+from moe_testlib import assert_grad_close, assert_moe_close, stratified_tokens, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -157,14 +157,11 @@ def test_backward_tiny_config(cuda_device):
     assert np.all(np.abs(dWr.sum(axis=1)) <= 1e-4 * np.abs(dWr).max() * cfg.E)
 
 
-def _sampled_reference(inp, dy, logits, k, e, J, toks):
-    """fp64 gradients the oracle's formulas give for expert e's channels J
-    (dW1[e][:, J], dW3[e][:, J], dW2[e][J, :]) and for the tokens `toks`
-    (dx), with their magnitudes; selection and gate weights from the fp32
-    logits, as moe_backward (oracle) takes them."""
-    L = logits.astype(np.float64)
-    idx = O.topk(L, k)
-    w = O.gate_weights(L, idx)
+def _channel_reference(inp, dy, L, idx, w, e, J):
+    """fp64 weight gradients the oracle's formulas give for expert e's
+    channels J (dW1[e][:, J], dW3[e][:, J], dW2[e][J, :]) with their
+    magnitudes; selection idx and gate weights w from the fp32 logits, as
+    moe_backward (oracle) takes them."""
     x64 = to64(inp["x"])
     dy64 = to64(dy)
     rows = np.argwhere(idx == e)               # (t, j) pairs routed to e, in token order
@@ -179,59 +176,73 @@ def _sampled_reference(inp, dy, logits, k, e, J, toks):
     h = a * u
     dh = we[:, None] * (dy64[ts] @ W2J.T)
     dg, du = dh * u * (s * (1 + g * (1 - s))), dh * a
-    out = {"dW1": X.T @ dg, "dW3": X.T @ du, "dW2": (we[:, None] * h).T @ dy64[ts],
-           "dW1_mag": np.abs(X).T @ np.abs(dg), "dW3_mag": np.abs(X).T @ np.abs(du),
-           "dW2_mag": np.abs(we[:, None] * h).T @ np.abs(dy64[ts])}
-    # dx of sampled tokens: every selected expert in full, plus the gate network
-    Wr = to64(inp["Wr"])
+    return {"dW1": X.T @ dg, "dW3": X.T @ du, "dW2": (we[:, None] * h).T @ dy64[ts],
+            "dW1_mag": np.abs(X).T @ np.abs(dg), "dW3_mag": np.abs(X).T @ np.abs(du),
+            "dW2_mag": np.abs(we[:, None] * h).T @ np.abs(dy64[ts])}
+
+
+def _dx_reference(inp, dy, idx, w, toks):
+    """fp64 dx of the tokens `toks` with magnitudes: every selected expert's
+    path in full plus the gate network's term, worked expert by expert so each
+    expert's weights are widened once."""
+    x64, dy64, Wr = to64(inp["x"]), to64(dy), to64(inp["Wr"])
+    k = idx.shape[1]
+    sel = idx[toks]                             # [S, k]
     dx = np.zeros((len(toks), x64.shape[1]))
     mag = np.zeros_like(dx)
-    cache = {}
-    for i, t in enumerate(toks):
-        dws = []
-        for j in range(k):
-            ej = int(idx[t, j])
-            if ej not in cache:
-                if len(cache) >= 4:  # bound the host memory of widened weights
-                    cache.clear()
-                cache[ej] = (to64(inp["W1"][ej]), to64(inp["W3"][ej]), to64(inp["W2"][ej]))
-            W1e, W3e, W2e = cache[ej]
-            gt, ut = x64[t] @ W1e, x64[t] @ W3e
-            st = O.sigmoid(gt)
-            at = gt * st
-            dhu = dy64[t] @ W2e.T
-            dws.append(float(dhu @ (at * ut)))
-            dgt, dut = w[t, j] * dhu * ut * (st * (1 + gt * (1 - st))), w[t, j] * dhu * at
-            dx[i] += W1e @ dgt + W3e @ dut
-            mag[i] += np.abs(W1e) @ np.abs(dgt) + np.abs(W3e) @ np.abs(dut)
-        dws = np.array(dws)
-        dl = w[t] * (dws - np.dot(w[t], dws))
-        dx[i] += Wr[:, idx[t]] @ dl
-        mag[i] += np.abs(Wr[:, idx[t]]) @ np.abs(dl)
-    out.update(dx=dx, dx_mag=mag)
-    return out
+    dws = np.zeros(sel.shape)
+    for e in np.unique(sel):
+        ii, jj = np.nonzero(sel == e)
+        ts = toks[ii]
+        W1e, W3e, W2e = to64(inp["W1"][int(e)]), to64(inp["W3"][int(e)]), to64(inp["W2"][int(e)])
+        X = x64[ts]
+        g, u = X @ W1e, X @ W3e
+        st = O.sigmoid(g)
+        a = g * st
+        dhu = dy64[ts] @ W2e.T
+        dws[ii, jj] = np.sum(dhu * a * u, axis=1)
+        wt = w[ts, jj][:, None]
+        dg, du = wt * dhu * u * (st * (1 + g * (1 - st))), wt * dhu * a
+        np.add.at(dx, ii, dg @ W1e.T + du @ W3e.T)
+        np.add.at(mag, ii, np.abs(dg) @ np.abs(W1e).T + np.abs(du) @ np.abs(W3e).T)
+    wt = w[toks]
+    dl = wt * (dws - np.sum(wt * dws, axis=1, keepdims=True))
+    for i in range(len(toks)):
+        dx[i] += Wr[:, sel[i]] @ dl[i]
+        mag[i] += np.abs(Wr[:, sel[i]]) @ np.abs(dl[i])
+    return dx, mag
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "dsv3", "b7", "skew"])
 def test_backward_full_size_sampled(cuda_device, name):
-    """The full-size layers in the bench's launch configuration: sampled
-    weight-gradient channels of two experts and sampled tokens' dx against
-    the oracle's formulas; dWr and dbias by the zero sum over experts."""
+    """The full-size layers in the bench's launch configuration: dx of an
+    expert-stratified token sample (every expert's first row, last 128-row
+    block and a random row; all tokens of the least- and most-loaded expert;
+    at least 1024 tokens) and the weight-gradient channels of several experts
+    (the least- and most-loaded ones among them) against the oracle's
+    formulas; dWr and dbias by the zero sum over experts."""
     cfg = I.get_config(name)
     inp, dy, s, W13p, W13i = _setup(cfg, cuda_device, seed=0)
     out, logits = _run(inp, dy, s, W13p, W13i, cuda_device)
-    logits = logits.cpu().numpy()
+    L = logits.cpu().numpy().astype(np.float64)
+    idx = O.topk(L, cfg.k)
+    w = O.gate_weights(L, idx)
+    counts, offsets, src, _ = O.permute(idx, cfg.E)
+    toks = stratified_tokens(offsets, src // cfg.k, cfg.T, seed=1, per_expert=1)
+    dx_ref, dx_mag = _dx_reference(inp, dy, idx, w, toks)
+    assert_grad_close(out["dx"][torch.from_numpy(toks).to(cuda_device)], dx_ref, dx_mag, what="dx")
     rng = np.random.default_rng(1)
-    toks = np.sort(rng.choice(cfg.T, size=6, replace=False))
-    for e in rng.choice(cfg.E, size=2, replace=False):
-        J = np.sort(rng.choice(cfg.n, size=6, replace=False))
-        ref = _sampled_reference(inp, dy, logits, cfg.k, int(e), J, toks)
+    nz = np.flatnonzero(counts > 0)
+    experts = {int(nz[np.argmin(counts[nz])]), int(np.argmax(counts))}
+    experts.update(int(e) for e in rng.choice(cfg.E, size=min(4, cfg.E), replace=False))
+    for e in sorted(experts):
+        J = np.sort(rng.choice(cfg.n, size=8, replace=False))
+        ref = _channel_reference(inp, dy, L, idx, w, e, J)
         Jt = torch.from_numpy(J).to(cuda_device)
         assert_grad_close(out["dW1"][e][:, Jt], ref["dW1"], ref["dW1_mag"], what=f"dW1[{e}]")
         assert_grad_close(out["dW3"][e][:, Jt], ref["dW3"], ref["dW3_mag"], what=f"dW3[{e}]")
         assert_grad_close(out["dW2"][e][Jt, :], ref["dW2"], ref["dW2_mag"], what=f"dW2[{e}]")
-    assert_grad_close(out["dx"][torch.from_numpy(toks).to(cuda_device)], ref["dx"], ref["dx_mag"], what="dx")
     dWr = to64(out["dWr"])
     assert np.all(np.abs(dWr.sum(axis=1)) <= 1e-4 * np.sqrt(np.mean(dWr ** 2)) * cfg.E)
     db = to64(out["dbias"])

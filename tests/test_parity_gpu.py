@@ -10,7 +10,7 @@ import torch
 from mixture_experts_layer_93_b300 import binding as B
 from mixture_experts_layer_93_b300 import inputs as I
 from oracle import moe_oracle as O
-from tests.moe_testlib import assert_moe_close, err_stats, robust_tokens, to64, valid_topk
+from tests.moe_testlib import assert_moe_close, err_stats, robust_tokens, stratified_tokens, to64, valid_topk
 
 pytestmark = pytest.mark.gpu
 
@@ -456,26 +456,56 @@ def test_device_timeout_is_reported_and_context_survives(cuda_device):
 
 
 # ----------------------------------------------- full-size configurations
-# sampled tokens per configuration: bounded by the expert weights the fp64
-# oracle has to widen (every expert a sampled token uses)
-SAMPLE = {"mixtral": 48, "dsv3": 16, "b7": 64, "skew": 32}
-
-
-def _sample_tokens(T, size, seed):
-    rng = np.random.default_rng(seed)
-    return np.sort(rng.choice(T, size=min(size, T), replace=False))
+def _gpu_routing(ws, T, E, k):
+    """The GPU's fp32 logits and permutation arrays, from the workspace."""
+    cap = T * k
+    L = ws.view("logits", torch.float32, T * E).view(T, E).cpu().numpy()
+    idx = ws.view("topk_idx", torch.int32, T * k).view(T, k).cpu().numpy()
+    counts = ws.view("counts", torch.int32, E).cpu().numpy()
+    offsets = ws.view("offsets", torch.int32, E + 1).cpu().numpy()
+    row_token = ws.view("row_token", torch.int32, cap).cpu().numpy()
+    dst = ws.view("dst", torch.int32, T * k).cpu().numpy()
+    return L, idx, counts, offsets, row_token, dst
 
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixtral", "dsv3", "b7", "skew"])
 def test_forward_full_size_sampled(cuda_device, name):
+    """The full-size layer in the launch configuration the benchmark times.
+    Integer work is checked whole: the top-k of the GPU's fp32 logits and the
+    permutation of all T*k assignments equal the oracle's on those logits.
+    The logits of a token sample meet the fp32 bound against the fp64 gate
+    network, and the outputs of an expert-stratified sample (every expert's
+    first row, last 128-row block and random rows; all tokens of the least-
+    and most-loaded expert; at least 1024 tokens) meet the layer tolerance
+    against the oracle routed on the same fp32 logits."""
     cfg = I.get_config(name)
     inp = I.make_inputs(cfg, device=cuda_device, seed=0)
     layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k)
-    toks = _sample_tokens(cfg.T, SAMPLE[name], 1)
-    stats, frac, y = _forward_and_check(cfg, cuda_device, tokens=toks, layer=layer, inp=inp)
-    assert frac > 0.9
-    # every token's output is finite and the whole batch is deterministic
+    y = layer.forward(inp["x"])
+    ws = layer.workspace(cfg.T, cuda_device)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    T, E, k = cfg.T, cfg.E, cfg.k
+    L, idx, counts, offsets, row_token, dst = _gpu_routing(ws, T, E, k)
+    # selection and permutation, every token, bit-exact given the fp32 logits
+    assert np.array_equal(idx, O.topk(L, k))
+    c_ref, o_ref, src_ref, dst_ref = O.permute(idx, E)
+    assert np.array_equal(counts, c_ref) and np.array_equal(offsets, o_ref)
+    assert np.array_equal(row_token[:T * k], src_ref // k) and np.array_equal(dst, dst_ref)
+    toks = stratified_tokens(offsets, row_token[:T * k], T, seed=1)
+    assert len(toks) >= min(1024, T)
+    assert set(np.unique(idx[toks])) == set(np.flatnonzero(counts > 0))   # every expert with rows is reached
+    # the gate network on a sample of tokens, against fp64
+    lt = toks[:: max(1, len(toks) // 256)]
+    L64 = O.router_logits(inp["x"][torch.from_numpy(lt).to(cuda_device)], inp["Wr"], inp["bias"])
+    absdot = np.abs(to64(inp["x"][torch.from_numpy(lt).to(cuda_device)])) @ np.abs(to64(inp["Wr"]))
+    err = np.abs(L[lt].astype(np.float64) - L64)
+    assert np.all(err <= (3 * cfg.d + 3) * 2.0 ** -23 * (absdot + np.abs(L64)) + 1e-30)
+    # outputs, the oracle routed on the GPU's fp32 logits
+    routing = O.route(None, None, None, k, logits=L, tokens=toks)
+    y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k,
+                          routing=routing)
+    assert_moe_close(y[torch.from_numpy(toks).to(cuda_device)], y_ref)
     assert torch.isfinite(y.float()).all()
     y2 = layer.forward(inp["x"])
     assert torch.equal(y, y2)
@@ -554,6 +584,8 @@ def _gpu_sets(ws, shape, T):
                                                  (700, 128, 192, 12, 3, 64, "up"),
                                                  (1200, 256, 128, 16, 4, 64, "stochastic")])
 def test_forward_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
+    """Rounded layer: given the GPU's fp32 logits, every token's final expert
+    set equals the oracle's, and the outputs meet the layer tolerance."""
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="zipf", bias_scale=1.1)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T)
     layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile, round=mode, seed=77)
@@ -563,16 +595,14 @@ def test_forward_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
     gsets = _gpu_sets(ws, layer.shape(T), T)
     counts = ws.view("counts", torch.int32, E).cpu().numpy()
     assert np.all(counts % tile == 0)
-    toks, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], k, tile=tile, mode=mode, seed=77)
-    same = np.array([np.array_equal(a, b) for a, b in zip(gsets, osets)])
-    # fp32 logits on the GPU vs fp64 ones in the oracle can flip a selection
-    # only at a near-tie between two tokens' logits
-    assert same.mean() > 0.97, same.mean()
-    keep = np.flatnonzero(same)
+    L = ws.view("logits", torch.float32, T * E).view(T, E).cpu().numpy()
+    routing = O.route(None, None, None, k, tile=tile, mode=mode, logits=L, seed=77)
+    for t in range(T):
+        assert np.array_equal(gsets[t], routing[1][t]), t
     y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=k, tile=tile,
-                          mode=mode, tokens=keep, seed=77)
-    assert_moe_close(y[torch.from_numpy(keep).to(cuda_device)], y_ref)
-    empty = [t for t in keep if len(osets[t]) == 0]
+                          mode=mode, routing=routing)
+    assert_moe_close(y, y_ref)
+    empty = [t for t in range(T) if len(routing[1][t]) == 0]
     if empty:
         assert torch.all(y[torch.tensor(empty, device=cuda_device)] == 0)
 
@@ -581,9 +611,9 @@ def test_forward_token_rounding(cuda_device, T, d, n, E, k, tile, mode):
 @pytest.mark.parametrize("mode", ["nearest", "stochastic"])
 def test_forward_full_size_skew_rounding(cuda_device, mode):
     """The skewed-load layer at full size with tile-128 token rounding: every
-    rounded count is a tile multiple, the GPU's final expert sets match the
-    oracle's on sampled tokens (except near-ties of fp32 vs fp64 logits), and
-    those tokens' outputs meet the tolerance."""
+    rounded count is a tile multiple, the GPU's final expert set of every
+    token equals the oracle's rounding of the same fp32 logits, and the
+    outputs of an expert-stratified token sample meet the tolerance."""
     cfg = I.get_config("skew")
     inp = I.make_inputs(cfg, device=cuda_device, seed=0)
     layer = B.MoELayer(inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k, tile=128, round=mode,
@@ -591,16 +621,21 @@ def test_forward_full_size_skew_rounding(cuda_device, mode):
     y = layer.forward(inp["x"])
     ws = layer.workspace(cfg.T, cuda_device)
     assert B.moe_check_device_status(ws) == B.MOE_OK
-    counts = ws.view("counts", torch.int32, cfg.E).cpu().numpy()
+    T, E = cfg.T, cfg.E
+    counts = ws.view("counts", torch.int32, E).cpu().numpy()
     assert np.all(counts % 128 == 0)
-    toks = _sample_tokens(cfg.T, 32, 3)
-    gsets = _gpu_sets(ws, layer.shape(cfg.T), cfg.T)
-    _, osets, _ = O.route(inp["x"], inp["Wr"], inp["bias"], cfg.k, tile=128, mode=mode, tokens=toks, seed=5)
-    same = np.array([np.array_equal(gsets[t], s) for t, s in zip(toks, osets)])
-    assert same.mean() >= 0.9, same.mean()
-    keep = toks[same]
+    gsets = _gpu_sets(ws, layer.shape(T), T)
+    L = ws.view("logits", torch.float32, T * E).view(T, E).cpu().numpy()
+    full = O.route(None, None, None, cfg.k, tile=128, mode=mode, logits=L, seed=5)
+    for t in range(T):
+        assert np.array_equal(gsets[t], full[1][t]), t
+    cap = B.moe_row_capacity(layer.shape(T))
+    offsets = ws.view("offsets", torch.int32, E + 1).cpu().numpy()
+    row_token = ws.view("row_token", torch.int32, cap).cpu().numpy()[:offsets[-1]]
+    toks = stratified_tokens(offsets, row_token, T, seed=3)
+    routing = (toks, [full[1][t] for t in toks], [full[2][t] for t in toks])
     y_ref = O.moe_forward(inp["x"], inp["Wr"], inp["bias"], inp["W1"], inp["W3"], inp["W2"], k=cfg.k, tile=128,
-                          mode=mode, tokens=keep, seed=5)
-    assert_moe_close(y[torch.from_numpy(keep).to(cuda_device)], y_ref)
+                          mode=mode, routing=routing)
+    assert_moe_close(y[torch.from_numpy(toks).to(cuda_device)], y_ref)
     del layer, inp
     torch.cuda.empty_cache()
