@@ -203,9 +203,11 @@ def test_expert_up_swiglu(cuda_device, gather, T, d, n, E, k, skew):
 
 
 # Per-expert counts whose last 128-row block takes sizes across 1..128 rows,
-# with odd and even block counts.  Plus 0 they take the separate odd-block
-# launch; plus 1024 each (same remainders) the host runs odd blocks as
-# half-empty SM pairs.
+# with odd and even block counts.  Plus 0 (about 200 rows per expert) the SM
+# pairs run super tiles and the odd last blocks the separate single-SM launch;
+# plus 800 (about 1000 rows per expert) super tiles with the odd last block in
+# the last unit; plus 1024 plain pair tiles with odd blocks as half-empty
+# pairs.
 ODD_COUNTS = [1, 31, 32, 33, 64, 95, 97, 128, 129, 160, 255, 256, 257, 300, 383, 384, 0, 450]
 
 
@@ -220,7 +222,7 @@ def _routing_with_counts(counts, seed):
     return idx, c, offsets, src, dst
 
 
-@pytest.mark.parametrize("extra", [0, 1024])
+@pytest.mark.parametrize("extra", [0, 800, 1024])
 def test_expert_up_odd_tails(cuda_device, extra):
     """Up GEMM on SM pairs (n % 128 == 0) with odd last blocks of every size:
     h within one bf16 rounding."""
@@ -247,7 +249,7 @@ def test_expert_up_odd_tails(cuda_device, extra):
     assert np.all(np.abs(h_gpu - h_ref) <= 2.0 ** -8 * np.abs(h_ref) + 1e-5 * rms), err_stats(h_gpu, h_ref)
 
 
-@pytest.mark.parametrize("extra", [0, 1024])
+@pytest.mark.parametrize("extra", [0, 800, 1024])
 def test_expert_down_odd_tails(cuda_device, extra):
     """Down GEMM on SM pairs (d % 256 == 0) with odd last blocks of every
     size: ys within one fp16 rounding, gate weight applied per row."""
