@@ -50,12 +50,14 @@ METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 METRIC_BWD = "MoE bwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one up-projection
-# launch, from an ncu capture of the current kernel on the full workload, keyed
-# by workload, A path and kernel revision; a kernel change bumps GEMM_REV and
-# drops stale entries.
-GEMM_REV = "cta-pair-pdl-fp8-bwd-router-topk-v11"
-UP_TRAFFIC = {("mixtral", 0, GEMM_REV): 3508259925}  # mean of three launches
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# up-projection's main GEMM kernel, from an ncu capture of the current kernel,
+# keyed by workload, A path and kernel revision; a kernel change bumps GEMM_REV
+# and drops stale entries.  DeepSeek-V3-style layer: captured on the same layer
+# with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.212 GB,
+# scaled by the experts processed (x8).
+GEMM_REV = "super-tiles-v12"
+UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2212011776}
 
 
 def load_peaks():
@@ -709,7 +711,8 @@ def run_ours(args, world, rank, local):
                 "achieved": up_tflops, "peak": up_peak, "unit": "TFLOP/s", "frac": up_tflops / up_peak,
                 "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV))
                 if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) and not args.fp8 else None,
-                "traffic_unit": "bytes per launch (ncu dram read+write)",
+                "traffic_unit": "bytes per launch of the main up GEMM kernel (ncu dram read+write)",
+                "algorithmic_bytes_per_launch": 2.0 * E * 2 * n * d + R * d * 2.0 + R * n * 2.0,
                 "peak_source": f"{peak_src} {up_peak_kind}",
                 "frac_of_sustained": up_tflops / (sustained * up_peak / peak_t),
                 "algorithmic_flops_per_launch": up_flops}
