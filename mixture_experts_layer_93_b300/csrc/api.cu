@@ -1,5 +1,6 @@
 // C ABI of libmoe.so: argument validation, workspace layout and the stage
 // sequence of the MoE-layer forward.  Every declaration is in include/moe.h.
+#include <algorithm>
 #include <cstring>
 
 #include "common.cuh"
@@ -47,7 +48,8 @@ int64_t layout(const moe_shape* s, int64_t* off, bool fp8 = false) {
       A * 4,              cap * 4,   cap * 4,   (T + 1) * 4, cap * 4,       cap * s->n * 2,
       cap * s->d * 2,     E * perm_num_chunks(cap) * 4,
       s->round != MOE_ROUND_OFF ? static_cast<int64_t>(round_scratch_bytes(s->T, s->E, s->k, s->tile)) : 0,
-      static_cast<int64_t>(router_split_elems(s->d, s->E)) * 2,
+      std::max<int64_t>(static_cast<int64_t>(router_split_elems(s->d, s->E)) * 2,
+                        router_is_small(s->d, s->E) ? static_cast<int64_t>(router_small_wp_bytes(s->d, s->E)) : 0),
       fp8 ? align256(cap * s->n) + cap * 4 : 0};
   int64_t pos = static_cast<int64_t>(kStatusBytes);
   for (int i = 0; i < kNumSlots; ++i) {
@@ -182,6 +184,13 @@ int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const 
   if (!shape_ok(s) || !x || !Wr || !logits || !ws || !aligned16(x) || !aligned16(ws)) return MOE_ERR_INVALID;
   int64_t off[kNumSlots];
   layout(s, off);
+  if (router_is_small(s->d, s->E)) {  // few experts: SIMT, bound by reading x
+    float* Wp = at<float>(ws, off[kRouterW]);
+    launch_router_small_prep(Wr, s->d, s->E, Wp, nullptr, 0, as_stream(stream));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_router_small(static_cast<const __nv_bfloat16*>(x), Wp, bias, logits, s->T, s->d, s->E, 0, nullptr,
+                               nullptr, nullptr, status_of(ws), kDefaultTimeoutNs, as_stream(stream));
+  }
   __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
   launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream));
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
@@ -216,9 +225,24 @@ int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const 
   layout(s, off);
   __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
   int32_t* chunk_hist = at<int32_t>(ws, off[kPermHist]);
+  const int64_t hist_count = static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k);
+  if (router_is_small(s->d, s->E) && s->k <= kFusedTopk) {
+    // few experts: the weight layout (and zeroed chunk counts), the SIMT
+    // router with the top-k and the chunk counts, then the scan and the
+    // scatter (4 launches)
+    float* Wp = at<float>(ws, off[kRouterW]);
+    launch_router_small_prep(Wr, s->d, s->E, Wp, chunk_hist, hist_count, as_stream(stream));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    const int rst = launch_router_small(static_cast<const __nv_bfloat16*>(x), Wp, bias, logits, s->T, s->d, s->E, s->k,
+                                        topk_idx, topk_w, chunk_hist, status_of(ws), kDefaultTimeoutNs,
+                                        as_stream(stream));
+    if (rst != MOE_OK) return rst;
+    launch_perm_scan_scatter(topk_idx, topk_w, static_cast<int64_t>(s->T) * s->k, s->k, s->E, chunk_hist, counts,
+                             offsets, src, dst, row_token, row_w, as_stream(stream));
+    return last_launch();
+  }
   const bool fused = s->E <= 256;  // the fused top-k + histogram kernel (counts start at zero)
-  launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), fused ? chunk_hist : nullptr,
-                      fused ? static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k) : 0);
+  launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), fused ? chunk_hist : nullptr, fused ? hist_count : 0);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   if (router_fuses_topk(s->E, s->k)) {
     // top-k and chunk counts in the router GEMM's epilogue

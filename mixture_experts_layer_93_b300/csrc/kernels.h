@@ -98,6 +98,21 @@ void launch_split_router(const float* Wr, __nv_bfloat16* Wr3, int d, int E, cuda
 // top-k + histogram kernel does; an SM pair then runs all n-blocks (64
 // experts each) of one row block in a row.
 constexpr int kFusedTopk = 8;
+// Router for few experts on the SIMT cores (route.cu): E <= 16 and Wr (fp32)
+// with the kernel's x staging fits in shared memory.  launch_router_small_prep
+// lays Wr out for it in Wp (router_small_wp_bytes, 16-byte aligned) and zeroes
+// zero[0, zero_count); launch_router_small then computes the logits and, with
+// k > 0, the top-k, gate weights and chunk counts (chunk_hist zero on entry),
+// as launch_router_tc does.  x must be 16-byte aligned.
+constexpr int kRouterSmallSmemMax = 227 * 1024 - 64;  // the per-block limit, less its static barrier
+constexpr int kRouterSmallStages = 3;             // x steps per warp in its ring
+bool router_is_small(int d, int E);
+size_t router_small_wp_bytes(int d, int E);
+void launch_router_small_prep(const float* Wr, int d, int E, float* Wp, int32_t* zero, int64_t zero_count,
+                              cudaStream_t stream);
+int launch_router_small(const __nv_bfloat16* x, const float* Wp, const float* bias, float* logits, int T, int d, int E,
+                        int k, int32_t* topk_idx, float* topk_w, int32_t* chunk_hist, int32_t* status,
+                        uint64_t timeout_ns, cudaStream_t stream);
 inline bool router_fuses_topk(int E, int k) { return E <= 256 && k <= kFusedTopk; }
 int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const float* bias, float* logits, int T,
                      int d, int E, int32_t* status, uint64_t timeout_ns, cudaStream_t stream, int k = 0,

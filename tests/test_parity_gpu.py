@@ -23,8 +23,15 @@ def ws_for(T, d, n, E, k, dev, tile=128, round="off"):
 
 
 # ------------------------------------------------------------------ router
+# E <= 16 runs the SIMT router while Wr (fp32) and its x staging fit in
+# shared memory (d <= 4160 at E <= 8, d <= 2816 at E <= 16), larger shapes
+# the tensor-core one: both sides of both limits, E not a multiple of 8,
+# token counts that leave a partial warp task
 @pytest.mark.parametrize("T,d,E,bias", [(256, 128, 8, False), (1000, 512, 40, True), (300, 1024, 256, True),
-                                        (77, 64, 1, False), (130, 256, 1024, False)])
+                                        (77, 64, 1, False), (130, 256, 1024, False), (1, 64, 16, True),
+                                        (99, 192, 5, True), (517, 1536, 12, True), (258, 2816, 16, False),
+                                        (333, 4096, 8, True), (130, 4160, 8, False), (64, 4224, 8, True),
+                                        (70, 2880, 16, False), (45, 3200, 3, True)])
 def test_router_logits(cuda_device, T, d, E, bias):
     cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=1, bias="normal" if bias else None, bias_scale=0.5)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T + E, weights=False)
@@ -32,12 +39,35 @@ def test_router_logits(cuda_device, T, d, E, bias):
     L = B.moe_router_logits(inp["x"], inp["Wr"], inp["bias"], ws)
     assert B.moe_check_device_status(ws) == B.MOE_OK
     torch.cuda.synchronize()
-    L64 = O.router_logits(inp["x"], inp["Wr"], inp["bias"])
+    _assert_logits_bound(L, inp["x"], inp["Wr"], inp["bias"], d)
+
+
+def test_router_logits_unaligned_wr(cuda_device):
+    """A Wr that does not start on 16 bytes (fp32 alignment only), under the
+    same bound."""
+    T, d, E = 200, 256, 8
+    cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=1, bias="normal", bias_scale=0.5)
+    inp = I.make_inputs(cfg, device=cuda_device, seed=5, weights=False)
+    buf = torch.empty(d * E + 1, dtype=torch.float32, device=cuda_device)
+    Wr = buf[1:].view(d, E)
+    Wr.copy_(inp["Wr"])
+    assert Wr.data_ptr() % 16 != 0
+    s, ws = ws_for(T, d, 64, E, 1, cuda_device)
+    L = B.moe_router_logits(inp["x"], Wr, inp["bias"], ws)
+    assert B.moe_check_device_status(ws) == B.MOE_OK
+    torch.cuda.synchronize()
+    _assert_logits_bound(L, inp["x"], inp["Wr"], inp["bias"], d)
+
+
+def _assert_logits_bound(L, x, Wr, bias, d):
+    L64 = O.router_logits(x, Wr, bias)
     err = np.abs(to64(L) - L64)
     # rigorous bound for an fp32-accumulated dot product of 3d exact terms
-    # (hi/mid/lo split, each product exact), rounding toward zero allowed:
-    # (3d + 3) * 2^-23 * sum_i |x_i w_ie|, plus the split residue 2^-27
-    absdot = np.abs(to64(inp["x"])) @ np.abs(to64(inp["Wr"]))
+    # (the tensor-core router: hi/mid/lo split of Wr, each product exact),
+    # rounding toward zero allowed: (3d + 3) * 2^-23 * sum_i |x_i w_ie|, plus
+    # the split residue 2^-27.  The SIMT router (d fused multiply-adds in
+    # chains of d/32, then a 32-way butterfly) stays far inside it.
+    absdot = np.abs(to64(x)) @ np.abs(to64(Wr))
     assert np.all(err <= (3 * d + 3) * 2.0 ** -23 * (absdot + np.abs(L64)) + 1e-30)
     rms = float(np.sqrt(np.mean(L64 ** 2)))
     assert err.max() <= 5e-5 * rms, (err.max(), rms)
@@ -89,6 +119,8 @@ def test_permute_bit_exact(cuda_device, T, E, k, skew):
 
 # ------------------------------------------------------- fused route+permute
 @pytest.mark.parametrize("T,d,E,k,bias", [(1, 128, 1, 1, False), (777, 256, 8, 2, True), (1500, 128, 40, 3, False),
+                                          (999, 1024, 12, 4, True), (2049, 2816, 16, 8, False),
+                                          (513, 4096, 8, 2, True), (301, 4224, 8, 2, False),
                                           (5000, 256, 128, 8, False), (3001, 128, 256, 5, True),
                                           (700, 128, 256, 6, False), (333, 128, 300, 7, True),
                                           (4096, 128, 64, 1, False), (600, 128, 64, 12, False),
