@@ -126,10 +126,17 @@ int moe_prepare_weights(const moe_shape* s, const void* W1, const void* W3, cons
 
 /* Router logits (gate network; "MoE架构的物理瓶颈与扩展限制解析", 工作原理 step 1):
  *   logits[T, E] fp32 = float(x[T, d] bf16) @ Wr[d, E] fp32 + bias[E] fp32.
- * bias may be NULL.  Runs on the tensor cores: Wr is split into three bf16
- * terms hi + mid + lo (equal to Wr within 2^-27 relative; the split is kept
- * in the workspace, which must hold moe_workspace_bytes(s) bytes), each
- * product with the bf16 x is exact and accumulates in fp32. */
+ * bias may be NULL.  The workspace must hold moe_workspace_bytes(s) bytes.
+ * With E > 16 (or Wr too large for shared memory) it runs on the tensor
+ * cores: Wr is split into three bf16 terms hi + mid + lo (equal to Wr within
+ * 2^-27 relative; the split is kept in the workspace), each product with the
+ * bf16 x is exact and accumulates in fp32.  With E <= 16 and
+ * ((E + 1) & ~1) * d * 4 bytes plus the x staging within an SM's shared
+ * memory (d <= 4160 for E <= 8, d <= 2816 for E <= 16) it runs on the SIMT
+ * cores: one fp32 fused multiply-add per product, in a fixed order (a copy of
+ * Wr laid out by expert pairs is kept in the workspace).  Either way every
+ * call gives the same bits for the same inputs, and moe_route_permute and
+ * moe_forward use the same router. */
 int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                       float* logits, void* ws, void* stream);
 
