@@ -49,6 +49,8 @@ from mixture_experts_layer_93_b300 import inputs as I  # noqa: E402
 METRIC = "MoE fwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 METRIC_BWD = "MoE bwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+# streams (and buffer sets) the forward e2e loop rotates over
+E2E_STREAMS = 3
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # up-projection's main GEMM kernel, from an ncu capture of the current kernel,
@@ -643,21 +645,23 @@ def run_ours(args, world, rank, local):
 
     # ------------------------------------------------ e2e: through moe_forward, host buffers
     # Each step copies its x from pinned host memory, runs moe_forward and
-    # copies its y back.  Steps alternate between two streams (each with its
-    # own buffers and workspace), so one step's copies overlap the other's
-    # compute, as a serving loop would run them.
+    # copies its y back.  Steps rotate over E2E_STREAMS streams (each with its
+    # own buffers and workspace), as a serving loop would run them: the next
+    # step's input copy and the previous step's output copy (separate copy
+    # engines) overlap this step's compute.  With two streams, step i + 2
+    # could not copy its input in before step i's output copy had finished.
     x_cpu = x.cpu()
-    streams = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
-    wss = [ws, B.Workspace(shape, dev, fp8=args.fp8)]
-    x_host = [torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
-    y_host = [torch.empty(T, d, dtype=torch.float32, pin_memory=True) for _ in range(2)]
+    streams = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
+    wss = [ws] + [B.Workspace(shape, dev, fp8=args.fp8) for _ in range(E2E_STREAMS - 1)]
+    x_host = [torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(E2E_STREAMS)]
+    y_host = [torch.empty(T, d, dtype=torch.float32, pin_memory=True) for _ in range(E2E_STREAMS)]
     for xh in x_host:
         xh.copy_(x_cpu)
-    x_dev = [torch.empty_like(x) for _ in range(2)]
-    y_dev = [torch.empty_like(y) for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(E2E_STREAMS)]
+    y_dev = [torch.empty_like(y) for _ in range(E2E_STREAMS)]
 
     def e2e_step(i):
-        b = i % 2
+        b = i % E2E_STREAMS
         st_b = streams[b]
         with torch.cuda.stream(st_b):
             x_dev[b].copy_(x_host[b], non_blocking=True)
@@ -670,18 +674,18 @@ def run_ours(args, world, rank, local):
                                     wss[b].nbytes, ctypes.c_void_p(st_b.cuda_stream)), "forward")
             y_host[b].copy_(y_dev[b], non_blocking=True)
 
-    for i in range(max(2, args.warmup)):
+    for i in range(max(E2E_STREAMS, args.warmup)):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     ev0 = torch.cuda.Event(enable_timing=True)
-    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(E2E_STREAMS)]
     ev0.record(stream)
     for st_b in streams:
         st_b.wait_event(ev0)
     for i in range(args.steps):
         e2e_step(i)
-    for b in range(2):
+    for b in range(E2E_STREAMS):
         ev_end[b].record(streams[b])
     torch.cuda.synchronize()
     barrier(world)
@@ -759,8 +763,8 @@ def run_ours(args, world, rank, local):
         "stages": extra,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "tokens_per_s": world * T * args.steps / (e2e_ms * 1e-3),
                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 4,
-                "how": "moe_forward per step with its x H2D from pinned memory and y D2H, steps alternating "
-                       "over two streams; weights resident (inputs exceed L2, no flush)"},
+                "how": "moe_forward per step with its x H2D from pinned memory and y D2H, steps rotating "
+                       f"over {E2E_STREAMS} streams; weights resident (inputs exceed L2, no flush)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
