@@ -161,8 +161,9 @@ def test_route_permute_fused_matches_separate(cuda_device, T, d, E, k, bias):
     assert np.array_equal(fused["dst"].cpu().numpy(), dst)
 
 
-def test_route_permute_fused_reports_nan(cuda_device):
-    T, d, E, k = 300, 128, 16, 2
+@pytest.mark.parametrize("E", [16, 64])  # the SIMT router, the tensor-core router's epilogue
+def test_route_permute_fused_reports_nan(cuda_device, E):
+    T, d, k = 300, 128, 2
     cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=k)
     inp = I.make_inputs(cfg, device=cuda_device, seed=3, weights=False)
     x = inp["x"].clone()
