@@ -26,6 +26,12 @@ step (twice the forward's, recomputation not counted).
 
 --graph adds a `graph` key: moe_forward captured once into a CUDA graph and
 replayed per step.  --fp8 runs both expert GEMMs in e4m3.
+
+With rounding off, and experts averaging at least 512 rows, the line also
+carries `token_rounding`: the same layer with each expert's token count
+rounded to the nearest multiple of the 256-row SM-pair tile, the method's
+token rounding, timed the same way (--no-rounding-variant skips it).  It is
+reported beside `value`, not in it.
 """
 from __future__ import annotations
 
@@ -51,6 +57,9 @@ METRIC_BWD = "MoE bwd active TFLOPS & tokens/s on 1 B300; % bf16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 # streams (and buffer sets) the forward e2e loop rotates over
 E2E_STREAMS = 3
+# token-rounding tile of the variant timed beside the plain layer: the
+# 256-row M of an SM-pair tile
+ROUND_TILE = 256
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # up-projection's main GEMM kernel, from an ncu capture of the current kernel,
@@ -224,10 +233,23 @@ def oracle_baseline(cfg, inp_host, round_mode, budget_s: float, n_samples: int =
             "kind": "oracle", "sample": smp.describe(n_samples, sum(meas))}
 
 
+def bench_config(args):
+    """The workload: the named config with --tokens, --experts and --tile applied."""
+    from dataclasses import replace
+    cfg = I.get_config(args.config)
+    if getattr(args, "tokens", 0):
+        cfg = cfg.with_tokens(args.tokens)
+    if getattr(args, "experts", 0):
+        cfg = replace(cfg, E=args.experts)
+    if getattr(args, "tile", 0):
+        cfg = replace(cfg, tile=args.tile)
+    return cfg
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    cfg = I.get_config(args.config)
+    cfg = bench_config(args)
     inp = I.make_inputs(cfg, device="cpu", seed=0)
     if args.backward:
         inp["dy"] = torch.randn(cfg.T, cfg.d, generator=torch.Generator().manual_seed(1000)).to(torch.bfloat16)
@@ -325,9 +347,7 @@ def run_backward(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
-    cfg = I.get_config(args.config)
-    if args.tokens:
-        cfg = cfg.with_tokens(args.tokens)
+    cfg = bench_config(args)
     T, k, E, d, n = cfg.T, cfg.k, cfg.E, cfg.d, cfg.n
     shape = B.make_shape(T, d, n, E, k, cfg.tile, args.round, args.seed)
     inp = I.make_replica_inputs(cfg, rank, device=dev)
@@ -464,12 +484,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
-    cfg = I.get_config(args.config)
-    if args.tokens:
-        cfg = cfg.with_tokens(args.tokens)
-    if args.experts:
-        from dataclasses import replace
-        cfg = replace(cfg, E=args.experts)
+    cfg = bench_config(args)
     mode = args.round
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
     inp = I.make_replica_inputs(cfg, rank, device=dev)
@@ -643,6 +658,49 @@ def run_ours(args, world, rank, local):
                       "ms_per_step": g_ms / args.steps,
                       "how": "moe_forward captured once into a CUDA graph, replayed per step (L2 flushed between)"}
 
+    # ------------------------------------------------ the same layer with the pages' token rounding
+    # Each expert's count rounded to the nearest multiple of the 256-row
+    # SM-pair tile (MOE_ROUND_NEAREST): a variant of the method, reported
+    # beside `value`, never in its place.  Rows come from the rounding of the
+    # same logits, read outside the timed region.  Only where experts average
+    # at least two tiles of rows: below that the rounding mostly drops rows.
+    rounding_line = None
+    if (args.round == "off" and not args.fp8 and not args.no_rounding_variant
+            and T * k >= 2 * ROUND_TILE * E):
+        rshape = B.make_shape(T, d, n, E, k, ROUND_TILE, "nearest", args.seed)
+        rws = B.Workspace(rshape, dev)
+        ry = torch.empty_like(y)
+        rsp = ctypes.byref(rshape)
+
+        def rforward():
+            check(L.moe_forward(rsp, P(x), P(Wr), P(bias), P(W13p), P(W2p), P(ry), rws.ptr, rws.nbytes,
+                                ctypes.c_void_p(stream.cuda_stream)), "forward (token rounding)")
+
+        for _ in range(args.warmup):
+            rforward()
+        torch.cuda.synchronize()
+        rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        barrier(world)
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            rev[i][0].record(stream)
+            rforward()
+            rev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        B.moe_check_device_status(rws)
+        r_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in rev), world, dev)
+        rlogits, ridx, _ = B.moe_route(x, Wr, bias, k, rws)
+        R_round = int(B.moe_token_round(rshape, rlogits, ridx, rws)["offsets"][E].item())
+        rounding_line = {"round": "nearest", "tile": ROUND_TILE,
+                         "value": world * active * args.steps / (r_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "executed_tflops": world * 6.0 * R_round * d * n * args.steps / (r_ms * 1e-3) / 1e12,
+                         "rows": R_round, "ms_per_step": r_ms / args.steps,
+                         "how": "moe_forward on the same inputs with each expert's token count rounded to the "
+                                "nearest multiple of the SM-pair tile (L2 flushed between steps); value counts "
+                                "6*T*k*d*n like the line's, executed_tflops the rounded rows"}
+        del rws, ry
+
     # ------------------------------------------------ e2e: through moe_forward, host buffers
     # Each step copies its x from pinned host memory, runs moe_forward and
     # copies its y back.  Steps rotate over E2E_STREAMS streams (each with its
@@ -770,6 +828,9 @@ def run_ours(args, world, rank, local):
     }
     if graph_line is not None:
         line["graph"] = graph_line
+    if rounding_line is not None:
+        rounding_line["frac_of_bf16_peak"] = rounding_line["value"] / world / burst
+        line["token_rounding"] = rounding_line
     if inp_host is not None:
         line["cpu_baseline"] = oracle_baseline(cfg, inp_host, mode, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -816,6 +877,10 @@ def main():
     ap.add_argument("--config", default="dsv3", choices=sorted(I.CONFIGS))
     ap.add_argument("--round", default="off", choices=["off", "nearest", "up", "stochastic"])
     ap.add_argument("--seed", type=int, default=0, help="seed of the stochastic rounding draws")
+    ap.add_argument("--no-rounding-variant", action="store_true",
+                    help="skip the token-rounding variant timed beside the plain layer")
+    ap.add_argument("--tile", type=int, default=0, choices=[0, 64, 128, 256],
+                    help="token-rounding tile (default: the config's, 128)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (profiling of small cases only)")
     ap.add_argument("--experts", type=int, default=0, help="override E (profiling of small cases only)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
