@@ -772,7 +772,8 @@ def run_ours(args, world, rank, local):
     roofline = {"bound": "tensor", "kernel": "moe_gemm_kernel<up%s, SwiGLU>" % (" e4m3" if args.fp8 else ""),
                 "achieved": up_tflops, "peak": up_peak, "unit": "TFLOP/s", "frac": up_tflops / up_peak,
                 "traffic": UP_TRAFFIC.get((cfg.name, args.gather, GEMM_REV))
-                if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) and not args.fp8 else None,
+                if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) and not args.fp8
+                and args.round == "off" else None,
                 "traffic_unit": "bytes per launch of the main up GEMM kernel (ncu dram read+write)",
                 "algorithmic_bytes_per_launch": 2.0 * E * 2 * n * d + R * d * 2.0 + R * n * 2.0,
                 "peak_source": f"{peak_src} {up_peak_kind}",
