@@ -226,37 +226,44 @@ int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const 
   __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
   int32_t* chunk_hist = at<int32_t>(ws, off[kPermHist]);
   const int64_t hist_count = static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k);
-  if (router_is_small(s->d, s->E) && s->k <= kFusedTopk) {
-    // few experts: the weight layout (and zeroed chunk counts), the SIMT
-    // router with the top-k and the chunk counts, then the scan and the
-    // scatter (4 launches)
+  if (router_is_small(s->d, s->E)) {
+    // few experts: the weight layout (and zeroed chunk counts), then the SIMT
+    // router, which moe_router_logits uses too.  With k <= kFusedTopk it
+    // also takes the top-k and the chunk counts, and the scan and the
+    // scatter follow (4 launches); with larger k the top-k + histogram
+    // kernel reads its logits.
     float* Wp = at<float>(ws, off[kRouterW]);
     launch_router_small_prep(Wr, s->d, s->E, Wp, chunk_hist, hist_count, as_stream(stream));
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    const int rst = launch_router_small(static_cast<const __nv_bfloat16*>(x), Wp, bias, logits, s->T, s->d, s->E, s->k,
-                                        topk_idx, topk_w, chunk_hist, status_of(ws), kDefaultTimeoutNs,
+    const bool fuse = s->k <= kFusedTopk;
+    const int rst = launch_router_small(static_cast<const __nv_bfloat16*>(x), Wp, bias, logits, s->T, s->d, s->E,
+                                        fuse ? s->k : 0, fuse ? topk_idx : nullptr, fuse ? topk_w : nullptr,
+                                        fuse ? chunk_hist : nullptr, status_of(ws), kDefaultTimeoutNs,
                                         as_stream(stream));
     if (rst != MOE_OK) return rst;
-    launch_perm_scan_scatter(topk_idx, topk_w, static_cast<int64_t>(s->T) * s->k, s->k, s->E, chunk_hist, counts,
-                             offsets, src, dst, row_token, row_w, as_stream(stream));
-    return last_launch();
-  }
-  const bool fused = s->E <= 256;  // the fused top-k + histogram kernel (counts start at zero)
-  launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), fused ? chunk_hist : nullptr, fused ? hist_count : 0);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  if (router_fuses_topk(s->E, s->k)) {
-    // top-k and chunk counts in the router GEMM's epilogue
+    if (fuse) {
+      launch_perm_scan_scatter(topk_idx, topk_w, static_cast<int64_t>(s->T) * s->k, s->k, s->E, chunk_hist, counts,
+                               offsets, src, dst, row_token, row_w, as_stream(stream));
+      return last_launch();
+    }
+  } else {
+    const bool fused = s->E <= 256;  // the fused top-k + histogram kernel (counts start at zero)
+    launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), fused ? chunk_hist : nullptr, fused ? hist_count : 0);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (router_fuses_topk(s->E, s->k)) {
+      // top-k and chunk counts in the router GEMM's epilogue
+      const int rst = launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
+                                       status_of(ws), kDefaultTimeoutNs, as_stream(stream), s->k, topk_idx, topk_w,
+                                       chunk_hist);
+      if (rst != MOE_OK) return rst;
+      launch_perm_scan_scatter(topk_idx, topk_w, static_cast<int64_t>(s->T) * s->k, s->k, s->E, chunk_hist, counts,
+                               offsets, src, dst, row_token, row_w, as_stream(stream));
+      return last_launch();
+    }
     const int rst = launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
-                                     status_of(ws), kDefaultTimeoutNs, as_stream(stream), s->k, topk_idx, topk_w,
-                                     chunk_hist);
+                                     status_of(ws), kDefaultTimeoutNs, as_stream(stream));
     if (rst != MOE_OK) return rst;
-    launch_perm_scan_scatter(topk_idx, topk_w, static_cast<int64_t>(s->T) * s->k, s->k, s->E, chunk_hist, counts,
-                             offsets, src, dst, row_token, row_w, as_stream(stream));
-    return last_launch();
   }
-  const int rst = launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
-                                   status_of(ws), kDefaultTimeoutNs, as_stream(stream));
-  if (rst != MOE_OK) return rst;
   launch_topk_permute(logits, s->T, s->E, s->k, topk_idx, topk_w, chunk_hist, counts, offsets, src, dst, row_token,
                       row_w, status_of(ws), as_stream(stream));
   return last_launch();

@@ -258,9 +258,10 @@ void launch_permute(const int32_t* idx, const float* w, int64_t A, int k, int E,
 }
 
 // Top-k gating and the permutation of its assignments.  E <= 256: the fused
-// top-k + histogram kernel (chunk_hist zeroed beforehand, see
-// launch_split_router), the scan and the scatter (three launches instead of
-// four); larger E: the top-k kernel and the three permutation launches.
+// top-k + histogram kernel (chunk_hist zeroed beforehand, by
+// launch_split_router or launch_router_small_prep), the scan and the scatter
+// (three launches instead of four); larger E: the top-k kernel and the three
+// permutation launches.
 void launch_topk_permute(const float* logits, int T, int E, int k, int32_t* idx, float* w, int32_t* chunk_hist,
                          int32_t* counts, int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
                          float* row_w, int32_t* status, cudaStream_t stream) {

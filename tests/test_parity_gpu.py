@@ -124,14 +124,15 @@ def test_permute_bit_exact(cuda_device, T, E, k, skew):
                                           (5000, 256, 128, 8, False), (3001, 128, 256, 5, True),
                                           (700, 128, 256, 6, False), (333, 128, 300, 7, True),
                                           (4096, 128, 64, 1, False), (600, 128, 64, 12, False),
-                                          (500, 128, 200, 16, True)])
+                                          (500, 128, 200, 16, True), (777, 256, 16, 12, True),
+                                          (500, 128, 12, 10, False), (300, 192, 9, 9, True)])
 def test_route_permute_fused_matches_separate(cuda_device, T, d, E, k, bias):
     """moe_route_permute equals moe_route then moe_permute bit for bit (every
     output), matches the oracle's top-k and permutation on the same fp32
     logits, and gives the same bits when called again.  k = 3, 5, 6, 7 put
     tokens across the 2048-assignment chunk boundaries; E = 300 takes the
     unfused path; k = 12 and 16 (k > 8) take the top-k + histogram kernel
-    instead of the router epilogue."""
+    instead of the router epilogue, also behind the SIMT router (E <= 16)."""
     cfg = I.MoEConfig("t", T=T, d=d, n=64, E=E, k=k, bias="normal" if bias else None, bias_scale=0.3)
     inp = I.make_inputs(cfg, device=cuda_device, seed=T + E + k, weights=False)
     s, ws = ws_for(T, d, 64, E, k, cuda_device)
