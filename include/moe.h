@@ -148,7 +148,10 @@ int moe_router_logits(const moe_shape* s, const void* x, const float* Wr, const 
 int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, float* topk_w,
                     void* ws, void* stream);
 
-/* moe_router_logits followed by moe_topk_gating. */
+/* moe_router_logits followed by moe_topk_gating: the same logits, indices
+ * and weights, bit for bit.  Where the router can (k <= 8 with E <= 256) it
+ * takes the top-k in its own last step, one launch fewer; `ws` must hold
+ * moe_workspace_bytes(s) bytes. */
 int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* bias,
               float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream);
 

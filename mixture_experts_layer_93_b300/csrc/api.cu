@@ -207,6 +207,29 @@ int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, 
 
 int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
               int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
+  if (!shape_ok(s) || !x || !Wr || !logits || !topk_idx || !topk_w || !ws || !aligned16(x) || !aligned16(ws))
+    return MOE_ERR_INVALID;
+  // Where the router takes the top-k in its last step (the bits of
+  // moe_topk_gating on its logits), one launch fewer.  Its chunk counts go
+  // to the permutation's histogram slot, which moe_permute overwrites.
+  int64_t off[kNumSlots];
+  layout(s, off);
+  int32_t* chunk_hist = at<int32_t>(ws, off[kPermHist]);
+  const int64_t hist_count = static_cast<int64_t>(s->E) * perm_num_chunks(static_cast<int64_t>(s->T) * s->k);
+  if (s->k <= kFusedTopk && router_is_small(s->d, s->E)) {
+    float* Wp = at<float>(ws, off[kRouterW]);
+    launch_router_small_prep(Wr, s->d, s->E, Wp, chunk_hist, hist_count, as_stream(stream));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_router_small(static_cast<const __nv_bfloat16*>(x), Wp, bias, logits, s->T, s->d, s->E, s->k,
+                               topk_idx, topk_w, chunk_hist, status_of(ws), kDefaultTimeoutNs, as_stream(stream));
+  }
+  if (!router_is_small(s->d, s->E) && router_fuses_topk(s->E, s->k)) {
+    __nv_bfloat16* Wr3 = at<__nv_bfloat16>(ws, off[kRouterW]);
+    launch_split_router(Wr, Wr3, s->d, s->E, as_stream(stream), chunk_hist, hist_count);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_router_tc(static_cast<const __nv_bfloat16*>(x), Wr3, bias, logits, s->T, s->d, s->E,
+                            status_of(ws), kDefaultTimeoutNs, as_stream(stream), s->k, topk_idx, topk_w, chunk_hist);
+  }
   int st = moe_router_logits(s, x, Wr, bias, logits, ws, stream);
   if (st != MOE_OK) return st;
   return moe_topk_gating(s, logits, topk_idx, topk_w, ws, stream);
