@@ -65,10 +65,11 @@ ROUND_TILE = 256
 # up-projection's main GEMM kernel, from an ncu capture of the current kernel,
 # keyed by workload, A path and kernel revision; a kernel change bumps GEMM_REV
 # and drops stale entries.  DeepSeek-V3-style layer: captured on the same layer
-# with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.212 GB,
-# scaled by the experts processed (x8).
-GEMM_REV = "super-tiles-v12"
-UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2212011776}
+# with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.210 GB,
+# scaled by the experts processed (x8).  The others at full size.
+GEMM_REV = "super-tiles-mchunk8-v13"
+UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2210303744, ("mixtral", 0, GEMM_REV): 3743594752,
+              ("b7", 0, GEMM_REV): 1131990528, ("skew", 0, GEMM_REV): 6240171008}
 
 
 def load_peaks():

@@ -155,14 +155,20 @@ struct GemmCfg {
                 "group table alignment");
 };
 
+// Tile units of one group that run as a chunk (see decode_tile).
+constexpr int kMChunk = 8;
+
 // e: on entry the group of a tile at or before tau (each warp visits its tiles
 // in increasing order, starting from e = 0); on exit the group of tau.  A few
 // linear probes cover the usual step to the same or a nearby group, then a
 // binary search over the rest.  prefix[E] * n_blocks > tau bounds both.
 // Within a group the m-block runs fastest (N_FAST false): the expert's weight
-// slice of one n-block stays in L2 for all its m-blocks.  N_FAST (the router,
-// whose whole B is a few MB) runs the n-blocks of one m-block together, so
-// each A row block is read from HBM once.
+// slice of one n-block stays in L2 for all its m-blocks.  A group with more
+// than kMChunk units runs them in chunks of kMChunk, each over every n-block
+// (m fastest within the chunk): its A rows stay in L2 across the n-blocks
+// instead of streaming from HBM once per n-block (a heavily loaded expert's
+// rows exceed L2).  N_FAST (the router, whose whole B is a few MB) runs the
+// n-blocks of one m-block together, so each A row block is read from HBM once.
 template <bool N_FAST = false>
 __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int E, int n_blocks, int& e, int& nb,
                                             int& mb) {
@@ -187,8 +193,16 @@ __device__ __forceinline__ void decode_tile(int tau, const int32_t* prefix, int 
     nb = local - mb * n_blocks;
   } else {
     const int me = prefix[e + 1] - prefix[e];
-    nb = local / me;
-    mb = local - nb * me;
+    if (me <= kMChunk) {
+      nb = local / me;
+      mb = local - nb * me;
+    } else {
+      const int chunk = local / (kMChunk * n_blocks);
+      const int r = local - chunk * (kMChunk * n_blocks);
+      const int units = min(kMChunk, me - chunk * kMChunk);  // the last chunk may be short
+      nb = r / units;
+      mb = chunk * kMChunk + (r - nb * units);
+    }
   }
 }
 
