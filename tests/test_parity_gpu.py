@@ -463,9 +463,12 @@ def test_forward_tiny_config(cuda_device):
     assert frac > 0.95
 
 
+# the last shape gives two experts about 3000 rows each: 12 row-pair units,
+# which the grouped GEMMs run as a chunk of 8 and a short chunk of 4 over
+# every n-block
 @pytest.mark.parametrize("T,d,n,E,k,bias", [(1000, 256, 192, 16, 4, True), (333, 128, 128, 9, 9, False),
                                             (2049, 384, 256, 32, 8, True), (1, 64, 64, 4, 2, False),
-                                            (130, 64, 64, 1, 1, False)])
+                                            (130, 64, 64, 1, 1, False), (3001, 512, 384, 2, 2, False)])
 def test_forward_ragged_shapes(cuda_device, T, d, n, E, k, bias):
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k, bias="normal" if bias else None, bias_scale=0.3)
     _forward_and_check(cfg, cuda_device, seed=T + E)
