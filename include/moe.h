@@ -173,12 +173,14 @@ int moe_permute(const moe_shape* s, const int32_t* topk_idx, const float* topk_w
  * "硬件加速的考量", section 自定义核与核融合: gate scores, top-k, and the
  * grouping that collects each expert's tokens).  Same outputs, bit for bit, as
  * moe_route followed by moe_permute with topk_w given, in fewer launches:
- * for E <= 256 and k <= 8 the router GEMM's epilogue takes each token's top-k
- * and gate weights and counts each chunk's assignments per expert (integer
- * atomics); for E <= 256 one kernel does that from the stored logits; the
+ * for E <= 256 and k <= 8 the router's last step (the tensor-core GEMM's
+ * epilogue, or the SIMT router for E <= 16) takes each token's top-k and gate
+ * weights and counts each chunk's assignments per expert (integer atomics);
+ * for E <= 256 and larger k one kernel does that from the stored logits; the
  * scan of the counts and the scatter follow.  (E > 256 runs the separate
- * top-k and permutation kernels.)  Arrays as in moe_route and moe_permute; every output pointer is
- * required.  Uses the workspace (split weights, chunk histograms). */
+ * top-k and permutation kernels.)  Arrays as in moe_route and moe_permute;
+ * every output pointer is required.  Uses the workspace (router weights,
+ * chunk histograms). */
 int moe_route_permute(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                       float* logits, int32_t* topk_idx, float* topk_w, int32_t* counts,
                       int32_t* offsets, int32_t* src, int32_t* dst, int32_t* row_token,
