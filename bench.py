@@ -488,6 +488,8 @@ def run_ours(args, world, rank, local):
     cfg = bench_config(args)
     mode = args.round
     shape = B.make_shape(cfg.T, cfg.d, cfg.n, cfg.E, cfg.k, cfg.tile, mode, args.seed)
+    if args.gather < 0:  # the A path moe_forward takes (the e4m3 layer has its own quantising gather)
+        args.gather = 0 if args.fp8 else B.moe_forward_a_path(shape)
     inp = I.make_replica_inputs(cfg, rank, device=dev)
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     W13q = sW13 = W2q = sW2 = None
@@ -551,7 +553,9 @@ def run_ours(args, world, rank, local):
         up_launches = 2  # quantising gather + one SM-pair e4m3 GEMM
         gemm_launches = 2  # down: h quantisation + one SM-pair e4m3 GEMM
     fused_route = 4 if (E <= 256 and k <= 8) else (5 if E <= 256 else 6)
-    route_launches = fused_route if mode == "off" else 3 + 9
+    # rounding: moe_route (weights prepared + router with the top-k where
+    # k <= 8 and E <= 256, else + a top-k kernel) then the 9 rounding launches
+    route_launches = fused_route if mode == "off" else (2 if (E <= 256 and k <= 8) else 3) + 9
     launches_per_step = route_launches + up_launches + gemm_launches + 1
 
     def check(rc, what):
@@ -808,7 +812,8 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 expert GEMMs" if args.fp8 else "bf16",
         "data": "synthetic",
         "config": {"workload": cfg.description, "T": T, "d": d, "n": n, "E": E, "k": k, "round": mode,
-                   "up_gather": ["gather_kernel+tma", "tma_gather4", "cp_async"][args.gather],
+                   "up_gather": ["gather_kernel+tma", "tma_gather4",
+                                 "cp_async (gather in the operand load)"][args.gather],
                    "expert_gemm_operands": "e4m3 (x per token, W1/W3 per channel, h per row, W2 per channel)"
                    if args.fp8 else "bf16",
                    "tile": cfg.tile if mode != "off" else None,
@@ -891,9 +896,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
                     help="e4m3 expert GEMMs (moe_forward_fp8); the default measures the bf16 layer")
-    ap.add_argument("--gather", type=int, default=0, choices=[0, 1, 2],
-                    help="up-projection A operand: 0 = gather kernel then tiled TMA, 1 = TMA gather4 of token "
-                         "rows, 2 = per-lane cp.async of token rows")
+    ap.add_argument("--gather", type=int, default=-1, choices=[-1, 0, 1, 2],
+                    help="up-projection A operand: -1 = the path moe_forward takes for the shape (default), "
+                         "0 = gather kernel then tiled TMA, 1 = TMA gather4 of token rows, 2 = per-lane "
+                         "cp.async of token rows")
     ap.add_argument("--graph", action="store_true",
                     help="also time moe_forward replayed from one captured CUDA graph")
     ap.add_argument("--backward", action="store_true",

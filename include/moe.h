@@ -24,9 +24,11 @@
  * gate weight into the down-projection's ("SonicMoE: 加速 MoE 模型的 IO 与 Tile
  * 感知优化", the "关键 Kernel 对比" table).  The gather of token rows can also be
  * fused into the up-projection's operand load (same page, "Gather 与加载融合";
- * moe_expert_up with gather = 1 or 2), but moe_forward stages the rows with a
- * token-order copy kernel and loads them with tiled TMA (gather = 0), which
- * measured faster on B300.  The optional token rounding (same page, "3. Token
+ * moe_expert_up with gather = 1 or 2).  moe_forward fuses it (gather = 2,
+ * wide tiles) where the up GEMM has two 256-wide n-blocks (n = 256), so each
+ * row is gathered once; elsewhere it stages the rows with a token-order copy
+ * kernel and loads them with tiled TMA (gather = 0), which measured faster on
+ * B300 there (moe_forward_a_path).  The optional token rounding (same page, "3. Token
  * Rounding 路由算法") rounds each expert's row count to a multiple of a tile
  * (moe_token_round).
  *
@@ -272,6 +274,13 @@ int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const in
  * moe_permute).  A token with no rows gets y[t] = 0. */
 int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets,
                 const int32_t* tok_rows, void* y, void* stream);
+
+/* The A-operand path (the `gather` argument of moe_expert_up) that
+ * moe_forward uses for this shape: 2 (rows gathered into the operand load by
+ * cp.async, with wide tiles that put both 256-wide n-blocks against each
+ * gathered row block) where n = 256, else 0 (the token-order staging copy,
+ * then tiled TMA).  -1 for an invalid shape. */
+int moe_forward_a_path(const moe_shape* s);
 
 /* The whole layer: route, (round), permute, up, down, combine.
  *   x [T, d] bf16, Wr [d, E] fp32, bias [E] fp32 or NULL,

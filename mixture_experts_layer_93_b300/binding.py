@@ -76,6 +76,7 @@ _SIGNATURES = {
     "moe_expert_down": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_SHP, _P, _P, _P, _P, _P]),
     "moe_forward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_a_path": (_I, [_SHP]),
     "moe_workspace_layout": (_I, [_SHP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
     "moe_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
     "moe_backward_workspace_bytes": (_SZ, [_SHP]),
@@ -393,6 +394,11 @@ def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
     _check(lib().moe_combine(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
                              _stream(ys.device)), "moe_combine")
     return y
+
+
+def moe_forward_a_path(shape: moe_shape) -> int:
+    """The A-operand path (moe_expert_up's `gather`) moe_forward uses for the shape."""
+    return int(lib().moe_forward_a_path(ctypes.byref(shape)))
 
 
 def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):

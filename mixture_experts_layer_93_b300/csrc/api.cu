@@ -70,8 +70,14 @@ inline int last_launch() { return cudaGetLastError() == cudaSuccess ? MOE_OK : M
 
 inline int32_t* status_of(void* ws) { return reinterpret_cast<int32_t*>(ws); }
 
-// A-operand path moe_forward uses for the up-projection (see moe_expert_up).
-constexpr int kForwardGather = 0;
+// A-operand path moe_forward uses for the up-projection (see moe_expert_up):
+// rows gathered into the operand load by cp.async (path 2) where the up GEMM
+// has exactly two 256-wide n-blocks (n = 256), so that one wide tile covers
+// all of N and each row is gathered once; else the token-order staging copy
+// and tiled TMA (path 0).  Measured: the 7B-class layer (n = 256) +8 % with
+// path 2; the layers with 8 to 112 n-blocks, which would gather each row 4 to
+// 56 times, 5-11 % slower.
+int forward_gather(const moe_shape* s) { return s->n == 256 ? 2 : 0; }
 
 int check_ws(const moe_shape* s, void* ws, size_t ws_bytes, bool fp8 = false) {
   if (!ws || !aligned16(ws)) return MOE_ERR_INVALID;
@@ -204,6 +210,8 @@ int moe_topk_gating(const moe_shape* s, const float* logits, int32_t* topk_idx, 
   launch_topk_gating(logits, topk_idx, topk_w, s->T, s->E, s->k, status_of(ws), as_stream(stream));
   return last_launch();
 }
+
+int moe_forward_a_path(const moe_shape* s) { return shape_ok(s) ? forward_gather(s) : -1; }
 
 int moe_route(const moe_shape* s, const void* x, const float* Wr, const float* bias, float* logits,
               int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
@@ -397,8 +405,8 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
     combine_offsets = tok_offsets;
     combine_rows = tok_rows;
   }
-  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, combine_offsets, combine_rows, h, kForwardGather, ws,
-                          ws_bytes, stream)) != MOE_OK)
+  if ((st = moe_expert_up(s, x, W13p, counts, offsets, row_token, combine_offsets, combine_rows, h,
+                          forward_gather(s), ws, ws_bytes, stream)) != MOE_OK)
     return st;
   if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
   return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);

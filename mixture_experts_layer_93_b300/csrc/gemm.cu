@@ -125,17 +125,18 @@ __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (
 // memory traffic per 1024 MMA cycles instead of 64 KB per 512, and a third
 // less TMA traffic per FLOP.  The two accumulators fill the 512 TMEM columns,
 // so the epilogue of one super tile does not overlap the next one's MMAs.
-template <int BN, bool PAIR, int EPI, bool SUP = false>
+template <int BN, bool PAIR, int EPI, int SUP = 0>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows held per CTA
   static constexpr int A_TILE_BYTES = BM * BK * 2;   // one 128-row A tile
-  static constexpr int A_BYTES = A_TILE_BYTES * (SUP ? 2 : 1);
-  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int A_BYTES = A_TILE_BYTES * (SUP == 1 ? 2 : 1);
+  static constexpr int B_TILE_BYTES = B_ROWS * BK * 2;  // one n-block's B rows
+  static constexpr int B_BYTES = B_TILE_BYTES * (SUP == 2 ? 2 : 1);
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // epilogue staging for TMA stores: per epilogue warp two 32 x 64-byte boxes
   // (one with eight warps on super tiles, which keeps their fourth stage)
-  static constexpr int OUT_BOXES = (SUP && EPI == 8) ? 1 : 2;
+  static constexpr int OUT_BOXES = (SUP != 0 && EPI == 8) ? 1 : 2;
   // operand ring: what is left of 227 KB after the staging boxes, barriers,
   // prefix table and token table (at most 8 stages)
   static constexpr int RING_BUDGET =
@@ -267,13 +268,14 @@ __device__ __forceinline__ void wgrad_tile(int tau, const GemmParams& p, int& e,
   }
 }
 
-template <int BN, int MODE, bool PAIR, int EPI, bool SUP = false>
+template <int BN, int MODE, bool PAIR, int EPI, int SUP = 0>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN, PAIR, EPI, SUP>;
-  static_assert(!SUP || (PAIR && BN == 256 && (MODE == kModeUp || MODE == kModeDown)),
-                "super tiles: up or down GEMM on SM pairs with 256-wide n-blocks");
+  static_assert(SUP == 0 || (PAIR && BN == 256 && (MODE == kModeUp || MODE == kModeDown)),
+                "super and wide tiles: up or down GEMM on SM pairs with 256-wide n-blocks");
+  static_assert(SUP != 2 || MODE == kModeUp, "wide tiles: the up GEMM");
   constexpr int kPer = PAIR ? 2 : 1;  // CTAs per tile unit
   constexpr bool kF8 = MODE == kModeUpF8 || MODE == kModeDownF8;
   constexpr bool kDown = MODE == kModeDown || MODE == kModeDownF8 || MODE == kModeDxRows;
@@ -483,7 +485,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           tok_s[r] = p.row_token[tok_base + min(r, last)];
           __syncwarp();
         }
-        const int brow = e * p.b_rows_per_expert + nb * BN + rank * C::B_ROWS;
+        // wide tiles cover n-blocks 2nb and 2nb + 1
+        const int brow = e * p.b_rows_per_expert + (SUP == 2 ? 2 * nb : nb) * BN + rank * C::B_ROWS;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           int w = 1;
           if (lane == 0)
@@ -497,7 +500,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           const uint32_t a_dst = smem_u32(sA + stage * C::A_BYTES);
           const uint32_t b_dst = smem_u32(sB + stage * C::B_BYTES);
           if (issuer) {
-            if (SUP) {
+            if (SUP == 1) {
               // super tile: this CTA's block of each pair (if the kernel runs
               // it) and its half of the B tile; the even CTA's barrier counts
               // every A tile either CTA loads
@@ -527,6 +530,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                                                           : 2 * C::STAGE_BYTES - (partner_empty ? C::A_BYTES : 0));
                 if (p.gather == 0 && rows_valid > 0) tma_load_2d_pair(a_dst, &tmA, kb * KB_ELEMS, row0, fb0, pol_a);
                 tma_load_2d_pair(b_dst, &tmB, kb * KB_ELEMS, brow, fb0, pol_b);
+                // wide tile: the next n-block's B rows beside this one's
+                if (SUP == 2)
+                  tma_load_2d_pair(b_dst + C::B_TILE_BYTES, &tmB, kb * KB_ELEMS, brow + BN, fb0, pol_b);
               }
             } else {
               if (lane == 0) mbar_arrive_expect_tx(fb, p.gather == 2 ? C::B_BYTES : C::STAGE_BYTES);
@@ -577,10 +583,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           break;
         tc_fence_after();
         // SUP: one accumulator pair per tile (columns 0..BN-1 and BN..2BN-1);
-        // the second pair's MMAs run only when the kernel runs its blocks
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(SUP ? 0 : acc * BN);
-        [[maybe_unused]] bool two = false;
-        if constexpr (SUP) {
+        // a super tile's second pair's MMAs run only when the kernel runs its
+        // blocks, a wide tile's second n-block's always
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(SUP != 0 ? 0 : acc * BN);
+        [[maybe_unused]] bool two = SUP == 2;
+        if constexpr (SUP == 1) {
           int nb_, mu_, gstart_, gcount_;
           decode_tile<false>(tau, prefix, n_groups, p.n_blocks, mma_e, nb_, mu_);
           group_rows(p, grp_s, mma_e, gstart_, gcount_);
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
             else
               tc_mma_bf16(d_tmem, ad, bd, idesc, accum);
           }
-          if constexpr (SUP) {
+          if constexpr (SUP == 1) {
             if (two) {
               const uint32_t a1 = a0 + C::A_TILE_BYTES;
 #pragma unroll
@@ -623,6 +630,13 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                 tc_mma_bf16_pair(d_tmem + BN, smem_desc_k128(a1 + kk * 32), smem_desc_k128(b0 + kk * 32), idesc,
                                  (kb > 0 || kk > 0) ? 1u : 0u);
             }
+          } else if constexpr (SUP == 2) {
+            // wide tile: the same A rows against the next n-block's B rows
+            const uint32_t b1 = b0 + C::B_TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < C::BK / 16; ++kk)
+              tc_mma_bf16_pair(d_tmem + BN, smem_desc_k128(a0 + kk * 32), smem_desc_k128(b1 + kk * 32), idesc,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
           }
           // the slot is free in both CTAs once these MMAs have read it
           if (PAIR)
@@ -639,7 +653,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           tc_commit_pair_multicast(smem_u32(&tfull_bar[acc]), 0x3);
         else
           tc_commit(smem_u32(&tfull_bar[acc]));
-        if (SUP) {
+        if (SUP != 0) {
           acc_phase ^= 1u;  // one accumulator set: every tile waits for the last one's epilogue
         } else {
           acc ^= 1;
@@ -784,7 +798,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         // channels' scales are applied per column)
         if (MODE == kModeDownF8)
           nx_w = r_in_tile < nx_rows ? p.row_w[nx_row0 + r_in_tile] * p.row_scale[nx_row0 + r_in_tile] : 0.f;
-        if constexpr (SUP) {
+        if constexpr (SUP == 1) {
           const int lim = super_blocks(p.units, gcount), mb2 = mb + 2;
           nx_two = 4 * mu + 2 < lim;
           nx_row0b = gstart + mb2 * C::BM;
@@ -798,11 +812,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       uint64_t best[kFusedTopk];
       bool nan_seen = false;
       for (int it = 0, tau = tau_of(0); tau < total_tiles; tau = tau_next(tau, it), ++it) {
-        const int nb = nx_nb, row0a = nx_row0, rowsa = nx_rows, e_tile = nx_e;
+        const int nb_t = nx_nb, row0a = nx_row0, rowsa = nx_rows, e_tile = nx_e;
         const float wra = nx_w;
         [[maybe_unused]] const int row0b = nx_row0b, rowsb = nx_rowsb;
         [[maybe_unused]] const float wrb = nx_wb;
-        const int n_sub = (SUP && nx_two) ? 2 : 1;
+        const int n_sub = SUP == 2 ? 2 : ((SUP == 1 && nx_two) ? 2 : 1);
         const int tau_n = tau_next(tau, it);
         if (tau_n < total_tiles) decode_next(tau_n);
         int w = 1;
@@ -811,13 +825,17 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
                                 p.timeout_ns);
         if (!__shfl_sync(0xffffffffu, w, 0)) break;
         tc_fence_after();
-        // SUP: the two pairs' accumulators, columns 0.. and BN..; else one
+        // SUP: the two accumulators, columns 0.. and BN.. (super tiles: the
+        // two pairs' rows; wide tiles: the same rows, n-blocks 2nb and
+        // 2nb + 1); else one
 #pragma unroll 1
         for (int sp = 0; sp < n_sub; ++sp) {
-        const int row0 = sp ? row0b : row0a, rows_valid = sp ? rowsb : rowsa;
-        const float wr = sp ? wrb : wra;
+        const bool rows_b = SUP == 1 && sp;
+        const int row0 = rows_b ? row0b : row0a, rows_valid = rows_b ? rowsb : rowsa;
+        const float wr = rows_b ? wrb : wra;
+        const int nb = SUP == 2 ? 2 * nb_t + sp : nb_t;
         const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(SUP ? sp * BN : acc * BN);
+            tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(SUP != 0 ? sp * BN : acc * BN);
         const bool valid = r_in_tile < rows_valid;
         const int64_t row = static_cast<int64_t>(row0) + r_in_tile;
         const int warp_rows = max(0, min(32, rows_valid - ew * 32));
@@ -1078,7 +1096,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           else
             mbar_arrive(smem_u32(&tempty_bar[acc]));
         }
-        if (SUP) {
+        if (SUP != 0) {
           acc_phase ^= 1u;
         } else {
           acc ^= 1;
@@ -1112,14 +1130,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 }
 
 // ----------------------------------------------------------------- host
-template <int BN, int MODE, bool PAIR, int EPI, bool SUP>
+template <int BN, int MODE, bool PAIR, int EPI, int SUP>
 static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const GemmParams& p, cudaStream_t stream);
 
 // Eight epilogue warps when the K loop is short enough for the epilogue to be
 // on the critical path (measured: 7B-style layer +9 %, long-K layers -2..-3 %
 // with eight).
-template <int BN, int MODE, bool PAIR, bool SUP = false>
+template <int BN, int MODE, bool PAIR, int SUP = 0>
 static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, const GemmParams& p,
                        cudaStream_t stream) {
   const bool wide = ((MODE == kModeUp || MODE == kModeUpF8 || MODE == kModeUpPre) && p.num_kb <= 24) ||
@@ -1133,7 +1151,7 @@ static int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
     if constexpr (MODE != kModeRouter && MODE != kModeWgrad) {
       // super tiles: eight warps drain their two accumulators before the
       // next tile's MMAs can start
-      if (wide || SUP) return launch_gemm_epi<BN, MODE, PAIR, 8, SUP>(tmA, tmB, tmC, p, stream);
+      if (wide || SUP != 0) return launch_gemm_epi<BN, MODE, PAIR, 8, SUP>(tmA, tmB, tmC, p, stream);
     }
     return launch_gemm_epi<BN, MODE, PAIR, 4, SUP>(tmA, tmB, tmC, p, stream);
   }
@@ -1219,7 +1237,7 @@ int num_sms() {
 // launch.
 constexpr int kMaxGemmDevices = 64;
 
-template <int BN, int MODE, bool PAIR, int EPI, bool SUP>
+template <int BN, int MODE, bool PAIR, int EPI, int SUP>
 static int launch_gemm_epi(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                            const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BN, PAIR, EPI, SUP>;
@@ -1390,10 +1408,28 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
   if (pair && gather == 0 && BN == 256 && super_tiles(E, rows_cap)) {
     if (tails_in_pairs(E, rows_cap)) {
       p.units = 4;
-      return launch_gemm<256, kModeUp, true, true>(tmA, tmB, tmC, p, stream);
+      return launch_gemm<256, kModeUp, true, 1>(tmA, tmB, tmC, p, stream);
     }
     p.units = 5;
-    const int st = launch_gemm<256, kModeUp, true, true>(tmA, tmB, tmC, p, stream);
+    const int st = launch_gemm<256, kModeUp, true, 1>(tmA, tmB, tmC, p, stream);
+    if (st != MOE_OK) return st;
+    CUtensorMap tmB1;
+    if (!make_map_bf16(&tmB1, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
+    p.units = 2;
+    return launch_gemm<256, kModeUp, false>(tmA, tmB1, tmC, p, stream);
+  }
+  if (pair && gather == 2 && BN == 256 && p.n_blocks % 2 == 0) {
+    // rows gathered by cp.async (A path 2) feed wide tiles: each gathered
+    // row block serves two n-blocks, so the gather moves each row once per
+    // two n-blocks
+    GemmParams pw = p;
+    pw.n_blocks = p.n_blocks / 2;
+    if (tails_in_pairs(E, rows_cap)) {
+      pw.units = 3;
+      return launch_gemm<256, kModeUp, true, 2>(tmA, tmB, tmC, pw, stream);
+    }
+    pw.units = 1;
+    const int st = launch_gemm<256, kModeUp, true, 2>(tmA, tmB, tmC, pw, stream);
     if (st != MOE_OK) return st;
     CUtensorMap tmB1;
     if (!make_map_bf16(&tmB1, W13p, d, static_cast<uint64_t>(E) * 2 * n, BN)) return MOE_ERR_CUDA;
@@ -1515,10 +1551,10 @@ static int launch_down_like(const __nv_bfloat16* h, const __nv_bfloat16* W2p, co
     if (BN == 256 && super_tiles(E, rows_cap)) {
       if (tails_in_pairs(E, rows_cap)) {
         p.units = 4;
-        return launch_gemm<256, MODE, true, true>(tmA, tmB, tmC, p, stream);
+        return launch_gemm<256, MODE, true, 1>(tmA, tmB, tmC, p, stream);
       }
       p.units = 5;
-      const int st = launch_gemm<256, MODE, true, true>(tmA, tmB, tmC, p, stream);
+      const int st = launch_gemm<256, MODE, true, 1>(tmA, tmB, tmC, p, stream);
       if (st != MOE_OK) return st;
       CUtensorMap tmB1;
       if (!make_map_bf16(&tmB1, W2p, n, static_cast<uint64_t>(E) * d, BN)) return MOE_ERR_CUDA;

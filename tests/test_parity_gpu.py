@@ -256,10 +256,12 @@ def _routing_with_counts(counts, seed):
     return idx, c, offsets, src, dst
 
 
+@pytest.mark.parametrize("gather", [0, 2])
 @pytest.mark.parametrize("extra", [0, 800, 1024])
-def test_expert_up_odd_tails(cuda_device, extra):
+def test_expert_up_odd_tails(cuda_device, extra, gather):
     """Up GEMM on SM pairs (n % 128 == 0) with odd last blocks of every size:
-    h within one bf16 rounding."""
+    h within one bf16 rounding.  gather 2 (rows gathered by cp.async) runs
+    wide tiles, both n-blocks of n = 256 against one gathered row block."""
     counts = [c + extra for c in ODD_COUNTS]
     T, d, n, E, k = sum(counts), 256, 256, len(counts), 1
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
@@ -269,8 +271,8 @@ def test_expert_up_odd_tails(cuda_device, extra):
     W13p, W2p = B.moe_prepare_weights(inp["W1"], inp["W3"], inp["W2"])
     row_token = torch.from_numpy((src // k).astype(np.int32)).to(cuda_device)
     h = B.moe_expert_up(s, inp["x"], W13p, torch.from_numpy(c.astype(np.int32)).to(cuda_device),
-                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=0,
-                        tok_rows=torch.from_numpy(dst.astype(np.int32)).to(cuda_device))
+                        torch.from_numpy(offsets.astype(np.int32)).to(cuda_device), row_token, ws, gather=gather,
+                        tok_rows=torch.from_numpy(dst.astype(np.int32)).to(cuda_device) if gather == 0 else None)
     assert B.moe_check_device_status(ws) == B.MOE_OK
     h_gpu = to64(h[:T])
     h_ref = np.zeros((T, n))
