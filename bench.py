@@ -65,11 +65,12 @@ ROUND_TILE = 256
 # up-projection's main GEMM kernel, from an ncu capture of the current kernel,
 # keyed by workload, A path and kernel revision; a kernel change bumps GEMM_REV
 # and drops stale entries.  DeepSeek-V3-style layer: captured on the same layer
-# with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.210 GB,
-# scaled by the experts processed (x8).  The others at full size.
-GEMM_REV = "super-tiles-mchunk8-v13"
-UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2210303744, ("mixtral", 0, GEMM_REV): 3743594752,
-              ("b7", 0, GEMM_REV): 1131990528, ("skew", 0, GEMM_REV): 6240171008}
+# with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.212 GB,
+# scaled by the experts processed (x8).  The others at full size; the 7B-class
+# layer with the rows gathered in the operand load (A path 2, wide tiles).
+GEMM_REV = "wide-tiles-v14"
+UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2211549440, ("mixtral", 0, GEMM_REV): 4240926720,
+              ("b7", 2, GEMM_REV): 777297664, ("skew", 0, GEMM_REV): 6169012224}
 
 
 def load_peaks():
@@ -780,7 +781,10 @@ def run_ours(args, world, rank, local):
                 if (T, E) == (I.get_config(cfg.name).T, I.get_config(cfg.name).E) and not args.fp8
                 and args.round == "off" else None,
                 "traffic_unit": "bytes per launch of the main up GEMM kernel (ncu dram read+write)",
-                "algorithmic_bytes_per_launch": 2.0 * E * 2 * n * d + R * d * 2.0 + R * n * 2.0,
+                # W13, the A rows (staged rows, or x itself once where the
+                # gather is in the operand load), h
+                "algorithmic_bytes_per_launch": 2.0 * E * 2 * n * d + (R if args.gather == 0 else T) * d * 2.0
+                + R * n * 2.0,
                 "peak_source": f"{peak_src} {up_peak_kind}",
                 "frac_of_sustained": up_tflops / (sustained * up_peak / peak_t),
                 "algorithmic_flops_per_launch": up_flops}
