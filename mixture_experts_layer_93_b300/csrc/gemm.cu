@@ -1418,10 +1418,13 @@ int launch_expert_up(const __nv_bfloat16* x, const __nv_bfloat16* W13p, const in
     p.units = 2;
     return launch_gemm<256, kModeUp, false>(tmA, tmB1, tmC, p, stream);
   }
-  if (pair && gather == 2 && BN == 256 && p.n_blocks % 2 == 0) {
-    // rows gathered by cp.async (A path 2) feed wide tiles: each gathered
-    // row block serves two n-blocks, so the gather moves each row once per
-    // two n-blocks
+  if (pair && (gather == 0 || gather == 2) && BN == 256 && p.n_blocks % 2 == 0) {
+    // wide tiles: each row block serves two n-blocks, so A reaches shared
+    // memory once per two n-blocks: half the gather of A path 2, and half
+    // the A traffic of staged rows.  Measured over 20 power-capped steps:
+    // the 7B-class layer (n = 256, path 2) +8 %; the skewed layer (staged
+    // rows) +2-3 %, with rounding +1.8 %; the Mixtral-style layer even.
+    // (Super tiles, for few rows per expert, take their own branch above.)
     GemmParams pw = p;
     pw.n_blocks = p.n_blocks / 2;
     if (tails_in_pairs(E, rows_cap)) {
