@@ -66,11 +66,12 @@ ROUND_TILE = 256
 # keyed by workload, A path and kernel revision; a kernel change bumps GEMM_REV
 # and drops stale entries.  DeepSeek-V3-style layer: captured on the same layer
 # with 32 of its 256 experts (T=2048, the same 512 rows per expert), 2.212 GB,
-# scaled by the experts processed (x8).  The others at full size; the 7B-class
-# layer with the rows gathered in the operand load (A path 2, wide tiles).
-GEMM_REV = "wide-tiles-v14"
-UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2211549440, ("mixtral", 0, GEMM_REV): 4240926720,
-              ("b7", 2, GEMM_REV): 777297664, ("skew", 0, GEMM_REV): 6169012224}
+# scaled by the experts processed (x8).  The others at full size, on wide
+# tiles: the 7B-class layer with the rows gathered in the operand load (A path
+# 2), Mixtral-style and skewed layers on staged rows.
+GEMM_REV = "wide-tiles-v15"
+UP_TRAFFIC = {("dsv3", 0, GEMM_REV): 8 * 2211549440, ("mixtral", 0, GEMM_REV): 3741821696,
+              ("b7", 2, GEMM_REV): 777297664, ("skew", 0, GEMM_REV): 5549915904}
 
 
 def load_peaks():
