@@ -318,8 +318,11 @@ def test_expert_down_odd_tails(cuda_device, extra):
 
 
 # ---------------------------------------------------------- down-projection
+# the last two: more than 1024 rows per expert and K = n over 32 k-blocks
+# with two 256-wide n-blocks, which run as wide tiles (odd last blocks in
+# the pairs), with a ragged last block
 @pytest.mark.parametrize("T,d,n,E,k", [(700, 320, 128, 6, 2), (600, 384, 192, 5, 3), (500, 512, 64, 7, 2),
-                                       (256, 128, 64, 8, 2)])
+                                       (256, 128, 64, 8, 2), (3000, 512, 2176, 2, 1), (2601, 512, 2112, 2, 2)])
 def test_expert_down_gate_weight(cuda_device, T, d, n, E, k):
     cfg = I.MoEConfig("t", T=T, d=d, n=n, E=E, k=k)
     inp = I.make_inputs(cfg, device=cuda_device, seed=d + n)
