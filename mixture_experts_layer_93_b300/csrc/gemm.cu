@@ -118,13 +118,16 @@ __host__ __device__ constexpr int tmem_cols_for(int n) { return n <= 32 ? 32 : (
 // operands; D rows 128r.. land in CTA r's TMEM.  Each SM thus stores and feeds
 // half of B: per k-block 32 KB of shared-memory writes and reads instead of
 // 48 KB, which is what keeps a 1-CTA M=128 x N=256 MMA from full rate.
-// SUP (super tiles): the pair runs two 256-row tiles of one group against the
-// same B tile, so a stage holds two A tiles (one per tile) and one B tile and
-// each k-block issues both tiles' MMAs.  Per k-block an SM then stores 48 KB
-// and its tensor core reads 64 KB for twice the MMA work: 112 KB of shared-
-// memory traffic per 1024 MMA cycles instead of 64 KB per 512, and a third
-// less TMA traffic per FLOP.  The two accumulators fill the 512 TMEM columns,
-// so the epilogue of one super tile does not overlap the next one's MMAs.
+// SUP = 1 (super tiles): the pair runs two 256-row tiles of one group against
+// the same B tile, so a stage holds two A tiles (one per tile) and one B tile
+// and each k-block issues both tiles' MMAs.  Per k-block an SM then stores
+// 48 KB and its tensor core reads 64 KB for twice the MMA work: 112 KB of
+// shared-memory traffic per 1024 MMA cycles instead of 64 KB per 512, and a
+// third less TMA traffic per FLOP.  SUP = 2 (wide tiles): the same along N,
+// one A tile against the B tiles of two consecutive n-blocks, so each row
+// block reaches shared memory (or is gathered) once per two n-blocks.  Either
+// way the two accumulators fill the 512 TMEM columns, so the epilogue of one
+// tile does not overlap the next one's MMAs.
 template <int BN, bool PAIR, int EPI, int SUP = 0>
 struct GemmCfg {
   static constexpr int BM = 128, BK = 64;
