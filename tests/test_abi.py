@@ -82,6 +82,16 @@ def test_invalid_shapes_rejected(lib, T, d, n, E, k):
     assert lib.moe_forward(ctypes.byref(s), p, p, None, p, p, p, p, 1 << 40, None) == B.MOE_ERR_INVALID
 
 
+def test_forward_a_path_policy(lib):
+    """moe_forward gathers rows in the up GEMM's operand load (path 2, wide
+    tiles) exactly where the up GEMM has two 256-wide n-blocks (n = 256), else
+    it stages them (path 0); an invalid shape gets -1."""
+    assert B.moe_forward_a_path(B.make_shape(32768, 1536, 256, 128, 8)) == 2
+    for n in (64, 128, 384, 1024, 2048, 14336):
+        assert B.moe_forward_a_path(B.make_shape(1024, 512, n, 16, 2)) == 0
+    assert B.moe_forward_a_path(B.make_shape(1024, 500, 256, 16, 2)) == -1  # d % 64 != 0
+
+
 def test_null_and_misaligned_pointers_rejected(lib):
     s = B.make_shape(256, 128, 64, 8, 2)
     p = ctypes.c_void_p(4096)
