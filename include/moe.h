@@ -275,6 +275,12 @@ int moe_expert_down(const moe_shape* s, const void* h, const void* W2p, const in
 int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets,
                 const int32_t* tok_rows, void* y, void* stream);
 
+/* The same combine with y bf16 [T, d], the layer's output in a bf16 model:
+ * each element is moe_combine's fp32 sum rounded to nearest-even bf16.
+ * Arguments, ownership and errors as moe_combine. */
+int moe_combine_bf16(const moe_shape* s, const void* ys, const int32_t* tok_offsets,
+                     const int32_t* tok_rows, void* y, void* stream);
+
 /* The A-operand path (the `gather` argument of moe_expert_up) that
  * moe_forward uses for this shape: 2 (rows gathered into the operand load by
  * cp.async, with wide tiles that put both 256-wide n-blocks against each
@@ -289,6 +295,16 @@ int moe_forward_a_path(const moe_shape* s);
 int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias,
                 const void* W13p, const void* W2p, void* y, void* ws, size_t ws_bytes,
                 void* stream);
+
+/* moe_forward with y bf16 [T, d] out (moe_combine_bf16 as its last step):
+ * each element is moe_forward's fp32 y rounded to nearest-even bf16, with
+ * half the bytes written and copied out.  That rounding adds up to 2^-8 of
+ * |y|: on outputs beyond about 5 rms it can take the error past the layer's
+ * max-error tolerance (2e-2 rms), which the fp32 y meets.  Everything else
+ * as moe_forward. */
+int moe_forward_bf16(const moe_shape* s, const void* x, const float* Wr, const float* bias,
+                     const void* W13p, const void* W2p, void* y, void* ws, size_t ws_bytes,
+                     void* stream);
 
 /* Byte offsets into the moe_forward workspace of its intermediate arrays, so
  * a caller can inspect them after a forward (all -1 for an invalid shape):

@@ -75,7 +75,9 @@ _SIGNATURES = {
     "moe_expert_up": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _SZ, _P]),
     "moe_expert_down": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_SHP, _P, _P, _P, _P, _P]),
+    "moe_combine_bf16": (_I, [_SHP, _P, _P, _P, _P, _P]),
     "moe_forward": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_bf16": (_I, [_SHP, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_a_path": (_I, [_SHP]),
     "moe_workspace_layout": (_I, [_SHP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
     "moe_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
@@ -128,6 +130,17 @@ def _stream(device=None) -> ctypes.c_void_p:
 def _check(status: int, where: str):
     if status != MOE_OK:
         raise MoEError(status, where)
+
+
+def _out(y, shape: moe_shape, dtype, device):
+    """The [T, d] output buffer: a new one, or the caller's after checking its
+    shape and dtype (the kernels write T*d elements of that dtype)."""
+    if y is None:
+        return torch.empty(shape.T, shape.d, dtype=dtype, device=device)
+    if y.dtype != dtype or tuple(y.shape) != (shape.T, shape.d):
+        raise ValueError(f"y must be {dtype} of shape ({shape.T}, {shape.d}), not {y.dtype} {tuple(y.shape)}")
+    _need_cuda(y)
+    return y
 
 
 def _need_cuda(*ts):
@@ -389,10 +402,18 @@ def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Worksp
 
 def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
     _need_cuda(ys, tok_offsets, tok_rows)
-    if y is None:
-        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=ys.device)
+    y = _out(y, shape, torch.float32, ys.device)
     _check(lib().moe_combine(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
                              _stream(ys.device)), "moe_combine")
+    return y
+
+
+def moe_combine_bf16(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
+    """moe_combine with y bf16: the fp32 sum rounded to nearest-even."""
+    _need_cuda(ys, tok_offsets, tok_rows)
+    y = _out(y, shape, torch.bfloat16, ys.device)
+    _check(lib().moe_combine_bf16(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
+                                  _stream(ys.device)), "moe_combine_bf16")
     return y
 
 
@@ -403,10 +424,18 @@ def moe_forward_a_path(shape: moe_shape) -> int:
 
 def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
     _need_cuda(x, Wr, bias, W13p, W2p)
-    if y is None:
-        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=x.device)
+    y = _out(y, shape, torch.float32, x.device)
     _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p), _ptr(y),
                              ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward")
+    return y
+
+
+def moe_forward_bf16(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
+    """moe_forward with y bf16: its fp32 y rounded to nearest-even."""
+    _need_cuda(x, Wr, bias, W13p, W2p)
+    y = _out(y, shape, torch.bfloat16, x.device)
+    _check(lib().moe_forward_bf16(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p),
+                                  _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward_bf16")
     return y
 
 
@@ -471,9 +500,14 @@ class MoELayer:
             self._ws[key] = Workspace(self.shape(T), device)
         return self._ws[key]
 
-    def forward(self, x, y=None):
+    def forward(self, x, y=None, out_dtype=torch.float32):
+        """y = the layer applied to x, in fp32 or (out_dtype bf16) rounded to bf16."""
         T = x.shape[0]
         ws = self.workspace(T, x.device)
+        if out_dtype == torch.bfloat16:
+            return moe_forward_bf16(self.shape(T), x, self.Wr, self.bias, self.W13p, self.W2p, ws, y)
+        if out_dtype != torch.float32:
+            raise ValueError(f"out_dtype must be torch.float32 or torch.bfloat16, not {out_dtype}")
         return moe_forward(self.shape(T), x, self.Wr, self.bias, self.W13p, self.W2p, ws, y)
 
     __call__ = forward

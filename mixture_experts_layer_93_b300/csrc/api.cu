@@ -369,8 +369,20 @@ int moe_combine(const moe_shape* s, const void* ys, const int32_t* tok_offsets, 
   return last_launch();
 }
 
-int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
-                const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
+int moe_combine_bf16(const moe_shape* s, const void* ys, const int32_t* tok_offsets, const int32_t* tok_rows,
+                     void* y, void* stream) {
+  if (!shape_ok(s) || !ys || !tok_rows || !y || !aligned16(ys) || !aligned16(y)) return MOE_ERR_INVALID;
+  launch_combine(static_cast<const __half*>(ys), tok_offsets, tok_rows, static_cast<__nv_bfloat16*>(y), s->T, s->d,
+                 s->k, as_stream(stream));
+  return last_launch();
+}
+
+namespace {
+
+// The bf16 layer: route (+ round) + permute, up, down, then the combine into
+// y in fp32 or bf16.
+int forward_bf16_layer(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                       const void* W2p, void* y, bool y_bf16, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !x || !Wr || !W13p || !W2p || !y) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(W13p) || !aligned16(W2p) || !aligned16(y)) return MOE_ERR_INVALID;
   int st = check_ws(s, ws, ws_bytes);
@@ -409,7 +421,20 @@ int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float*
                           forward_gather(s), ws, ws_bytes, stream)) != MOE_OK)
     return st;
   if ((st = moe_expert_down(s, h, W2p, counts, offsets, row_w, ys, ws, ws_bytes, stream)) != MOE_OK) return st;
-  return moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
+  return y_bf16 ? moe_combine_bf16(s, ys, combine_offsets, combine_rows, y, stream)
+                : moe_combine(s, ys, combine_offsets, combine_rows, y, stream);
+}
+
+}  // namespace
+
+int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
+  return forward_bf16_layer(s, x, Wr, bias, W13p, W2p, y, false, ws, ws_bytes, stream);
+}
+
+int moe_forward_bf16(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                     const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
+  return forward_bf16_layer(s, x, Wr, bias, W13p, W2p, y, true, ws, ws_bytes, stream);
 }
 
 int moe_quantize_rows_fp8(const void* src, int64_t rows, int32_t K, void* codes, float* scales, void* stream) {

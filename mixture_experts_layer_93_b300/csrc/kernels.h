@@ -121,6 +121,9 @@ int launch_router_tc(const __nv_bfloat16* x, const __nv_bfloat16* Wr3, const flo
 // combine.cu
 void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, float* y, int T, int d,
                     int k, cudaStream_t stream);
+// the same sum rounded to nearest-even bf16
+void launch_combine(const __half* ys, const int32_t* tok_offsets, const int32_t* tok_rows, __nv_bfloat16* y, int T,
+                    int d, int k, cudaStream_t stream);
 
 // prepare.cu
 void launch_prepare_weights(const __nv_bfloat16* W1, const __nv_bfloat16* W3, const __nv_bfloat16* W2,

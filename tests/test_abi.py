@@ -101,6 +101,10 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert lib.moe_forward(ctypes.byref(s), odd, p, None, p, p, p, p, big, None) == B.MOE_ERR_INVALID
     assert lib.moe_permute(ctypes.byref(s), None, None, p, p, p, p, p, None, p, big, None) == B.MOE_ERR_INVALID
     assert lib.moe_combine(ctypes.byref(s), p, None, None, p, None) == B.MOE_ERR_INVALID
+    assert lib.moe_forward_bf16(ctypes.byref(s), None, p, None, p, p, p, p, big, None) == B.MOE_ERR_INVALID
+    assert lib.moe_forward_bf16(ctypes.byref(s), p, p, None, p, p, odd, p, big, None) == B.MOE_ERR_INVALID
+    assert lib.moe_combine_bf16(ctypes.byref(s), p, None, None, p, None) == B.MOE_ERR_INVALID
+    assert lib.moe_combine_bf16(ctypes.byref(s), p, None, p, odd, None) == B.MOE_ERR_INVALID
     assert lib.moe_prepare_weights(ctypes.byref(s), p, p, None, p, p, None) == B.MOE_ERR_INVALID
     assert lib.moe_check_device_status(None, None, None) == B.MOE_ERR_INVALID
 
@@ -110,6 +114,7 @@ def test_small_workspace_rejected(lib):
     need = B.moe_workspace_bytes(s)
     p = ctypes.c_void_p(4096)
     assert lib.moe_forward(ctypes.byref(s), p, p, None, p, p, p, p, need - 1, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_forward_bf16(ctypes.byref(s), p, p, None, p, p, p, p, need - 1, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_permute(ctypes.byref(s), p, None, p, p, p, p, p, None, p, need - 256, None) == B.MOE_ERR_WORKSPACE
 
 
@@ -127,6 +132,21 @@ def test_product_refuses_cpu_tensors():
     Wr = torch.zeros(64, 4)
     with pytest.raises(ValueError, match="CUDA"):
         B.moe_router_logits(x, Wr, None, None)
+
+
+def test_output_buffers_are_checked():
+    # the kernels write T*d elements of the entry point's output dtype, so a
+    # caller's y of another dtype or shape is refused before any launch
+    import torch
+    s = B.make_shape(4, 64, 64, 8, 2)
+    with pytest.raises(ValueError, match="bfloat16"):
+        B._out(torch.zeros(4, 64), s, torch.bfloat16, "cpu")
+    with pytest.raises(ValueError, match="float32"):
+        B._out(torch.zeros(4, 64, dtype=torch.bfloat16), s, torch.float32, "cpu")
+    with pytest.raises(ValueError, match="shape"):
+        B._out(torch.zeros(4, 32), s, torch.float32, "cpu")
+    with pytest.raises(ValueError, match="CUDA"):
+        B._out(torch.zeros(4, 64), s, torch.float32, "cpu")
 
 
 def test_backward_workspace_and_host_checks(lib):
