@@ -132,15 +132,16 @@ def _check(status: int, where: str):
         raise MoEError(status, where)
 
 
-def _out(y, shape: moe_shape, dtype, device):
-    """The [T, d] output buffer: a new one, or the caller's after checking its
-    shape and dtype (the kernels write T*d elements of that dtype)."""
-    if y is None:
-        return torch.empty(shape.T, shape.d, dtype=dtype, device=device)
-    if y.dtype != dtype or tuple(y.shape) != (shape.T, shape.d):
-        raise ValueError(f"y must be {dtype} of shape ({shape.T}, {shape.d}), not {y.dtype} {tuple(y.shape)}")
-    _need_cuda(y)
-    return y
+def _buf(t, dims, dtype, device, what: str):
+    """An output buffer: a new one, or the caller's after checking its shape
+    and dtype (the kernels write every element of `dims` in that dtype)."""
+    dims = tuple(int(v) for v in dims)
+    if t is None:
+        return torch.empty(dims, dtype=dtype, device=device)
+    if t.dtype != dtype or tuple(t.shape) != dims:
+        raise ValueError(f"{what} must be {dtype} of shape {dims}, not {t.dtype} {tuple(t.shape)}")
+    _need_cuda(t)
+    return t
 
 
 def _need_cuda(*ts):
@@ -313,8 +314,7 @@ def moe_quantize_rows_fp8(src):
 def moe_expert_up_fp8(shape: moe_shape, x, W13q, sW13, counts, offsets, tok_rows, ws: Workspace,
                       tok_offsets=None, h=None):
     _need_cuda(x, W13q, sW13, counts, offsets, tok_rows, tok_offsets)
-    if h is None:
-        h = torch.empty(moe_row_capacity(shape), shape.n, dtype=torch.bfloat16, device=x.device)
+    h = _buf(h, (moe_row_capacity(shape), shape.n), torch.bfloat16, x.device, "h")
     _check(lib().moe_expert_up_fp8(ctypes.byref(shape), _ptr(x), _ptr(W13q), _ptr(sW13), _ptr(counts),
                                    _ptr(offsets), _ptr(tok_offsets), _ptr(tok_rows), _ptr(h), ws.ptr, ws.nbytes,
                                    _stream(x.device)), "moe_expert_up_fp8")
@@ -341,8 +341,7 @@ def moe_workspace_bytes_fp8(shape: moe_shape) -> int:
 
 def moe_expert_down_fp8(shape: moe_shape, h, W2q, sW2, counts, offsets, row_w, ws: Workspace, ys=None):
     _need_cuda(h, W2q, sW2, counts, offsets, row_w)
-    if ys is None:
-        ys = torch.empty(moe_row_capacity(shape), shape.d, dtype=torch.float16, device=h.device)
+    ys = _buf(ys, (moe_row_capacity(shape), shape.d), torch.float16, h.device, "ys")
     _check(lib().moe_expert_down_fp8(ctypes.byref(shape), _ptr(h), _ptr(W2q), _ptr(sW2), _ptr(counts), _ptr(offsets),
                                      _ptr(row_w), _ptr(ys), ws.ptr, ws.nbytes, _stream(h.device)),
            "moe_expert_down_fp8")
@@ -351,8 +350,7 @@ def moe_expert_down_fp8(shape: moe_shape, h, W2q, sW2, counts, offsets, row_w, w
 
 def moe_forward_fp8(shape: moe_shape, x, Wr, bias, W13q, sW13, W2q, sW2, ws: Workspace, y=None):
     _need_cuda(x, Wr, bias, W13q, sW13, W2q, sW2)
-    if y is None:
-        y = torch.empty(shape.T, shape.d, dtype=torch.float32, device=x.device)
+    y = _buf(y, (shape.T, shape.d), torch.float32, x.device, "y")
     _check(lib().moe_forward_fp8(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13q), _ptr(sW13),
                                  _ptr(W2q), _ptr(sW2), _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)),
            "moe_forward_fp8")
@@ -381,9 +379,7 @@ def moe_token_round(shape: moe_shape, logits, topk_idx, ws: Workspace) -> dict:
 def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Workspace, gather: int = 2,
                   h=None, tok_offsets=None, tok_rows=None):
     _need_cuda(x, W13p, counts, offsets, row_token, tok_offsets, tok_rows)
-    cap = moe_row_capacity(shape)
-    if h is None:
-        h = torch.empty(cap, shape.n, dtype=torch.bfloat16, device=x.device)
+    h = _buf(h, (moe_row_capacity(shape), shape.n), torch.bfloat16, x.device, "h")
     _check(lib().moe_expert_up(ctypes.byref(shape), _ptr(x), _ptr(W13p), _ptr(counts), _ptr(offsets),
                                _ptr(row_token), _ptr(tok_offsets), _ptr(tok_rows), _ptr(h), int(gather), ws.ptr,
                                ws.nbytes, _stream(x.device)), "moe_expert_up")
@@ -392,9 +388,7 @@ def moe_expert_up(shape: moe_shape, x, W13p, counts, offsets, row_token, ws: Wor
 
 def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Workspace, ys=None):
     _need_cuda(h, W2p, counts, offsets, row_w)
-    cap = moe_row_capacity(shape)
-    if ys is None:
-        ys = torch.empty(cap, shape.d, dtype=torch.float16, device=h.device)
+    ys = _buf(ys, (moe_row_capacity(shape), shape.d), torch.float16, h.device, "ys")
     _check(lib().moe_expert_down(ctypes.byref(shape), _ptr(h), _ptr(W2p), _ptr(counts), _ptr(offsets),
                                  _ptr(row_w), _ptr(ys), ws.ptr, ws.nbytes, _stream(h.device)), "moe_expert_down")
     return ys
@@ -402,7 +396,7 @@ def moe_expert_down(shape: moe_shape, h, W2p, counts, offsets, row_w, ws: Worksp
 
 def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
     _need_cuda(ys, tok_offsets, tok_rows)
-    y = _out(y, shape, torch.float32, ys.device)
+    y = _buf(y, (shape.T, shape.d), torch.float32, ys.device, "y")
     _check(lib().moe_combine(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
                              _stream(ys.device)), "moe_combine")
     return y
@@ -411,7 +405,7 @@ def moe_combine(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
 def moe_combine_bf16(shape: moe_shape, ys, tok_offsets, tok_rows, y=None):
     """moe_combine with y bf16: the fp32 sum rounded to nearest-even."""
     _need_cuda(ys, tok_offsets, tok_rows)
-    y = _out(y, shape, torch.bfloat16, ys.device)
+    y = _buf(y, (shape.T, shape.d), torch.bfloat16, ys.device, "y")
     _check(lib().moe_combine_bf16(ctypes.byref(shape), _ptr(ys), _ptr(tok_offsets), _ptr(tok_rows), _ptr(y),
                                   _stream(ys.device)), "moe_combine_bf16")
     return y
@@ -424,7 +418,7 @@ def moe_forward_a_path(shape: moe_shape) -> int:
 
 def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
     _need_cuda(x, Wr, bias, W13p, W2p)
-    y = _out(y, shape, torch.float32, x.device)
+    y = _buf(y, (shape.T, shape.d), torch.float32, x.device, "y")
     _check(lib().moe_forward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p), _ptr(y),
                              ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward")
     return y
@@ -433,7 +427,7 @@ def moe_forward(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None)
 def moe_forward_bf16(shape: moe_shape, x, Wr, bias, W13p, W2p, ws: Workspace, y=None):
     """moe_forward with y bf16: its fp32 y rounded to nearest-even."""
     _need_cuda(x, Wr, bias, W13p, W2p)
-    y = _out(y, shape, torch.bfloat16, x.device)
+    y = _buf(y, (shape.T, shape.d), torch.bfloat16, x.device, "y")
     _check(lib().moe_forward_bf16(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W2p),
                                   _ptr(y), ws.ptr, ws.nbytes, _stream(x.device)), "moe_forward_bf16")
     return y
@@ -460,13 +454,13 @@ def moe_backward(shape: moe_shape, x, Wr, bias, W13p, W13i, W2, dy, ws: Workspac
     _need_cuda(x, Wr, bias, W13p, W13i, W2, dy)
     dev = x.device
     T, d, n, E = shape.T, shape.d, shape.n, shape.E
-    if out is None:
-        out = {"dx": torch.empty(T, d, dtype=torch.float32, device=dev),
-               "dWr": torch.empty(d, E, dtype=torch.float32, device=dev),
-               "dbias": torch.empty(E, dtype=torch.float32, device=dev) if want_dbias else None,
-               "dW1": torch.empty(E, d, n, dtype=torch.float32, device=dev),
-               "dW3": torch.empty(E, d, n, dtype=torch.float32, device=dev),
-               "dW2": torch.empty(E, n, d, dtype=torch.float32, device=dev)}
+    # the caller's buffers (checked), or new ones; dbias is skipped when the
+    # caller's dict holds None for it, or has no entry and want_dbias is off
+    given = out or {}
+    dims = {"dx": (T, d), "dWr": (d, E), "dbias": (E,), "dW1": (E, d, n), "dW3": (E, d, n), "dW2": (E, n, d)}
+    skip_dbias = given["dbias"] is None if "dbias" in given else not want_dbias
+    out = {key: None if key == "dbias" and skip_dbias else _buf(given.get(key), dims[key], torch.float32, dev, key)
+           for key in dims}
     _check(lib().moe_backward(ctypes.byref(shape), _ptr(x), _ptr(Wr), _ptr(bias), _ptr(W13p), _ptr(W13i), _ptr(W2),
                               _ptr(dy), _ptr(out["dx"]), _ptr(out["dWr"]), _ptr(out.get("dbias")), _ptr(out["dW1"]),
                               _ptr(out["dW3"]), _ptr(out["dW2"]), ws.ptr, ws.nbytes, _stream(dev)), "moe_backward")

@@ -138,15 +138,17 @@ def test_output_buffers_are_checked():
     # the kernels write T*d elements of the entry point's output dtype, so a
     # caller's y of another dtype or shape is refused before any launch
     import torch
-    s = B.make_shape(4, 64, 64, 8, 2)
     with pytest.raises(ValueError, match="bfloat16"):
-        B._out(torch.zeros(4, 64), s, torch.bfloat16, "cpu")
+        B._buf(torch.zeros(4, 64), (4, 64), torch.bfloat16, "cpu", "y")
     with pytest.raises(ValueError, match="float32"):
-        B._out(torch.zeros(4, 64, dtype=torch.bfloat16), s, torch.float32, "cpu")
+        B._buf(torch.zeros(4, 64, dtype=torch.bfloat16), (4, 64), torch.float32, "cpu", "y")
     with pytest.raises(ValueError, match="shape"):
-        B._out(torch.zeros(4, 32), s, torch.float32, "cpu")
+        B._buf(torch.zeros(4, 32), (4, 64), torch.float32, "cpu", "y")
     with pytest.raises(ValueError, match="CUDA"):
-        B._out(torch.zeros(4, 64), s, torch.float32, "cpu")
+        B._buf(torch.zeros(4, 64), (4, 64), torch.float32, "cpu", "y")
+    assert B._buf(None, (3, 5), torch.float16, "cpu", "ys").shape == (3, 5)
+    with pytest.raises(ValueError, match="dW2"):
+        B._buf(torch.zeros(8, 64, 64, dtype=torch.bfloat16), (8, 64, 64), torch.float32, "cpu", "dW2")
 
 
 def test_backward_workspace_and_host_checks(lib):
