@@ -379,10 +379,10 @@ int moe_combine_bf16(const moe_shape* s, const void* ys, const int32_t* tok_offs
 
 namespace {
 
-// The bf16 layer: route (+ round) + permute, up, down, then the combine into
-// y in fp32 or bf16.
-int forward_bf16_layer(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
-                       const void* W2p, void* y, bool y_bf16, void* ws, size_t ws_bytes, void* stream) {
+// The layer with bf16 expert GEMMs: route (+ round) + permute, up, down,
+// then the combine into y in fp32 or, with y_bf16, rounded to bf16.
+int forward_layer(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
+                  const void* W2p, void* y, bool y_bf16, void* ws, size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !x || !Wr || !W13p || !W2p || !y) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(W13p) || !aligned16(W2p) || !aligned16(y)) return MOE_ERR_INVALID;
   int st = check_ws(s, ws, ws_bytes);
@@ -429,12 +429,12 @@ int forward_bf16_layer(const moe_shape* s, const void* x, const float* Wr, const
 
 int moe_forward(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
                 const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
-  return forward_bf16_layer(s, x, Wr, bias, W13p, W2p, y, false, ws, ws_bytes, stream);
+  return forward_layer(s, x, Wr, bias, W13p, W2p, y, false, ws, ws_bytes, stream);
 }
 
 int moe_forward_bf16(const moe_shape* s, const void* x, const float* Wr, const float* bias, const void* W13p,
                      const void* W2p, void* y, void* ws, size_t ws_bytes, void* stream) {
-  return forward_bf16_layer(s, x, Wr, bias, W13p, W2p, y, true, ws, ws_bytes, stream);
+  return forward_layer(s, x, Wr, bias, W13p, W2p, y, true, ws, ws_bytes, stream);
 }
 
 int moe_quantize_rows_fp8(const void* src, int64_t rows, int32_t K, void* codes, float* scales, void* stream) {
