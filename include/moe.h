@@ -15,7 +15,8 @@
  *   y[t]   = sum over t's rows of ys[r], fixed order    combine            (moe_combine)
  *
  * Precision: x, the expert weights and h are bf16; every product accumulates
- * in fp32 (tensor memory); ys is stored as fp16 and y is fp32.
+ * in fp32 (tensor memory); ys is stored as fp16 and y is fp32
+ * (moe_combine_bf16 / moe_forward_bf16 round it to bf16).
  *
  * Also here: e4m3 variants of the two expert GEMMs (the FP8 block below) and
  * the layer's backward pass by recomputation (moe_backward, at the end).
